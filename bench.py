@@ -1,0 +1,528 @@
+"""Benchmark: sparse verification attention on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+incremental representative build for the newest full block of every
+sequence, block scoring, budgeted top-k selection, split-KV sparse attention
+and the log-sum-exp merge (for a multi-layer stack: every layer, with the
+selection recomputed on computing layers and reused on the others).
+
+Prints ONE JSON line (rank 0). Timing: W warm-up steps, then exactly K steps
+replayed from CUDA graphs, bracketed by a barrier and a device synchronize on
+both sides, CUDA events on the launching stream, max over ranks. L2: the
+steps rotate over enough independent input sets that their working set is
+>= 4x the L2 size, so every step reads cold HBM.
+
+Roofline: the attention launch (selected-block gather + tensor-core
+attention + merge) is timed per launch with CUDA events on its stream over a
+second timed loop; algorithmic bytes per launch are the selected K/V pages,
+the draft K/V, Q and O.
+
+--impl reference runs the CPU oracle (the only reference this method has) on
+a bounded sample of the same workload and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_verification_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verify-attn draft tokens/s & achieved HBM GB/s (fraction of peak) at 32K-128K ctx"
+UNIT = "draft tokens/s"
+DEFAULT_WORKLOAD = "llama8b_128k_b4"
+
+
+# --------------------------------------------------------------- byte model
+def budget_k(wl: W.Workload) -> int:
+    from sparse_verification_attention_gb300 import api
+    return api.sv_budget_blocks(wl.budget, wl.ctx, wl.NB)
+
+
+def attend_bytes(wl: W.Workload, k: int) -> int:
+    """Algorithmic bytes of one attention launch (one layer)."""
+    e = wl.elt
+    sel_kv = wl.B * wl.Hkv * k * wl.blk * wl.d * e * 2
+    draft = wl.B * wl.T * wl.Hkv * wl.d * e * 2
+    q = o = wl.B * wl.T * wl.Hq * wl.d * e
+    return sel_kv + draft + q + o
+
+
+def layer_bytes(wl: W.Workload, k: int, computing: bool) -> int:
+    """Algorithmic bytes of one layer of the step: incremental rep build of
+    one block per sequence (read its keys, write its fp32 rep), the fp32
+    representative stream when the layer computes its selection, and the
+    attention launch."""
+    inc = wl.B * wl.Hkv * (wl.blk * wl.d * wl.elt + wl.d * 4)
+    reps = wl.B * wl.Hkv * wl.NB * wl.d * 4 if computing else 0
+    return inc + reps + attend_bytes(wl, k)
+
+
+def step_bytes(wl: W.Workload, k: int) -> int:
+    return sum(layer_bytes(wl, k, l % wl.compute_every == 0) for l in range(wl.layers))
+
+
+# --------------------------------------------------------------- helpers
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def attend_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attend_fast.cu", "attend_generic.cu", "ptx.h", "internal.h"):
+        with open(os.path.join(ROOT, "sparse_verification_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(wl_name: str):
+    """ncu DRAM bytes per attention launch recorded under profiles/, or None
+    when absent or taken on a different attention source."""
+    p = os.path.join(ROOT, "profiles", "attend_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(wl_name)
+    if not ent or ent.get("source_hash") != attend_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/sva_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 6:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[2:6]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        # harness-only collectives (barrier, max of timings) on CPU tensors;
+        # the data path has no collective
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- oracle arm
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: sequence 0 of layer
+    0, one (sequence, kv head) verification (score, budget, select, attend)
+    per unit, rotating over the kv heads; representatives prebuilt (prefill,
+    untimed). One unit is 1/(B*Hkv*layers) of a step, i.e. T/(Hkv*layers)
+    draft tokens' worth of verification."""
+
+    def __init__(self, wl: W.Workload, x_cpu=None):
+        from oracle import sva_oracle as O
+        self.O, self.wl = O, wl
+        if x_cpu is None:
+            x_cpu = W.make_layer(W.scaled(wl, layers=1) if wl.layers > 1 else wl, 0, device="cpu")
+        pages = x_cpu.block_table[0].long()
+        self.kp = x_cpu.k_pool[pages].contiguous()
+        self.vp = x_cpu.v_pool[pages].contiguous()
+        self.bt = torch.arange(wl.NB, dtype=torch.int32).view(1, -1)
+        self.q, self.dk, self.dv = x_cpu.q[:1], x_cpu.draft_k[:1], x_cpu.draft_v[:1]
+        self.reps = O.block_representatives(self.kp, self.bt, wl.NB, wl.blk)
+        self.i = 0
+
+    def unit(self):
+        wl, h = self.wl, self.i % self.wl.Hkv
+        self.i += 1
+        G = wl.G
+        self.O.verify_layer(self.q[:, :, h * G:(h + 1) * G], self.kp[:, h:h + 1],
+                            self.vp[:, h:h + 1], self.bt, self.dk[:, :, h:h + 1],
+                            self.dv[:, :, h:h + 1], wl.parent_list(), wl.ctx, wl.blk, wl.budget,
+                            reps=self.reps[:, h:h + 1])
+
+    def tokens_per_unit(self) -> float:
+        # a step is B*Hkv*layers such units for B*T draft tokens
+        return self.wl.T / (self.wl.Hkv * self.wl.layers)
+
+    def timed(self, seconds: float = 0.0, units: int = 0):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            self.unit()
+            n += 1
+            el = time.perf_counter() - t0
+            if (units and n >= units) or (not units and el >= seconds):
+                break
+        return n, el
+
+    def describe(self, n, el) -> str:
+        return (f"{n} (sequence, kv head) verifications of sequence 0, layer 0 of {self.wl.name} "
+                f"(score {self.wl.NB} reps, budget, top-k, attend), {el:.1f} s of CPU time, "
+                f"fp64 PyTorch-CPU oracle")
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    o = OracleSample(wl)
+    o.timed(units=1)
+    t_unit = o.timed(units=2)[1] / 2
+    # size each step so that warm-up + K steps stay within about two minutes
+    per_step = max(1, min(wl.Hkv, int(120.0 / max(1, args.steps + args.warmup) / t_unit)))
+    o.timed(units=per_step * args.warmup)
+    n, el = o.timed(units=per_step * args.steps)
+    tok_s = n * o.tokens_per_unit() / el
+    desc = o.describe(n, el) + f"; {per_step} per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(wl, None),
+        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": torch.get_num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": tok_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl: W.Workload, k):
+    return {"workload": f"{wl.name}: {wl.description}", "B": wl.B, "ctx": wl.ctx, "T": wl.T,
+            "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "blk": wl.blk, "layers": wl.layers,
+            "budget_blocks": k, "draft_mask": "chain" if wl.parents is None else
+            "tree " + ",".join(map(str, wl.parents)), "parallelism": "replicas (1 GPU each)"}
+
+
+# --------------------------------------------------------------- GPU arm
+class StepSet:
+    """One independent input set resident in HBM (one per layer of a stack)."""
+
+    def __init__(self, wl, index, layers_planted):
+        from sparse_verification_attention_gb300 import api
+        self.layers = []
+        for l in range(wl.layers):
+            x = W.make_layer(wl, index * wl.layers + l, device="cuda",
+                             planted=layers_planted[l])
+            self.layers.append(api.LayerState(wl, x))
+        # reuse layers share the computing layer's selection buffer
+        for l in range(wl.layers):
+            if l % wl.compute_every:
+                self.layers[l].sel = self.layers[l - (l % wl.compute_every)].sel
+
+
+def run_step(wl, ss: StepSet, ev=None):
+    """Launch one step on the current stream (graph-capturable)."""
+    from sparse_verification_attention_gb300 import api
+    nb = wl.NB
+    for l, st in enumerate(ss.layers):
+        computing = l % wl.compute_every == 0
+        if nb:
+            api.sv_build_reps(st.shape, st.kv, nb - 1, 1, st.reps)
+        if computing:
+            api.sv_score_select(st.shape, st.x.q, st.reps, st.kv, wl.budget, st.sel, st.kmax,
+                                st.ws)
+        if ev is not None:
+            ev[0].record()
+        api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
+                             st.x.draft_v, st.parents, st.out, st.ws)
+        if ev is not None:
+            ev[1].record()
+
+
+def run_gpu(args, wl, rank, world, dist):
+    from sparse_verification_attention_gb300 import api, build_lib
+    build_lib.build()
+    dev = args.local_rank
+    torch.cuda.set_device(dev)
+    k = budget_k(wl)
+    sbytes = step_bytes(wl, k)
+    abytes = attend_bytes(wl, k)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 129 * 2 ** 20)
+    n_sets = max(2, math.ceil(4 * l2 / sbytes))
+    if args.sets:
+        n_sets = args.sets
+    ps = W.planted_sets(wl)
+    sets = [StepSet(wl, i, ps) for i in range(n_sets)]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    # one CUDA graph per input set, each holding one whole step
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for ss in sets:  # warm the launch paths once outside capture
+            run_step(wl, ss)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    for ss in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run_step(wl, ss)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for s in sets:
+        for st in s.layers:
+            flags = api.sv_read_status(st.ws)
+            if flags:
+                raise RuntimeError(f"device status flags {flags:#x}")
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    for i in range(args.warmup):
+        graphs[i % n_sets].replay()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        graphs[i % n_sets].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms_total = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(dist, ms_total)
+    ms_step = ms_total / args.steps
+    tokens = sum_over_ranks(dist, wl.B * wl.T * args.steps)
+    value = tokens / (ms_total / 1e3)
+
+    # roofline: per-launch events around the attention call, eager, cold L2
+    n_launch = max(10, min(args.steps, 200))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_launch)]
+    for i in range(n_launch):
+        ss = sets[i % n_sets]
+        st = ss.layers[(i // n_sets) % wl.layers]
+        evs[i][0].record()
+        api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
+                             st.x.draft_v, st.parents, st.out, st.ws)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    durs = sorted(a.elapsed_time(b) for a, b in evs)
+    attend_ms = sum(durs) / len(durs)
+    peak, peak_kind = read_peaks()
+    achieved = abytes / (attend_ms / 1e3) / 1e9
+
+    # dense full-KV verification (same kernels, every block) for comparison
+    st0 = sets[0].layers[0]
+    dense = None
+    if args.dense and wl.NB:
+        dws = api.alloc_workspace(st0.shape, wl.NB, wl.NB)
+        dout = torch.empty_like(st0.out)
+        de = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(5)]
+        api.sv_sparse_attend(st0.shape, st0.x.q, st0.kv, None, 0, 0, st0.x.draft_k,
+                             st0.x.draft_v, st0.parents, dout, dws)
+        for a, b in de:
+            a.record()
+            api.sv_sparse_attend(st0.shape, st0.x.q, st0.kv, None, 0, 0, st0.x.draft_k,
+                                 st0.x.draft_v, st0.parents, dout, dws)
+            b.record()
+        torch.cuda.synchronize()
+        dms = statistics.median(a.elapsed_time(b) for a, b in de)
+        dbytes = attend_bytes(wl, wl.NB)
+        dense = {"attend_ms": dms, "gbs": dbytes / (dms / 1e3) / 1e9,
+                 "sparse_speedup": dms / attend_ms, "note": "same kernels, all blocks kept"}
+
+    # e2e: the public call with host buffers, copies inside the timed region
+    e2e = run_e2e(args, wl, sets, dist)
+
+    # CPU oracle baseline on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        o = OracleSample(wl, sets[0].layers[0].x.to("cpu"))
+        n, el = o.timed(seconds=args.cpu_seconds)
+        cpu = {"value": n * o.tokens_per_unit() / el, "unit": UNIT,
+               "cores": torch.get_num_threads(), "kind": "oracle", "sample": o.describe(n, el)}
+
+    traffic = traffic_from_profile(wl.name)
+    launches_per_step = sum(1 + (1 if l % wl.compute_every == 0 else 0) * 2 + 2
+                            for l in range(wl.layers))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded Gaussian Q/K/V, planted high-affinity blocks + sink)",
+        "config": dict(config_of(wl, k), l2=(
+            f"rotating {n_sets} input sets, {n_sets * sbytes / 1e6:.0f} MB touched per "
+            f"rotation vs {l2 / 1e6:.0f} MB L2 (inputs larger than L2, no flush)")),
+        "step_bytes": sbytes, "step_gbs": sbytes / (ms_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "sv_sparse_attend (split-KV attend + LSE merge)",
+                     "bytes_per_launch": abytes, "launch_ms": attend_ms,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+                     "frac_of_nominal_8tbs": achieved / 8000.0},
+        "dense": dense,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, sets, dist):
+    """sv_build_reps + sv_verify_layer per layer through the public call, with
+    each step's per-token inputs (Q, draft K, draft V) copied in from pinned
+    host memory and the output copied back, inside the timed region. Steps
+    rotate over the same input sets as the device-timed loop."""
+    from sparse_verification_attention_gb300 import api
+    host = []
+    for ss in sets:
+        host.append([(st.x.q.cpu().pin_memory(), st.x.draft_k.cpu().pin_memory(),
+                      st.x.draft_v.cpu().pin_memory(),
+                      torch.empty_like(st.out, device="cpu").pin_memory()) for st in ss.layers])
+    h2d = sum(t.numel() * t.element_size() for hq, hk, hv, _ in host[0] for t in (hq, hk, hv))
+    d2h = sum(ho.numel() * ho.element_size() for *_, ho in host[0])
+    nb = wl.NB
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one(i):
+        ss, hb = sets[i % len(sets)], host[i % len(sets)]
+        for l, st in enumerate(ss.layers):
+            hq, hk, hv, ho = hb[l]
+            st.x.q.copy_(hq, non_blocking=True)
+            st.x.draft_k.copy_(hk, non_blocking=True)
+            st.x.draft_v.copy_(hv, non_blocking=True)
+            if nb:
+                api.sv_build_reps(st.shape, st.kv, nb - 1, 1, st.reps)
+            reuse = int(l % wl.compute_every != 0)
+            api.sv_verify_layer(st.shape, st.x.q, st.kv, st.reps, wl.budget, st.x.draft_k,
+                                st.x.draft_v, st.parents, reuse, st.sel, st.kmax, st.out, st.ws)
+            ho.copy_(st.out, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    tokens = sum_over_ranks(dist, wl.B * wl.T * steps)
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "note": "eager public calls (sv_build_reps + sv_verify_layer), rotating input sets"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--sets", type=int, default=0)
+    ap.add_argument("--dense", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    args.local_rank = local
+    wl = W.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    dist = init_dist(world)
+    try:
+        run_gpu(args, wl, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

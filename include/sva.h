@@ -1,0 +1,211 @@
+/*
+ * sva.h -- C ABI of the sparse verification attention library (libsva.so).
+ *
+ * The method: a target LLM verifying T draft tokens against a long, paged KV
+ * cache keeps only a budgeted set of KV blocks. Each block has a
+ * representative; the first draft token's query is dotted with every
+ * representative; a piecewise budget fixes how many top-scoring blocks are
+ * kept; all T drafts attend to that ONE shared set plus the drafts the mask
+ * lets them see; adjacent layers may reuse a previous layer's selection.
+ *
+ * Sources, cited by page title and part of the page:
+ *   [SV-Fig1] "Accelerate Speculative Decoding with Sparse Computation in
+ *             Verification" (paper summary page), Figure 1 caption.
+ *   [SV-Abs]  same page, Abstract (inter-draft and inter-layer reuse).
+ *   [SV-Tut1] same title, tutorial page, section "core technique 1" on sparse
+ *             attention for multiple tokens: importance-based block choice,
+ *             piecewise budget control, inter-layer retrieval reuse.
+ *   [SpecPV]  "SpecPV: Improving self-speculative decoding for long-context
+ *             generation via partial verification", introduction (full
+ *             verification as the baseline).
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is caller-owned DEVICE memory unless the argument
+ *     says "host". The library never allocates device memory.
+ *   - Layouts are dense row-major (C order) with the shapes given.
+ *   - dtype SV_BF16: q, k/v pools, draft k/v and out are bf16;
+ *     SV_F32: all of them fp32. Representatives and scores are always fp32.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). The return value covers host-side validation and
+ *     launch errors only. Device-side index checks (a block-table entry or a
+ *     selected block out of range) skip the bad access and OR a flag into
+ *     the workspace status word; read it with sv_read_status().
+ *   - Validation happens before anything is launched: a call that returns
+ *     SV_ERR_INVALID_ARG or SV_ERR_UNSUPPORTED has launched nothing.
+ *   - Nothing throws across the ABI. sv_last_error() describes the last
+ *     non-OK status of the calling thread.
+ *   - Limits: 1 <= T <= 64; Hq % Hkv == 0; d % 8 == 0 and 8 <= d <= 256;
+ *     ctx % blk == 0 (every prefix block is full); NB = ctx/blk <= 16384.
+ */
+#ifndef SVA_H_
+#define SVA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_ABI_VERSION 1
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shape   */
+  SV_ERR_UNSUPPORTED = 2,   /* valid but outside the limits above           */
+  SV_ERR_WORKSPACE = 3,     /* workspace smaller than sv_workspace_bytes()  */
+  SV_ERR_CUDA = 4,          /* a CUDA runtime call failed                   */
+  SV_ERR_DEVICE_FAULT = 5   /* sv_read_status() found a device-side flag    */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
+
+/* Device-side status flags (OR-ed into the workspace status word). */
+#define SV_FLAG_BAD_BLOCK_INDEX 0x1u  /* selected block index outside [0, NB)  */
+#define SV_FLAG_BAD_PAGE 0x2u         /* block_table entry outside [0, pages)  */
+#define SV_FLAG_WAIT_TIMEOUT 0x4u     /* a pipeline wait gave up (never hangs) */
+
+/* Problem shape. Stacked query rows per KV head: R = T * (Hq / Hkv). */
+typedef struct {
+  int B;      /* sequences in the batch                                  */
+  int Hq;     /* query heads                                             */
+  int Hkv;    /* KV heads (grouped-query attention: G = Hq / Hkv)        */
+  int d;      /* head dimension                                          */
+  int blk;    /* tokens per KV block (page)                              */
+  int T;      /* draft tokens being verified                             */
+  int dtype;  /* sv_dtype                                                */
+} sv_shape;
+
+/* Piecewise budget control [SV-Tut1]. The pages give the shape of the rule
+ * (more blocks kept at short context, harder sparsification at long context)
+ * but no constants; the caller supplies them. */
+#define SV_BUDGET_FIXED 0
+#define SV_BUDGET_PIECEWISE 1
+typedef struct {
+  int mode;           /* SV_BUDGET_FIXED or SV_BUDGET_PIECEWISE            */
+  int fixed_blocks;   /* FIXED: k = min(NB, fixed_blocks)                  */
+  int short_ctx;      /* PIECEWISE: ctx <= short_ctx keeps all NB blocks   */
+  int floor_blocks;   /* otherwise k = min(NB, max(floor, ceil(frac*NB)))  */
+  double frac_mid;    /*   frac = frac_mid when ctx <= long_ctx            */
+  int long_ctx;
+  double frac_long;   /*   frac = frac_long when ctx > long_ctx            */
+} sv_budget;
+
+/* Paged KV cache, caller-owned device memory. Page p of head h holds blk
+ * consecutive tokens: k_pool[p][h][0..blk)[0..d). Every sequence has ctx
+ * prefix tokens in NB = ctx/blk full blocks; logical block j of sequence b
+ * lives in page block_table[b * nb_max + j]. Pool base addresses must be
+ * 16-byte aligned. */
+typedef struct {
+  const void* k_pool;       /* [num_pages, Hkv, blk, d]                    */
+  const void* v_pool;       /* [num_pages, Hkv, blk, d]                    */
+  const int32_t* block_table; /* [B, nb_max]                              */
+  int nb_max;               /* row stride of block_table, >= NB            */
+  int num_pages;
+  int ctx;                  /* prefix tokens per sequence (same for all)   */
+} sv_kv;
+
+/* ABI version (SV_ABI_VERSION of the built library). Host only. */
+int sv_abi_version(void);
+
+/* Thread-local description of the calling thread's last non-OK status. */
+const char* sv_last_error(void);
+
+/* Piecewise budget control [SV-Tut1]: number of blocks kept for a context of
+ * ctx tokens in nb blocks. Pure host function, no GPU needed. Returns -1 on
+ * an invalid budget (NULL, unknown mode, negative sizes, fractions outside
+ * [0, 1]). */
+int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
+
+/* Bytes of workspace that score/select/attend/verify calls with this shape
+ * need, for selections of up to kmax blocks over up to nb_max blocks. The
+ * first 256 bytes hold the device status word, which must be zero before the
+ * first call (allocate zeroed, or call sv_clear_status). Returns 0 on an
+ * invalid shape. Host only. */
+size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax);
+
+/* Zero the workspace status word (async on stream). */
+sv_status sv_clear_status(void* workspace, void* stream);
+
+/* Synchronously read the workspace status word into *flags (host). Returns
+ * SV_ERR_DEVICE_FAULT when any flag is set. */
+sv_status sv_read_status(const void* workspace, uint32_t* flags, void* stream);
+
+/* Block representatives [SV-Fig1] (mean of a block's keys; the pages do not
+ * define the representative, the mean is this library's reading):
+ *   reps[b][h][j][:] = (1/blk) * sum_t K[page(b,j)][h][t][:],  fp32,
+ * for logical blocks j in [first_block, first_block + n_blocks) of every
+ * sequence. reps: [B, Hkv, nb_max, d] fp32, written only at those j. Call it
+ * over all full blocks after prefill and again for each block that fills
+ * up. Requires first_block >= 0, n_blocks >= 0, first_block + n_blocks <=
+ * ctx/blk. */
+sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block,
+                        int n_blocks, float* reps, void* stream);
+
+/* Block importance scores [SV-Fig1]: for every sequence b, KV head h and
+ * block j < NB,
+ *   scores[b][h][j] = sum_{g<G} < Q[b][0][h*G+g][:], reps[b][h][j][:] >
+ * (draft 0's query; a KV head's score sums its G query heads' dot products;
+ * no 1/sqrt(d), which does not change the ranking).
+ * q: [B, T, Hq, d]; reps: [B, Hkv, nb_max, d]; scores: [B, Hkv, NB] fp32. */
+sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* reps,
+                          const sv_kv* kv, float* scores, void* stream);
+
+/* Top-k block selection [SV-Fig1], [SV-Tut1]: for every (b, h), the k
+ * highest of scores[b][h][0..nb), ties to the lower block index, written in
+ * ascending block order to sel[b][h][0..k); sel[b][h][k..kmax) = -1.
+ * scores: [B, Hkv, nb] fp32; sel: [B, Hkv, kmax] int32; 0 <= k <= kmax;
+ * k > nb keeps all nb blocks. Scores must be finite (NaN order undefined);
+ * -0.0 and +0.0 tie. */
+sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, int k,
+                           int32_t* sel, int kmax, void* stream);
+
+/* Score + budget + select in one call [SV-Fig1], [SV-Tut1]:
+ * k = sv_budget_blocks(budget, kv->ctx, NB); scores go to the workspace;
+ * sel as in sv_select_blocks; *k_out (host, may be NULL) receives k.
+ * SV_ERR_INVALID_ARG if k > kmax. */
+sv_status sv_score_select(const sv_shape* shape, const void* q, const float* reps,
+                          const sv_kv* kv, const sv_budget* budget, int32_t* sel,
+                          int kmax, int* k_out, void* workspace, size_t ws_bytes,
+                          void* stream);
+
+/* Sparse multi-token verification attention [SV-Fig1]: every draft row
+ * (t, query head qh, KV head h = qh / G) attends, with softmax scale
+ * 1/sqrt(d), to
+ *   - every token of the n_sel blocks sel[b][h][0..n_sel) (logical block
+ *     indices, the SAME set for all T drafts and all G heads of h), and
+ *   - the drafts u that t may see: u = t and the ancestors of t.
+ * draft_parent: HOST int[T] with draft_parent[0] = -1 and
+ * 0 <= draft_parent[t] < t for t > 0 (a tree); NULL = linear chain.
+ * sel == NULL selects all NB blocks in order: dense full verification
+ * attention [SpecPV], the comparison baseline (n_sel is then ignored).
+ * sel: [B, Hkv, sel_stride] int32 with n_sel <= sel_stride.
+ * q: [B, T, Hq, d]; draft_k, draft_v: [B, T, Hkv, d]; out: [B, T, Hq, d].
+ * The workspace holds the split-KV partial results (its size from
+ * sv_workspace_bytes with kmax >= n_sel, or >= NB when sel == NULL). */
+sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv,
+                           const int32_t* sel, int n_sel, int sel_stride,
+                           const void* draft_k, const void* draft_v,
+                           const int32_t* draft_parent, void* out, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/* One layer of sparse verification [SV-Fig1], [SV-Tut1], [SV-Abs]:
+ *   reuse == 0: sv_score_select into sel_cache, then sv_sparse_attend on it;
+ *   reuse == 1: inter-layer retrieval reuse -- no scoring or selection; the
+ *               selection already in sel_cache (written by an earlier
+ *               reuse == 0 call with the same shape, kv->ctx and budget) is
+ *               attended to as is.
+ * reps may be NULL when reuse == 1. sel_cache: [B, Hkv, kmax] int32, in/out.
+ * *k_out (host, may be NULL) receives the number of blocks attended. */
+sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
+                          const float* reps, const sv_budget* budget,
+                          const void* draft_k, const void* draft_v,
+                          const int32_t* draft_parent, int reuse, int32_t* sel_cache,
+                          int kmax, int* k_out, void* out, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVA_H_ */

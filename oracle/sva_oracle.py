@@ -107,7 +107,9 @@ def budget_blocks(ctx: int, nb: int, mode: int, fixed_blocks: int = 0,
         return min(nb, fixed_blocks)
     if ctx <= short_ctx:
         return nb                                # short context: keep everything
-    frac = Fraction(frac_mid) if ctx <= long_ctx else Fraction(frac_long)
+    # fractions are decimal percentages (12.5% = 0.125): ceil of the exact
+    # decimal product, not of its binary floating-point approximation
+    frac = Fraction(repr(frac_mid)) if ctx <= long_ctx else Fraction(repr(frac_long))
     want = math.ceil(frac * nb)
     return min(nb, max(floor_blocks, want))
 

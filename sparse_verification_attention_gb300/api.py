@@ -1,0 +1,247 @@
+"""Thin ctypes binding over libsva.so (include/sva.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. torch is used for device memory and streams; tensors are passed by
+data_ptr(), streams by their cudaStream_t handle. Any non-OK status raises
+SvError with the library's own message. There is no fallback: if libsva.so is
+missing or was built for another machine, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import workloads as W
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsva.so")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE, SV_ERR_CUDA, \
+    SV_ERR_DEVICE_FAULT = range(6)
+SV_BF16, SV_F32 = 0, 1
+SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
+
+EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
+            "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
+            "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_verify_layer")
+
+
+class SvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"sva status {status}: {msg}")
+        self.status = status
+
+
+class Shape(C.Structure):
+    _fields_ = [("B", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int), ("d", C.c_int),
+                ("blk", C.c_int), ("T", C.c_int), ("dtype", C.c_int)]
+
+
+class BudgetC(C.Structure):
+    _fields_ = [("mode", C.c_int), ("fixed_blocks", C.c_int), ("short_ctx", C.c_int),
+                ("floor_blocks", C.c_int), ("frac_mid", C.c_double), ("long_ctx", C.c_int),
+                ("frac_long", C.c_double)]
+
+
+class KV(C.Structure):
+    _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("block_table", C.c_void_p),
+                ("nb_max", C.c_int), ("num_pages", C.c_int), ("ctx", C.c_int)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libsva.so (once). Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "sparse_verification_attention_gb300.build_lib.build()")
+        L = C.CDLL(LIB_PATH)
+        vp, i, sz = C.c_void_p, C.c_int, C.c_size_t
+        sig = {
+            "sv_abi_version": (i, []),
+            "sv_last_error": (C.c_char_p, []),
+            "sv_budget_blocks": (i, [C.POINTER(BudgetC), i, i]),
+            "sv_workspace_bytes": (sz, [C.POINTER(Shape), i, i]),
+            "sv_clear_status": (i, [vp, vp]),
+            "sv_read_status": (i, [vp, C.POINTER(C.c_uint32), vp]),
+            "sv_build_reps": (i, [C.POINTER(Shape), C.POINTER(KV), i, i, vp, vp]),
+            "sv_score_blocks": (i, [C.POINTER(Shape), vp, vp, C.POINTER(KV), vp, vp]),
+            "sv_select_blocks": (i, [C.POINTER(Shape), vp, i, i, vp, i, vp]),
+            "sv_score_select": (i, [C.POINTER(Shape), vp, vp, C.POINTER(KV), C.POINTER(BudgetC),
+                                    vp, i, C.POINTER(C.c_int), vp, sz, vp]),
+            "sv_sparse_attend": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, i, i, vp, vp,
+                                     C.POINTER(C.c_int32), vp, vp, sz, vp]),
+            "sv_verify_layer": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, C.POINTER(BudgetC),
+                                    vp, vp, C.POINTER(C.c_int32), i, vp, i, C.POINTER(C.c_int),
+                                    vp, vp, sz, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != SV_OK:
+        raise SvError(status, lib().sv_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return SV_BF16
+    if t == torch.float32:
+        return SV_F32
+    raise ValueError(f"unsupported dtype {t}")
+
+
+def make_shape(B, Hq, Hkv, d, blk, T, dtype) -> Shape:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return Shape(B, Hq, Hkv, d, blk, T, code)
+
+
+def make_budget(b: W.Budget) -> BudgetC:
+    return BudgetC(b.mode, b.fixed_blocks, b.short_ctx, b.floor_blocks, b.frac_mid, b.long_ctx,
+                   b.frac_long)
+
+
+def make_kv(k_pool: torch.Tensor, v_pool: Optional[torch.Tensor], block_table: torch.Tensor,
+            ctx: int) -> KV:
+    return KV(k_pool.data_ptr(), None if v_pool is None else v_pool.data_ptr(),
+              block_table.data_ptr(), block_table.shape[1], k_pool.shape[0], ctx)
+
+
+def _parents(parents: Optional[Sequence[int]]):
+    if parents is None:
+        return None
+    arr = (C.c_int32 * len(parents))(*parents)
+    return arr
+
+
+# ------------------------------------------------------------------ calls
+def sv_abi_version() -> int:
+    return lib().sv_abi_version()
+
+
+def sv_budget_blocks(budget: W.Budget, ctx: int, nb: int) -> int:
+    b = make_budget(budget)
+    return lib().sv_budget_blocks(C.byref(b), ctx, nb)
+
+
+def sv_workspace_bytes(shape: Shape, nb_max: int, kmax: int) -> int:
+    return lib().sv_workspace_bytes(C.byref(shape), nb_max, kmax)
+
+
+def alloc_workspace(shape: Shape, nb_max: int, kmax: int, device="cuda") -> torch.Tensor:
+    n = sv_workspace_bytes(shape, nb_max, kmax)
+    if n == 0:
+        raise SvError(SV_ERR_INVALID_ARG, "invalid shape for a workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def sv_clear_status(ws: torch.Tensor, stream=None):
+    _check(lib().sv_clear_status(_ptr(ws), _stream(stream)))
+
+
+def sv_read_status(ws: torch.Tensor, stream=None) -> int:
+    """Device status flags (0 = clean). Does not raise on set flags."""
+    v = C.c_uint32(0)
+    lib().sv_read_status(_ptr(ws), C.byref(v), _stream(stream))
+    return int(v.value)
+
+
+def sv_build_reps(shape: Shape, kv: KV, first_block: int, n_blocks: int, reps: torch.Tensor,
+                  stream=None):
+    _check(lib().sv_build_reps(C.byref(shape), C.byref(kv), first_block, n_blocks, _ptr(reps),
+                               _stream(stream)))
+
+
+def sv_score_blocks(shape: Shape, q, reps, kv: KV, scores, stream=None):
+    _check(lib().sv_score_blocks(C.byref(shape), _ptr(q), _ptr(reps), C.byref(kv), _ptr(scores),
+                                 _stream(stream)))
+
+
+def sv_select_blocks(shape: Shape, scores, nb: int, k: int, sel, kmax: int, stream=None):
+    _check(lib().sv_select_blocks(C.byref(shape), _ptr(scores), nb, k, _ptr(sel), kmax,
+                                  _stream(stream)))
+
+
+def sv_score_select(shape: Shape, q, reps, kv: KV, budget: W.Budget, sel, kmax: int, ws,
+                    stream=None) -> int:
+    b = make_budget(budget)
+    k = C.c_int(-1)
+    _check(lib().sv_score_select(C.byref(shape), _ptr(q), _ptr(reps), C.byref(kv), C.byref(b),
+                                 _ptr(sel), kmax, C.byref(k), _ptr(ws),
+                                 0 if ws is None else ws.numel(), _stream(stream)))
+    return k.value
+
+
+def sv_sparse_attend(shape: Shape, q, kv: KV, sel, n_sel: int, sel_stride: int, draft_k, draft_v,
+                     parents, out, ws, stream=None):
+    _check(lib().sv_sparse_attend(C.byref(shape), _ptr(q), C.byref(kv), _ptr(sel), n_sel,
+                                  sel_stride, _ptr(draft_k), _ptr(draft_v), _parents(parents),
+                                  _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(),
+                                  _stream(stream)))
+
+
+def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: W.Budget, draft_k, draft_v, parents,
+                    reuse: int, sel_cache, kmax: int, out, ws, stream=None) -> int:
+    b = make_budget(budget)
+    k = C.c_int(-1)
+    _check(lib().sv_verify_layer(C.byref(shape), _ptr(q), C.byref(kv), _ptr(reps), C.byref(b),
+                                 _ptr(draft_k), _ptr(draft_v), _parents(parents), int(reuse),
+                                 _ptr(sel_cache), kmax, C.byref(k), _ptr(out), _ptr(ws),
+                                 0 if ws is None else ws.numel(), _stream(stream)))
+    return k.value
+
+
+# ------------------------------------------------------------ convenience
+class LayerState:
+    """Device-resident state of one verification layer: the paged KV cache,
+    its block representatives, a selection cache slot and a workspace.
+
+    Built from workloads.LayerInputs already on the device. Only allocation
+    and marshalling happen here; the computation is the library's.
+    """
+
+    def __init__(self, wl: W.Workload, x: W.LayerInputs, kmax: Optional[int] = None,
+                 build_reps: bool = True, stream=None):
+        self.wl, self.x = wl, x
+        self.shape = make_shape(wl.B, wl.Hq, wl.Hkv, wl.d, wl.blk, wl.T, wl.torch_dtype)
+        self.kv = make_kv(x.k_pool, x.v_pool, x.block_table, wl.ctx)
+        nb = wl.NB
+        self.k = sv_budget_blocks(wl.budget, wl.ctx, nb)
+        self.kmax = self.k if kmax is None else kmax
+        dev = x.q.device
+        self.reps = torch.zeros(wl.B, wl.Hkv, max(nb, 1), wl.d, dtype=torch.float32, device=dev)
+        self.sel = torch.full((wl.B, wl.Hkv, max(self.kmax, 1)), -1, dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(x.q)
+        # sized for the budgeted selection and for a dense (all-block) pass
+        self.ws = alloc_workspace(self.shape, max(nb, 1), max(self.kmax, nb, 1), device=dev)
+        self.parents = None if wl.parents is None else list(wl.parents)
+        if build_reps and nb:
+            sv_build_reps(self.shape, self.kv, 0, nb, self.reps, stream)
+
+    def verify(self, reuse: int = 0, sel_from: Optional["LayerState"] = None, stream=None):
+        if sel_from is not None:
+            self.sel = sel_from.sel
+        sv_verify_layer(self.shape, self.x.q, self.kv, self.reps, self.wl.budget, self.x.draft_k,
+                        self.x.draft_v, self.parents, reuse, self.sel, self.kmax, self.out,
+                        self.ws, stream)
+        return self.out

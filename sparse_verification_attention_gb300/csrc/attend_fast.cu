@@ -1,0 +1,419 @@
+// Split-KV sparse verification attention, bf16 tensor-core path.
+//
+// [SV-Fig1] "Accelerate Speculative Decoding with Sparse Computation in
+// Verification", paper summary page, Figure 1 caption: all draft tokens use
+// the same selected set of KV blocks. That is what makes this kernel
+// bandwidth-efficient: the T*G query rows that share a KV head are stacked
+// into one tile (R = T*G rows) and every selected KV page is read from HBM
+// exactly once for all of them.
+//
+// Design (GB300):
+//   * grid = (splits, Hkv, B); each CTA owns a contiguous run of the selected
+//     blocks of one (b, kv head); the last split also owns the draft tile.
+//   * warp 0 is the producer: one lane walks the selection, resolves the page
+//     through the block table and issues 2-D bulk tensor copies (TMA, 128-byte
+//     swizzle) of the page's K and V tiles into an NS-stage shared-memory ring
+//     guarded by mbarriers (full: transaction bytes; empty: consumer warps).
+//   * warps 1..NWC are consumers, 16 stacked rows each: S = Q K^T and O += P V
+//     on tensor cores (m16n8k16 bf16, fp32 accumulate), operands fetched with
+//     ldmatrix from the swizzled tiles, online softmax in registers (log2
+//     domain), P re-packed to bf16 straight from the accumulator registers.
+//   * the CTA writes an unnormalised partial (o, m, l) per row; a small merge
+//     kernel combines the splits with log-sum-exp weights.
+//   * every wait is bounded: on timeout a status flag is raised and the CTA
+//     drains its own copies before leaving; no spin can hang the GPU.
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.h"
+
+namespace sva {
+namespace {
+
+template <int D, int BLK, int NWC, int NS>
+struct FastCfg {
+  static constexpr int kBoxes = D / 64;           // 128-byte-wide TMA boxes per tile
+  static constexpr int kBoxBytes = BLK * 128;     // BLK rows x 64 bf16
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
+  static constexpr int kThreads = 32 * (NWC + 1);
+  static constexpr int kSmem = NS * kStageBytes + 1024 + 256;
+  static_assert(BLK % 16 == 0 && D % 64 == 0, "tile shape");
+};
+
+__device__ __forceinline__ uint32_t ld_bf16x2(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
+template <int D, int BLK>
+__device__ __forceinline__ uint32_t swz(int row, int dcol) {
+  // byte offset of (row, dcol) inside a K or V tile laid out as D/64 boxes of
+  // [BLK][64] bf16 with the 128-byte TMA swizzle (16-byte chunk c of row r at
+  // chunk c ^ (r & 7)).
+  const int box = dcol >> 6;
+  const int c = (dcol & 63) >> 3;
+  return box * (BLK * 128) + row * 128 + ((c ^ (row & 7)) << 4);
+}
+
+template <int D, int BLK, int NWC>
+struct Consumer {
+  uint32_t qf[D / 16][4];
+  float o[D / 8][4];
+  float m_lo, m_hi, l_lo, l_hi;
+  int r_lo, r_hi;
+
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const AttendArgs& a,
+                                       bool masked, int lane) {
+    const int t4 = lane & 3;
+    float s[BLK / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < BLK / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+
+    // S = Q K^T: B fragments of two 8-token n-tiles per ldmatrix.x4.
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int ntp = 0; ntp < BLK / 16; ++ntp) {
+        const int mi = lane >> 3;
+        const int tok = 16 * ntp + 8 * (mi >> 1) + (lane & 7);
+        const int dcol = 16 * kk + 8 * (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz<D, BLK>(tok, dcol), b0, b1, b2, b3);
+        mma_bf16(s[2 * ntp], qf[kk], b0, b1);
+        mma_bf16(s[2 * ntp + 1], qf[kk], b2, b3);
+      }
+    }
+
+    // Scale into the log2 domain, mask (draft tile only), online softmax.
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < BLK / 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[nt][e] * a.scale_log2;
+        if (masked) {
+          const int row = (e < 2) ? r_lo : r_hi;
+          const int u = 8 * nt + 2 * t4 + (e & 1);
+          bool ok = false;
+          if (u < a.T && row < a.R) ok = (a.anc[row / a.G] >> u) & 1ull;
+          if (!ok) v = -INFINITY;
+        }
+        s[nt][e] = v;
+      }
+      mx_lo = fmaxf(mx_lo, fmaxf(s[nt][0], s[nt][1]));
+      mx_hi = fmaxf(mx_hi, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float base_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo;
+    const float base_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
+    const float al_lo = exp2f(m_lo - base_lo), al_hi = exp2f(m_hi - base_hi);
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    l_lo *= al_lo;
+    l_hi *= al_hi;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      o[nd][0] *= al_lo; o[nd][1] *= al_lo;
+      o[nd][2] *= al_hi; o[nd][3] *= al_hi;
+    }
+    uint32_t pa[BLK / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < BLK / 8; ++nt) {
+      const float p0 = exp2f(s[nt][0] - base_lo), p1 = exp2f(s[nt][1] - base_lo);
+      const float p2 = exp2f(s[nt][2] - base_hi), p3 = exp2f(s[nt][3] - base_hi);
+      l_lo += p0 + p1;
+      l_hi += p2 + p3;
+      // C fragment of n-tile nt -> A fragment of k-step nt/2 (FA2 register reuse).
+      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p0, p1);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
+    }
+
+    // O += P V: V is token-major, so its B fragments come from ldmatrix.trans.
+#pragma unroll
+    for (int kt = 0; kt < BLK / 16; ++kt) {
+#pragma unroll
+      for (int ndp = 0; ndp < D / 16; ++ndp) {
+        const int mi = lane >> 3;
+        const int tok = 16 * kt + 8 * (mi & 1) + (lane & 7);
+        const int dcol = 8 * (2 * ndp + (mi >> 1));
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + swz<D, BLK>(tok, dcol), b0, b1, b2, b3);
+        mma_bf16(o[2 * ndp], pa[kt], b0, b1);
+        mma_bf16(o[2 * ndp + 1], pa[kt], b2, b3);
+      }
+    }
+  }
+};
+
+template <int D, int BLK, int NWC, int NS>
+__global__ void __launch_bounds__(32 * (NWC + 1))
+    attend_fast_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ AttendArgs a) {
+  using C = FastCfg<D, BLK, NWC, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * C::kStageBytes);
+  uint64_t* empty = full + NS;
+  int* stage_ok = reinterpret_cast<int*>(empty + NS);
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = b * a.Hkv + h;
+  const int j0 = split * a.bps;
+  const int j1 = min(a.n_sel, j0 + a.bps);
+  const int nblk = max(0, j1 - j0);
+  const bool has_draft = (split == a.n_splits - 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), NWC);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // The whole warp resolves 32 selected blocks at a time (selection entry,
+    // then block-table page) so that these dependent global loads overlap;
+    // lane 0 then issues the copies in order.
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    const int oob_row = a.num_pages * a.Hkv * BLK;  // past the end: TMA zero-fills
+    int issued = 0;
+    bool stop = false;
+    for (int base = 0; base < nblk && !stop; base += 32) {
+      int row = oob_row, ok = 0;
+      if (base + lane < nblk) {
+        const int j = a.sel ? a.sel[(size_t)pair * a.sel_stride + j0 + base + lane]
+                            : j0 + base + lane;
+        if (j < 0 || j >= a.nb) {
+          atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
+        } else {
+          const int page = a.block_table[(size_t)b * a.nb_max + j];
+          if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.status, SV_FLAG_BAD_PAGE);
+          } else {
+            row = (page * a.Hkv + h) * BLK;
+            ok = 1;
+          }
+        }
+      }
+      const int cnt = min(32, nblk - base);
+      for (int qq = 0; qq < cnt; ++qq) {
+        const int i = base + qq;
+        const int rq = __shfl_sync(0xffffffffu, row, qq);
+        const int okq = __shfl_sync(0xffffffffu, ok, qq);
+        int fail = 0;
+        if (lane == 0) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, kSpinLimit)) {
+            atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+            fail = 1;
+          } else {
+            stage_ok[s] = okq;
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            const uint32_t kdst = smem_u32(smem + s * C::kStageBytes);
+            const uint32_t vdst = kdst + C::kTileBytes;
+#pragma unroll
+            for (int x = 0; x < C::kBoxes; ++x) {
+              tma_load_2d(kdst + x * C::kBoxBytes, &tmK, 64 * x, rq, fb);
+              tma_load_2d(vdst + x * C::kBoxBytes, &tmV, 64 * x, rq, fb);
+            }
+            issued = i + 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, fail, 0)) {
+          stop = true;
+          break;
+        }
+      }
+    }
+    // Never leave with a bulk copy still writing into this CTA's memory.
+    if (lane == 0)
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait(smem_u32(&full[i % NS]), (i / NS) & 1, kSpinLimit);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int g = lane >> 2, t4 = lane & 3;
+  Consumer<D, BLK, NWC> cs;
+  cs.r_lo = 16 * cw + g;
+  cs.r_hi = cs.r_lo + 8;
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* qlo = nullptr;
+    const __nv_bfloat16* qhi = nullptr;
+    if (cs.r_lo < a.R)
+      qlo = q + (((size_t)b * a.T + cs.r_lo / a.G) * a.Hq + h * a.G + cs.r_lo % a.G) * D;
+    if (cs.r_hi < a.R)
+      qhi = q + (((size_t)b * a.T + cs.r_hi / a.G) * a.Hq + h * a.G + cs.r_hi % a.G) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int col = 16 * kk + 2 * t4;
+      cs.qf[kk][0] = qlo ? ld_bf16x2(qlo + col) : 0u;
+      cs.qf[kk][1] = qhi ? ld_bf16x2(qhi + col) : 0u;
+      cs.qf[kk][2] = qlo ? ld_bf16x2(qlo + col + 8) : 0u;
+      cs.qf[kk][3] = qhi ? ld_bf16x2(qhi + col + 8) : 0u;
+    }
+  }
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) cs.o[nd][0] = cs.o[nd][1] = cs.o[nd][2] = cs.o[nd][3] = 0.f;
+  cs.m_lo = cs.m_hi = -INFINITY;
+  cs.l_lo = cs.l_hi = 0.f;
+
+  const uint32_t sbase = smem_u32(smem);
+  for (int i = 0; i < nblk; ++i) {
+    const int s = i % NS;
+    if (!mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit)) {
+      atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+      break;
+    }
+    if (stage_ok[s]) {
+      const uint32_t kb = sbase + s * C::kStageBytes;
+      cs.tile(kb, kb + C::kTileBytes, a, false, lane);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+  }
+
+  if (has_draft) {
+    // Draft tile: draft K/V rows u < T (rows T..BLK-1 zero) copied into stage
+    // 0 in the same swizzled layout, then one masked tile.
+    asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
+    const int ctid = threadIdx.x - 32;
+    const uint4* dk = static_cast<const uint4*>(a.draft_k);
+    const uint4* dv = static_cast<const uint4*>(a.draft_v);
+    for (int idx = ctid; idx < BLK * (D / 8); idx += NWC * 32) {
+      const int u = idx / (D / 8), c = idx % (D / 8);
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (u < a.T) {
+        const size_t off = (((size_t)b * a.T + u) * a.Hkv + h) * (D / 8) + c;
+        kv = dk[off];
+        vv = dv[off];
+      }
+      const uint32_t o = swz<D, BLK>(u, 8 * c);
+      *reinterpret_cast<uint4*>(smem + o) = kv;
+      *reinterpret_cast<uint4*>(smem + C::kTileBytes + o) = vv;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
+    cs.tile(sbase, sbase + C::kTileBytes, a, true, lane);
+  }
+
+  // Partial results: unnormalised o, running max m (log2 domain), sum l.
+  float l_lo = cs.l_lo, l_hi = cs.l_hi;
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) {
+    const int col = 8 * nd + 2 * t4;
+    if (cs.r_lo < a.rpad)
+      *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_lo) * D + col) =
+          make_float2(cs.o[nd][0], cs.o[nd][1]);
+    if (cs.r_hi < a.rpad)
+      *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_hi) * D + col) =
+          make_float2(cs.o[nd][2], cs.o[nd][3]);
+  }
+  if (t4 == 0) {
+    if (cs.r_lo < a.rpad)
+      *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_lo) * 2) = make_float2(cs.m_lo, l_lo);
+    if (cs.r_hi < a.rpad)
+      *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_hi) * 2) = make_float2(cs.m_hi, l_hi);
+  }
+}
+
+template <int D, int BLK, int NWC>
+cudaError_t launch_cfg(const AttendArgs& a, cudaStream_t st) {
+  constexpr int NS = 3;
+  using C = FastCfg<D, BLK, NWC, NS>;
+  CUtensorMap mk, mv;
+  const char* why = nullptr;
+  if (!encode_pool_map(&mk, a.k_pool, a.num_pages, a.Hkv, BLK, D, &why) ||
+      !encode_pool_map(&mv, a.v_pool, a.num_pages, a.Hkv, BLK, D, &why))
+    return cudaErrorInvalidValue;
+  auto kern = attend_fast_kernel<D, BLK, NWC, NS>;  // attribute set by occupancy_cfg
+  dim3 grid(a.n_splits, a.Hkv, a.B);
+  kern<<<grid, C::kThreads, C::kSmem, st>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
+template <int D, int BLK>
+cudaError_t launch_rows(const AttendArgs& a, cudaStream_t st) {
+  const int nwc = a.rpad / 16;
+  if (nwc <= 1) return launch_cfg<D, BLK, 1>(a, st);
+  if (nwc <= 2) return launch_cfg<D, BLK, 2>(a, st);
+  if (nwc <= 4) return launch_cfg<D, BLK, 4>(a, st);
+  return launch_cfg<D, BLK, 8>(a, st);
+}
+
+// Sets the kernel's shared-memory attribute and returns its resident CTAs per
+// SM; computed once per device and cached.
+template <int D, int BLK, int NWC>
+int occupancy_cfg() {
+  constexpr int NS = 3;
+  using C = FastCfg<D, BLK, NWC, NS>;
+  static std::atomic<int> cached[kMaxDevices];
+  const int dev = current_device();
+  const int c = cached[dev].load();
+  if (c > 0) return c;
+  auto kern = attend_fast_kernel<D, BLK, NWC, NS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+      cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmem) !=
+      cudaSuccess)
+    return 0;
+  cached[dev].store(n);
+  return n;
+}
+
+template <int D, int BLK>
+int occupancy_rows(const AttendArgs& a) {
+  const int nwc = a.rpad / 16;
+  if (nwc <= 1) return occupancy_cfg<D, BLK, 1>();
+  if (nwc <= 2) return occupancy_cfg<D, BLK, 2>();
+  if (nwc <= 4) return occupancy_cfg<D, BLK, 4>();
+  return occupancy_cfg<D, BLK, 8>();
+}
+
+}  // namespace
+
+int attend_fast_ctas_per_sm(const AttendArgs& a, int dtype) {
+  if (dtype != SV_BF16) return 0;
+  if (!(a.d == 64 || a.d == 128)) return 0;
+  if (!(a.blk == 32 || a.blk == 64)) return 0;
+  if (a.rpad > 128 || a.T > a.blk) return 0;
+  if ((reinterpret_cast<uintptr_t>(a.k_pool) & 15) || (reinterpret_cast<uintptr_t>(a.v_pool) & 15))
+    return 0;
+  if ((long long)(a.num_pages + 1) * a.Hkv * a.blk >= (1ll << 31)) return 0;
+  if (a.d == 128 && a.blk == 64) return occupancy_rows<128, 64>(a);
+  if (a.d == 128 && a.blk == 32) return occupancy_rows<128, 32>(a);
+  if (a.d == 64 && a.blk == 64) return occupancy_rows<64, 64>(a);
+  return occupancy_rows<64, 32>(a);
+}
+
+cudaError_t launch_attend_fast(const AttendArgs& a, cudaStream_t st) {
+  if (a.d == 128 && a.blk == 64) return launch_rows<128, 64>(a, st);
+  if (a.d == 128 && a.blk == 32) return launch_rows<128, 32>(a, st);
+  if (a.d == 64 && a.blk == 64) return launch_rows<64, 64>(a, st);
+  if (a.d == 64 && a.blk == 32) return launch_rows<64, 32>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sva

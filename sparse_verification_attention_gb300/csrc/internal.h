@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of libsva.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sva.h"
+
+namespace sva {
+
+constexpr int kMaxT = 64;          // draft tokens (ancestor masks are 64-bit)
+constexpr int kMaxD = 256;
+constexpr int kMaxNB = 16384;      // blocks per sequence (top-k keys fit in smem)
+constexpr int kMaxSplits = 64;     // split-KV partial slots per (b, kv head)
+constexpr int kStatusBytes = 256;  // workspace head: device status word
+
+// Bounded spin for every device-side wait: after this many polls the waiter
+// sets SV_FLAG_WAIT_TIMEOUT and gives up instead of hanging the GPU.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace carve-up (offsets in bytes from the workspace base).
+struct WsLayout {
+  size_t status, scores, part_o, part_ml, total;
+  int rpad, slots;
+};
+WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax);
+
+// ---------------------------------------------------------------- kernels
+struct RepsArgs {
+  const void* k_pool;
+  const int32_t* block_table;
+  float* reps;
+  int B, Hkv, d, blk, nb_max, num_pages, first_block, n_blocks;
+  unsigned* status;  // may be null (sv_build_reps has no workspace)
+};
+cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st);
+
+struct ScoreArgs {
+  const void* q;
+  const float* reps;
+  float* scores;
+  int B, T, Hq, Hkv, G, d, nb, nb_max;
+};
+cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st);
+
+struct SelectArgs {
+  const float* scores;
+  int32_t* sel;
+  int pairs, nb, k, kmax;
+};
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+struct AttendArgs {
+  const void* q;        // [B,T,Hq,d]
+  const void* k_pool;   // [P,Hkv,blk,d]
+  const void* v_pool;
+  const void* draft_k;  // [B,T,Hkv,d]
+  const void* draft_v;
+  const int32_t* block_table;
+  const int32_t* sel;   // null: identity selection over NB blocks
+  float* part_o;        // [B,Hkv,S,Rpad,d]
+  float* part_ml;       // [B,Hkv,S,Rpad,2]
+  unsigned* status;
+  int B, T, Hq, Hkv, G, d, blk, R, rpad;
+  int nb, nb_max, num_pages, n_sel, sel_stride;
+  int n_splits, bps;    // split s covers selected blocks [s*bps, min(n_sel,(s+1)*bps))
+  float scale_log2;     // log2(e) / sqrt(d)
+  unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
+};
+
+// Fast path availability: bf16, d in {64,128}, blk in {32,64}, rpad <= 128,
+// T <= blk, 16-byte aligned pools. Returns the number of CTAs per SM the
+// fast path keeps resident (0 when it does not apply).
+int attend_fast_ctas_per_sm(const AttendArgs& a, int dtype);
+cudaError_t launch_attend_fast(const AttendArgs& a, cudaStream_t st);
+cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
+
+struct MergeArgs {
+  const float* part_o;
+  const float* part_ml;
+  void* out;  // [B,T,Hq,d]
+  int B, T, Hq, Hkv, G, d, R, rpad, n_splits;
+};
+cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st);
+
+// Per-device once-only setup results (kernel attributes, occupancy), so that
+// steady-state calls only launch kernels and can be captured in CUDA graphs.
+int current_device();
+constexpr int kMaxDevices = 64;
+
+// TMA descriptor encoding through the driver entry point (no -lcuda).
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv, int blk,
+                     int d, const char** why);
+
+}  // namespace sva

@@ -1,0 +1,145 @@
+// Block representatives and block importance scores.
+//
+// [SV-Fig1] "Accelerate Speculative Decoding with Sparse Computation in
+// Verification", paper summary page, Figure 1 caption: blocks are chosen by
+// the dot product between the first draft token's query and a representative
+// value of each KV block. The representative is read here as the mean of the
+// block's keys, accumulated in fp32.
+#include "internal.h"
+
+namespace sva {
+namespace {
+
+// Loads 4 consecutive elements as fp32 (8 bytes for bf16, 16 for fp32).
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+  return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+}
+
+// ------------------------------------------------------------------ reps
+// One CTA per (logical block, kv head, sequence); thread i of the CTA owns
+// 4 consecutive dims and walks the blk tokens of the page in order.
+template <typename T>
+__global__ void build_reps_kernel(RepsArgs a) {
+  const int j = a.first_block + blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int i4 = threadIdx.x * 4;
+  if (i4 >= a.d) return;
+  const int page = a.block_table[(size_t)b * a.nb_max + j];
+  float* dst = a.reps + (((size_t)b * a.Hkv + h) * a.nb_max + j) * a.d + i4;
+  if (page < 0 || page >= a.num_pages) {
+    if (a.status && threadIdx.x == 0) atomicOr(a.status, SV_FLAG_BAD_PAGE);
+    *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const T* src = static_cast<const T*>(a.k_pool) + ((size_t)page * a.Hkv + h) * a.blk * a.d + i4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = 0; t < a.blk; ++t) {
+    float4 v = load4<T>(src + (size_t)t * a.d);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  const float inv = 1.0f / (float)a.blk;
+  *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+// ------------------------------------------------------------------ scores
+// grid = (ceil(nb / kRowsPerCta), B*Hkv). Each warp streams whole fp32
+// representative rows with 128-bit loads (lane c holds dims 4c..4c+3), dots
+// them with the group-summed draft-0 query held in registers, and reduces
+// across the warp. Rows are processed kUnroll at a time so that every lane
+// keeps several independent 16-byte loads in flight.
+constexpr int kScoreWarps = 8;
+constexpr int kUnroll = 4;
+constexpr int kRowsPerWarp = 8;
+constexpr int kRowsPerCta = kScoreWarps * kRowsPerWarp;
+constexpr int kMaxChunks = kMaxD / 4 / 32;  // float4 chunks per lane (d <= 256)
+
+template <typename T>
+__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(ScoreArgs a) {
+  const int pair = blockIdx.y;  // b * Hkv + h
+  const int b = pair / a.Hkv, h = pair % a.Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nchunk = a.d / 4;
+
+  // qhat = sum over the G query heads of KV head h of draft 0's query.
+  float4 qh[kMaxChunks];
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    qh[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int ch = lane + 32 * c;
+    if (ch < nchunk) {
+      const T* q0 = static_cast<const T*>(a.q) + ((size_t)b * a.T * a.Hq + (size_t)h * a.G) * a.d;
+      for (int g = 0; g < a.G; ++g) {
+        float4 v = load4<T>(q0 + (size_t)g * a.d + ch * 4);
+        qh[c].x += v.x; qh[c].y += v.y; qh[c].z += v.z; qh[c].w += v.w;
+      }
+    }
+  }
+
+  const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
+  const int row0 = blockIdx.x * kRowsPerCta + warp * kRowsPerWarp;
+#pragma unroll
+  for (int it = 0; it < kRowsPerWarp; it += kUnroll) {
+    float acc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      acc[u] = 0.f;
+      const int j = row0 + it + u;
+      if (j < a.nb) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+          const int ch = lane + 32 * c;
+          if (ch < nchunk) {
+            float4 r = __ldg(reinterpret_cast<const float4*>(rep0 + (size_t)j * a.d) + ch);
+            acc[u] = fmaf(qh[c].x, r.x, acc[u]);
+            acc[u] = fmaf(qh[c].y, r.y, acc[u]);
+            acc[u] = fmaf(qh[c].z, r.z, acc[u]);
+            acc[u] = fmaf(qh[c].w, r.w, acc[u]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+      const int j = row0 + it + u;
+      if (lane == 0 && j < a.nb) a.scores[(size_t)pair * a.nb + j] = acc[u];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st) {
+  if (a.n_blocks == 0) return cudaSuccess;
+  dim3 grid(a.n_blocks, a.Hkv, a.B);
+  dim3 block(round_up(a.d / 4, 32));
+  if (dtype == SV_BF16)
+    build_reps_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(a);
+  else
+    build_reps_kernel<float><<<grid, block, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st) {
+  if (a.nb == 0) return cudaSuccess;
+  dim3 grid((a.nb + kRowsPerCta - 1) / kRowsPerCta, a.B * a.Hkv);
+  if (dtype == SV_BF16)
+    score_kernel<__nv_bfloat16><<<grid, kScoreWarps * 32, 0, st>>>(a);
+  else
+    score_kernel<float><<<grid, kScoreWarps * 32, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sva

@@ -1,0 +1,447 @@
+// C ABI of libsva.so: argument validation, workspace carve-up, split-KV
+// planning and kernel launches. Declarations and contracts: include/sva.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace sva {
+namespace {
+
+thread_local std::string g_err;
+
+sv_status fail(sv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+sv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+sv_status check_shape(const sv_shape* s) {
+  if (!s) return fail(SV_ERR_INVALID_ARG, "shape is NULL");
+  if (s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->d < 1 || s->blk < 1 || s->T < 1)
+    return fail(SV_ERR_INVALID_ARG, "shape fields must be >= 1 (B=%d Hq=%d Hkv=%d d=%d blk=%d T=%d)",
+                s->B, s->Hq, s->Hkv, s->d, s->blk, s->T);
+  if (s->Hq % s->Hkv) return fail(SV_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", s->Hq, s->Hkv);
+  if (s->dtype != SV_BF16 && s->dtype != SV_F32)
+    return fail(SV_ERR_INVALID_ARG, "unknown dtype %d", s->dtype);
+  if (s->d % 8 || s->d > kMaxD)
+    return fail(SV_ERR_UNSUPPORTED, "head dim %d must be a multiple of 8 and <= %d", s->d, kMaxD);
+  if (s->T > kMaxT) return fail(SV_ERR_UNSUPPORTED, "T=%d drafts exceeds %d", s->T, kMaxT);
+  if ((long long)s->T * (s->Hq / s->Hkv) > 4096)
+    return fail(SV_ERR_UNSUPPORTED, "T*G=%d stacked rows exceeds 4096", s->T * (s->Hq / s->Hkv));
+  return SV_OK;
+}
+
+sv_status check_kv(const sv_shape* s, const sv_kv* kv, bool need_v) {
+  if (!kv) return fail(SV_ERR_INVALID_ARG, "kv is NULL");
+  if (kv->ctx < 0) return fail(SV_ERR_INVALID_ARG, "ctx=%d is negative", kv->ctx);
+  if (kv->ctx % s->blk)
+    return fail(SV_ERR_UNSUPPORTED, "ctx=%d is not a multiple of blk=%d", kv->ctx, s->blk);
+  const int nb = kv->ctx / s->blk;
+  if (nb > kMaxNB) return fail(SV_ERR_UNSUPPORTED, "NB=%d blocks exceeds %d", nb, kMaxNB);
+  if (kv->nb_max < nb) return fail(SV_ERR_INVALID_ARG, "nb_max=%d < NB=%d", kv->nb_max, nb);
+  if (nb > 0) {
+    if (!kv->k_pool || (need_v && !kv->v_pool) || !kv->block_table)
+      return fail(SV_ERR_INVALID_ARG, "k_pool/v_pool/block_table is NULL");
+    if (kv->num_pages < 1) return fail(SV_ERR_INVALID_ARG, "num_pages=%d", kv->num_pages);
+    if (!aligned(kv->k_pool, 16) || (need_v && !aligned(kv->v_pool, 16)))
+      return fail(SV_ERR_INVALID_ARG, "k_pool/v_pool must be 16-byte aligned");
+    if ((long long)(kv->num_pages + 1) * s->Hkv * s->blk >= (1ll << 31))
+      return fail(SV_ERR_UNSUPPORTED, "pool of %d pages is too large", kv->num_pages);
+  }
+  return SV_OK;
+}
+
+int budget_blocks(const sv_budget* bd, int ctx, int nb) {
+  if (!bd || ctx < 0 || nb < 0) return -1;
+  if (bd->mode == SV_BUDGET_FIXED) {
+    if (bd->fixed_blocks < 0) return -1;
+    return nb < bd->fixed_blocks ? nb : bd->fixed_blocks;
+  }
+  if (bd->mode != SV_BUDGET_PIECEWISE) return -1;
+  if (bd->floor_blocks < 0 || !(bd->frac_mid >= 0.0 && bd->frac_mid <= 1.0) ||
+      !(bd->frac_long >= 0.0 && bd->frac_long <= 1.0))
+    return -1;
+  if (ctx <= bd->short_ctx) return nb;
+  const double frac = (ctx <= bd->long_ctx) ? bd->frac_mid : bd->frac_long;
+  // ceil(frac * nb) with a guard against products like 0.125*960 landing a
+  // hair above an integer through rounding.
+  const double prod = frac * (double)nb;
+  long long want = (long long)std::ceil(prod - 1e-9 * (prod > 1.0 ? prod : 1.0));
+  long long k = want > bd->floor_blocks ? want : bd->floor_blocks;
+  return (int)(k < nb ? k : nb);
+}
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64) {
+    int c = cached[dev].load();
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev].store(n);
+  return n;
+}
+
+// Split planning: enough CTAs to fill every SM `per_sm` deep in one wave,
+// never more than one split per selected block, at most kMaxSplits.
+void plan_splits(int pairs, int n_sel, int per_sm, int* n_splits, int* bps) {
+  if (n_sel <= 0) {
+    *n_splits = 1;
+    *bps = 1;
+    return;
+  }
+  const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
+  int s = slots / (pairs > 0 ? pairs : 1);
+  if (s < 1) s = 1;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s > n_sel) s = n_sel;
+  const int per = (n_sel + s - 1) / s;
+  *bps = per;
+  *n_splits = (n_sel + per - 1) / per;
+}
+
+void fill_ancestors(const int32_t* parent, int T, unsigned long long* anc) {
+  for (int t = 0; t < kMaxT; ++t) anc[t] = 0ull;
+  for (int t = 0; t < T; ++t) {
+    unsigned long long m = 0ull;
+    int u = t;
+    while (u >= 0) {
+      m |= 1ull << u;
+      u = parent ? parent[u] : u - 1;
+    }
+    anc[t] = m;
+  }
+}
+
+sv_status check_parents(const int32_t* parent, int T) {
+  if (!parent) return SV_OK;
+  if (parent[0] != -1) return fail(SV_ERR_INVALID_ARG, "draft_parent[0]=%d must be -1", parent[0]);
+  for (int t = 1; t < T; ++t)
+    if (parent[t] < 0 || parent[t] >= t)
+      return fail(SV_ERR_INVALID_ARG, "draft_parent[%d]=%d must be in [0,%d)", t, parent[t], t);
+  return SV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
+
+WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
+  WsLayout L;
+  const int G = s.Hq / s.Hkv;
+  L.rpad = round_up(s.T * G, 16);
+  int slots = kmax < 1 ? 1 : (kmax > kMaxSplits ? kMaxSplits : kmax);
+  L.slots = slots;
+  const size_t pairs = (size_t)s.B * s.Hkv;
+  L.status = 0;
+  L.scores = kStatusBytes;
+  L.part_o = L.scores + align256(pairs * (size_t)(nb_max > 0 ? nb_max : 1) * sizeof(float));
+  L.part_ml = L.part_o + align256(pairs * slots * (size_t)L.rpad * s.d * sizeof(float));
+  L.total = L.part_ml + align256(pairs * slots * (size_t)L.rpad * 2 * sizeof(float));
+  return L;
+}
+
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv, int blk, int d,
+                     const char** why) {
+  auto enc = get_encode();
+  if (!enc) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return false;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * Hkv * blk};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)blk};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return false;
+  }
+  return true;
+}
+
+// Shared by sv_sparse_attend and sv_verify_layer once arguments are valid.
+static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, const int32_t* sel,
+                            int n_sel, int sel_stride, const void* dk, const void* dv,
+                            const int32_t* parent, void* out, void* ws, const WsLayout& L,
+                            cudaStream_t st) {
+  AttendArgs a{};
+  a.q = q;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.draft_k = dk;
+  a.draft_v = dv;
+  a.block_table = kv->block_table;
+  a.sel = sel;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.part_o = reinterpret_cast<float*>(w + L.part_o);
+  a.part_ml = reinterpret_cast<float*>(w + L.part_ml);
+  a.status = reinterpret_cast<unsigned*>(w + L.status);
+  a.B = s->B;
+  a.T = s->T;
+  a.Hq = s->Hq;
+  a.Hkv = s->Hkv;
+  a.G = s->Hq / s->Hkv;
+  a.d = s->d;
+  a.blk = s->blk;
+  a.R = s->T * a.G;
+  a.rpad = L.rpad;
+  a.nb = kv->ctx / s->blk;
+  a.nb_max = kv->nb_max;
+  a.num_pages = kv->num_pages;
+  a.n_sel = n_sel;
+  a.sel_stride = sel_stride;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s->d));
+  fill_ancestors(parent, s->T, a.anc);
+
+  const int fast = attend_fast_ctas_per_sm(a, s->dtype);
+  plan_splits(s->B * s->Hkv, n_sel, fast > 0 ? fast : 4, &a.n_splits, &a.bps);
+  if (a.n_splits > L.slots)
+    return fail(SV_ERR_WORKSPACE, "workspace sized for %d splits, plan needs %d", L.slots, a.n_splits);
+  cudaError_t e = (fast > 0) ? launch_attend_fast(a, st) : launch_attend_generic(a, s->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+  MergeArgs m{};
+  m.part_o = a.part_o;
+  m.part_ml = a.part_ml;
+  m.out = out;
+  m.B = a.B;
+  m.T = a.T;
+  m.Hq = a.Hq;
+  m.Hkv = a.Hkv;
+  m.G = a.G;
+  m.d = a.d;
+  m.R = a.R;
+  m.rpad = a.rpad;
+  m.n_splits = a.n_splits;
+  e = launch_merge(m, s->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SV_OK;
+}
+
+static sv_status check_ws(const sv_shape* s, int nb_max, int kmax, const void* ws, size_t bytes,
+                          WsLayout* L) {
+  *L = ws_layout(*s, nb_max, kmax);
+  if (!ws) return fail(SV_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(SV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (bytes < L->total)
+    return fail(SV_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, L->total);
+  return SV_OK;
+}
+
+static sv_status do_score_select(const sv_shape* s, const void* q, const float* reps,
+                                 const sv_kv* kv, int k, int32_t* sel, int kmax, void* ws,
+                                 const WsLayout& L, cudaStream_t st) {
+  const int nb = kv->ctx / s->blk;
+  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
+  ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max};
+  cudaError_t e = launch_score(sa, s->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "score launch");
+  SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax};
+  e = launch_select(se, st);
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return SV_OK;
+}
+
+}  // namespace sva
+
+using namespace sva;
+
+extern "C" {
+
+int sv_abi_version(void) { return SV_ABI_VERSION; }
+
+const char* sv_last_error(void) { return g_err.c_str(); }
+
+int sv_budget_blocks(const sv_budget* budget, int ctx, int nb) {
+  return budget_blocks(budget, ctx, nb);
+}
+
+size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax) {
+  if (check_shape(shape) != SV_OK || nb_max < 0 || kmax < 0) return 0;
+  return ws_layout(*shape, nb_max, kmax).total;
+}
+
+sv_status sv_clear_status(void* workspace, void* stream) {
+  if (!workspace) return fail(SV_ERR_INVALID_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+sv_status sv_read_status(const void* workspace, uint32_t* flags, void* stream) {
+  if (!workspace || !flags) return fail(SV_ERR_INVALID_ARG, "workspace/flags is NULL");
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *flags = v;
+  if (v) return fail(SV_ERR_DEVICE_FAULT, "device status flags 0x%x", v);
+  return SV_OK;
+}
+
+sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block, int n_blocks,
+                        float* reps, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
+  const int nb = kv->ctx / shape->blk;
+  if (first_block < 0 || n_blocks < 0 || first_block + n_blocks > nb)
+    return fail(SV_ERR_INVALID_ARG, "blocks [%d, %d) outside [0, %d)", first_block,
+                first_block + n_blocks, nb);
+  if (n_blocks == 0) return SV_OK;
+  if (!reps || !aligned(reps, 16)) return fail(SV_ERR_INVALID_ARG, "reps NULL or not 16-byte aligned");
+  RepsArgs a{kv->k_pool, kv->block_table, reps, shape->B, shape->Hkv, shape->d, shape->blk,
+             kv->nb_max, kv->num_pages, first_block, n_blocks, nullptr};
+  cudaError_t e = launch_build_reps(a, shape->dtype, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "build_reps launch");
+}
+
+sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* reps, const sv_kv* kv,
+                          float* scores, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
+  const int nb = kv->ctx / shape->blk;
+  if (nb == 0) return SV_OK;
+  if (!q || !reps || !scores) return fail(SV_ERR_INVALID_ARG, "q/reps/scores is NULL");
+  if (!aligned(q, 16) || !aligned(reps, 16))
+    return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
+  ScoreArgs sa{q, reps, scores, shape->B, shape->T, shape->Hq, shape->Hkv,
+               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max};
+  cudaError_t e = launch_score(sa, shape->dtype, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "score launch");
+}
+
+sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, int k, int32_t* sel,
+                           int kmax, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if (nb < 0 || nb > kMaxNB) return fail(SV_ERR_UNSUPPORTED, "nb=%d outside [0, %d]", nb, kMaxNB);
+  if (k < 0 || k > kmax) return fail(SV_ERR_INVALID_ARG, "k=%d outside [0, kmax=%d]", k, kmax);
+  if (kmax == 0) return SV_OK;
+  if (!sel || (nb > 0 && !scores)) return fail(SV_ERR_INVALID_ARG, "scores/sel is NULL");
+  SelectArgs se{scores, sel, shape->B * shape->Hkv, nb, k, kmax};
+  cudaError_t e = launch_select(se, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "select launch");
+}
+
+sv_status sv_score_select(const sv_shape* shape, const void* q, const float* reps, const sv_kv* kv,
+                          const sv_budget* budget, int32_t* sel, int kmax, int* k_out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
+  const int nb = kv->ctx / shape->blk;
+  const int k = budget_blocks(budget, kv->ctx, nb);
+  if (k < 0) return fail(SV_ERR_INVALID_ARG, "invalid budget");
+  if (k > kmax) return fail(SV_ERR_INVALID_ARG, "budget k=%d exceeds kmax=%d", k, kmax);
+  if (kmax > 0 && !sel) return fail(SV_ERR_INVALID_ARG, "sel is NULL");
+  if (nb > 0 && (!q || !reps)) return fail(SV_ERR_INVALID_ARG, "q/reps is NULL");
+  if (nb > 0 && (!aligned(q, 16) || !aligned(reps, 16)))
+    return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
+  WsLayout L;
+  if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+  if (k_out) *k_out = k;
+  if (kmax == 0) return SV_OK;
+  return do_score_select(shape, q, reps, kv, k, sel, kmax, workspace, L, (cudaStream_t)stream);
+}
+
+sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv, const int32_t* sel,
+                           int n_sel, int sel_stride, const void* draft_k, const void* draft_v,
+                           const int32_t* draft_parent, void* out, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
+  const int nb = kv->ctx / shape->blk;
+  if (!sel) {
+    n_sel = nb;
+    sel_stride = nb;
+  } else if (n_sel < 0 || n_sel > sel_stride) {
+    return fail(SV_ERR_INVALID_ARG, "n_sel=%d outside [0, sel_stride=%d]", n_sel, sel_stride);
+  }
+  if (!q || !draft_k || !draft_v || !out)
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out is NULL");
+  if (!aligned(q, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16) || !aligned(out, 16))
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out must be 16-byte aligned");
+  if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
+  WsLayout L;
+  if ((r = check_ws(shape, kv->nb_max, n_sel, workspace, ws_bytes, &L)) != SV_OK) return r;
+  return run_attend(shape, q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent, out,
+                    workspace, L, (cudaStream_t)stream);
+}
+
+sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,
+                          const sv_budget* budget, const void* draft_k, const void* draft_v,
+                          const int32_t* draft_parent, int reuse, int32_t* sel_cache, int kmax,
+                          int* k_out, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
+  if (reuse != 0 && reuse != 1) return fail(SV_ERR_INVALID_ARG, "reuse=%d must be 0 or 1", reuse);
+  const int nb = kv->ctx / shape->blk;
+  const int k = budget_blocks(budget, kv->ctx, nb);
+  if (k < 0) return fail(SV_ERR_INVALID_ARG, "invalid budget");
+  if (k > kmax) return fail(SV_ERR_INVALID_ARG, "budget k=%d exceeds kmax=%d", k, kmax);
+  if (kmax > 0 && !sel_cache) return fail(SV_ERR_INVALID_ARG, "sel_cache is NULL");
+  if (!q || !draft_k || !draft_v || !out)
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out is NULL");
+  if (!aligned(q, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16) || !aligned(out, 16))
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out must be 16-byte aligned");
+  if (!reuse && nb > 0 && (!reps || !aligned(reps, 16)))
+    return fail(SV_ERR_INVALID_ARG, "reps NULL or not 16-byte aligned");
+  if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
+  WsLayout L;
+  if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!reuse && kmax > 0) {
+    r = do_score_select(shape, q, reps, kv, k, sel_cache, kmax, workspace, L, st);
+    if (r != SV_OK) return r;
+  }
+  if (k_out) *k_out = k;
+  return run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out,
+                    workspace, L, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,136 @@
+"""Host-side checks of libsva.so that need no GPU: it loads, exports every
+symbol include/sva.h declares, computes the piecewise budget exactly like the
+oracle, sizes workspaces, and rejects bad arguments before launching."""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+from oracle import sva_oracle as O
+from sparse_verification_attention_gb300 import api, build_lib
+from sparse_verification_attention_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return api.lib()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "sva.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\*]+\s+)+\**(sv_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    syms = header_symbols()
+    assert len(syms) >= 12, syms
+    for s in syms:
+        assert hasattr(L, s), f"libsva.so does not export {s}"
+    assert set(syms) == set(api.EXPORTED)
+
+
+def test_abi_version(L):
+    assert api.sv_abi_version() == 1
+
+
+def test_budget_matches_oracle_golden(L):
+    path = os.path.join(ROOT, "tests", "golden", "budget_table.txt")
+    n = 0
+    for ln in open(path):
+        ln = ln.split("#")[0].strip()
+        if not ln:
+            continue
+        f = ln.split()
+        ctx, nb, mode, fixed, short, floor = map(int, f[:6])
+        b = W.Budget(mode, fixed, short, floor, float(f[6]), int(f[7]), float(f[8]))
+        assert api.sv_budget_blocks(b, ctx, nb) == int(f[9]), ln
+        n += 1
+    assert n >= 10
+
+
+def test_budget_matches_oracle_random(L):
+    g = torch.Generator().manual_seed(1)
+    fracs = [0.03125, 0.0625, 0.1, 0.125, 0.2, 0.25, 0.3, 0.5, 1.0]
+    for _ in range(3000):
+        mode = int(torch.randint(0, 2, (1,), generator=g))
+        nb = int(torch.randint(0, 5000, (1,), generator=g))
+        ctx = nb * int(torch.randint(1, 129, (1,), generator=g))
+        b = W.Budget(mode, int(torch.randint(0, 300, (1,), generator=g)),
+                     int(torch.randint(0, 70000, (1,), generator=g)),
+                     int(torch.randint(0, 200, (1,), generator=g)),
+                     fracs[int(torch.randint(0, len(fracs), (1,), generator=g))],
+                     int(torch.randint(0, 300000, (1,), generator=g)),
+                     fracs[int(torch.randint(0, len(fracs), (1,), generator=g))])
+        assert api.sv_budget_blocks(b, ctx, nb) == O.budget_from(b, ctx, nb), (b, ctx, nb)
+
+
+def test_budget_rejects_invalid(L):
+    assert L.sv_budget_blocks(None, 100, 10) == -1
+    assert api.sv_budget_blocks(W.Budget(7), 100, 10) == -1
+    assert api.sv_budget_blocks(W.Budget(1, 0, 0, 0, 1.5, 0, 0.1), 100, 10) == -1
+    assert api.sv_budget_blocks(W.Budget(0, -1), 100, 10) == -1
+
+
+def test_workspace_sizes(L):
+    s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
+    n = api.sv_workspace_bytes(s, 2048, 128)
+    # status + scores + partial o + partial (m, l), each 256-aligned
+    scores = 4 * 8 * 2048 * 4
+    part = 4 * 8 * 64 * 32 * 128 * 4
+    ml = 4 * 8 * 64 * 32 * 2 * 4
+    assert n == 256 + scores + part + ml
+    assert api.sv_workspace_bytes(s, 2048, 8) < n
+    bad = api.make_shape(4, 30, 8, 128, 64, 8, torch.bfloat16)  # Hq % Hkv != 0
+    assert api.sv_workspace_bytes(bad, 2048, 128) == 0
+    assert api.sv_workspace_bytes(api.make_shape(1, 4, 2, 12, 16, 4, 1), 64, 8) == 0  # d % 8
+
+
+def _status(L, fn, *args):
+    st = fn(*args)
+    return st, L.sv_last_error().decode()
+
+
+def test_invalid_arguments_rejected_before_launch(L):
+    """Every call below must fail validation on the host (no GPU here: a
+    launch attempt would come back as SV_ERR_CUDA instead)."""
+    s = api.make_shape(1, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    kv = api.KV(fake, fake, fake, 64, 64, 1024)
+    ws_n = api.sv_workspace_bytes(s, 64, 8)
+    b = api.make_budget(W.Budget(W.BUDGET_FIXED, 8, 0, 0, 0, 0, 0))
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(s), None, C.byref(kv), None, 0, 0, None, None,
+                      None, None, None, 0, None)
+    assert st == api.SV_ERR_INVALID_ARG and "NULL" in msg
+    bad_kv = api.KV(fake, fake, fake, 64, 64, 1000)  # ctx % blk != 0
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(bad_kv), 0, 1, fake, None)
+    assert st == api.SV_ERR_UNSUPPORTED, msg
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(kv), 60, 10, fake, None)
+    assert st == api.SV_ERR_INVALID_ARG, msg
+    small = api.KV(fake, fake, fake, 10, 64, 1024)  # nb_max < NB
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(small), 0, 1, fake, None)
+    assert st == api.SV_ERR_INVALID_ARG and "nb_max" in msg
+    k = C.c_int(0)
+    st, msg = _status(L, L.sv_score_select, C.byref(s), fake, fake, C.byref(kv), C.byref(b),
+                      fake, 4, C.byref(k), fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "kmax" in msg
+    st, msg = _status(L, L.sv_score_select, C.byref(s), fake, fake, C.byref(kv), C.byref(b),
+                      fake, 8, C.byref(k), fake, ws_n - 1, None)
+    assert st == api.SV_ERR_WORKSPACE, msg
+    bad_par = (C.c_int32 * 4)(-1, 0, 2, 1)  # parent[2] = 2 is not an earlier draft
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(s), fake, C.byref(kv), fake, 8, 8, fake, fake,
+                      bad_par, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "draft_parent" in msg
+    st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), fake, C.byref(b), fake,
+                      fake, None, 2, fake, 8, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "reuse" in msg
+    big_t = api.make_shape(1, 4, 2, 64, 16, 65, torch.float32)
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(big_t), fake, C.byref(kv), fake, 8, 8, fake,
+                      fake, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_UNSUPPORTED, msg
+    st, msg = _status(L, L.sv_clear_status, None, None)
+    assert st == api.SV_ERR_INVALID_ARG

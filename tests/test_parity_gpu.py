@@ -1,0 +1,349 @@
+"""CUDA path (through the C ABI) against the CPU oracle.
+
+Oracle-sized cases span several split tiles and ragged tails; the full-size
+workloads are checked on sampled (sequence, kv head) pairs that the oracle
+recomputes one by one, in the same launch configuration the benchmark uses.
+"""
+import pytest
+import torch
+
+from oracle import sva_oracle as O
+from sparse_verification_attention_gb300 import api, build_lib
+from sparse_verification_attention_gb300 import workloads as W
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    build_lib.build()
+    api.lib()
+    torch.cuda.set_device(0)
+
+
+def small_wl(dtype="bf16", **kw):
+    base = dict(name="small", B=2, Hq=8, Hkv=2, d=128, blk=64, ctx=64 * 40, T=8, dtype=dtype,
+                budget=W.Budget(W.BUDGET_FIXED, 13, 0, 0, 0, 0, 0), seed=21, n_planted=4,
+                permute_pages=True)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+def random_sel(B, H, NB, k, seed):
+    g = torch.Generator().manual_seed(seed)
+    sel = torch.full((B, H, max(k, 1)), -1, dtype=torch.int32)
+    for b in range(B):
+        for h in range(H):
+            if k:
+                sel[b, h, :k] = torch.sort(torch.randperm(NB, generator=g)[:k]).values.to(torch.int32)
+    return sel
+
+
+# ------------------------------------------------------------------ reps
+@pytest.mark.parametrize("dtype,d,blk", [("bf16", 128, 64), ("f32", 64, 16), ("bf16", 96, 32)])
+def test_build_reps(dtype, d, blk):
+    wl = small_wl(dtype, d=d, blk=blk, ctx=blk * 37)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    shape = api.make_shape(wl.B, wl.Hq, wl.Hkv, wl.d, wl.blk, wl.T, wl.torch_dtype)
+    kv = api.make_kv(xd.k_pool, xd.v_pool, xd.block_table, wl.ctx)
+    reps = torch.full((wl.B, wl.Hkv, wl.NB, wl.d), float("nan"), device="cuda")
+    # incremental: two ranges, a gap left untouched in between
+    api.sv_build_reps(shape, kv, 0, 20, reps)
+    api.sv_build_reps(shape, kv, 25, wl.NB - 25, reps)
+    torch.cuda.synchronize()
+    ref = O.block_representatives(x.k_pool, x.block_table, wl.NB, wl.blk)
+    got = reps.cpu().double()
+    assert torch.isnan(got[:, :, 20:25]).all()
+    keep = torch.cat([torch.arange(20), torch.arange(25, wl.NB)])
+    assert torch.allclose(got[:, :, keep], ref[:, :, keep], rtol=0, atol=1e-5)
+
+
+# ------------------------------------------------------------------ scores / select
+@pytest.mark.parametrize("dtype,d,G", [("bf16", 128, 4), ("f32", 64, 2), ("bf16", 256, 8)])
+def test_score_blocks(dtype, d, G):
+    wl = small_wl(dtype, d=d, Hkv=2, Hq=2 * G, blk=32, ctx=32 * 301)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    shape = api.make_shape(wl.B, wl.Hq, wl.Hkv, wl.d, wl.blk, wl.T, wl.torch_dtype)
+    kv = api.make_kv(xd.k_pool, xd.v_pool, xd.block_table, wl.ctx)
+    reps_ref = O.block_representatives(x.k_pool, x.block_table, wl.NB, wl.blk)
+    reps = reps_ref.float().cuda()  # exact oracle reps, rounded to the fp32 the ABI takes
+    scores = torch.empty(wl.B, wl.Hkv, wl.NB, device="cuda")
+    api.sv_score_blocks(shape, xd.q, reps, kv, scores)
+    torch.cuda.synchronize()
+    ref = O.block_scores(x.q, reps.cpu().double(), wl.G)
+    assert torch.allclose(scores.cpu().double(), ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("nb,k", [(64, 8), (512, 64), (2048, 128), (1000, 999), (37, 37), (37, 50),
+                                  (1, 1), (16384, 1024), (300, 0)])
+def test_select_blocks_exact(nb, k):
+    """Host-made scores with many ties (small integers), +-0 and negatives:
+    the GPU selection must equal the oracle's, bit for bit."""
+    g = torch.Generator().manual_seed(nb * 7 + k)
+    B, H = 2, 3
+    scores = torch.randint(-20, 21, (B, H, nb), generator=g).float() * 0.25
+    scores[0, 0, ::7] = -0.0
+    scores[1, 2] = torch.randn(nb, generator=g)  # one row without ties
+    shape = api.make_shape(B, 4 * H, H, 64, 64, 4, torch.bfloat16)
+    kmax = max(k, 1) + 3
+    sel = torch.zeros(B, H, kmax, dtype=torch.int32, device="cuda")
+    api.sv_select_blocks(shape, scores.cuda(), nb, k, sel, kmax)
+    torch.cuda.synchronize()
+    s = sel.cpu()
+    for b in range(B):
+        for h in range(H):
+            want = O.select_blocks(scores[b, h].tolist(), k)
+            kk = len(want)
+            assert s[b, h, :kk].tolist() == want, (b, h)
+            assert (s[b, h, kk:] == -1).all()
+
+
+def test_score_select_vs_oracle():
+    wl = small_wl(ctx=64 * 150, budget=W.Budget(W.BUDGET_FIXED, 21, 0, 0, 0, 0, 0))
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    k = api.sv_score_select(st.shape, xd.q, st.reps, st.kv, wl.budget, st.sel, st.kmax, st.ws)
+    torch.cuda.synchronize()
+    assert k == 21
+    reps_ref = O.block_representatives(x.k_pool, x.block_table, wl.NB, wl.blk)
+    ref_scores = O.block_scores(x.q, reps_ref, wl.G)
+    U.compare_selection(st.sel.cpu(), ref_scores, k)
+    # the kernel's top-k is exact on its own fp32 scores
+    scores = torch.empty(wl.B, wl.Hkv, wl.NB, device="cuda")
+    api.sv_score_blocks(st.shape, xd.q, st.reps, st.kv, scores)
+    torch.cuda.synchronize()
+    U.check_topk_property(st.sel.cpu(), scores.cpu(), k)
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            assert set(x.planted[b, h].tolist()) <= set(st.sel[b, h].cpu().tolist())
+
+
+# ------------------------------------------------------------------ attend
+ATTEND_CASES = [
+    # name, workload overrides, n_sel
+    ("fast_d128_blk64_R32", dict(), 13),
+    ("fast_d128_blk64_R32_ragged", dict(B=3, ctx=64 * 77), 61),
+    ("fast_tree16_G8_R128", dict(Hq=16, Hkv=2, T=16, parents=W.TREE16_PARENTS), 29),
+    ("fast_R16_pad", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), 17),
+    ("fast_R48_rows_pad", dict(Hq=8, Hkv=2, T=12, blk=32, ctx=32 * 45), 9),
+    ("fast_T1_G1", dict(Hq=2, Hkv=2, T=1), 5),
+    ("fast_nsel0_drafts_only", dict(), 0),
+    ("fast_all_blocks", dict(ctx=64 * 24), 24),
+    ("generic_f32", dict(dtype="f32", d=64, blk=16, ctx=16 * 64, Hq=4, Hkv=2, T=4), 8),
+    ("generic_d96", dict(d=96, blk=32, ctx=32 * 40), 11),
+    ("generic_T_gt_blk", dict(T=40, Hq=2, Hkv=1, blk=32, ctx=32 * 30), 7),
+    ("generic_R256", dict(T=32, Hq=16, Hkv=2, ctx=64 * 20), 6),
+    ("generic_blk16_bf16", dict(blk=16, ctx=16 * 90), 19),
+]
+
+
+@pytest.mark.parametrize("name,over,n_sel", ATTEND_CASES, ids=[c[0] for c in ATTEND_CASES])
+def test_sparse_attend(name, over, n_sel):
+    over = dict(over)
+    dtype = over.pop("dtype", "bf16")
+    wl = small_wl(dtype, **over)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, kmax=max(n_sel, 1), build_reps=False)
+    sel = random_sel(wl.B, wl.Hkv, wl.NB, n_sel, seed=len(name))
+    out = torch.zeros_like(xd.q)
+    api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, sel.shape[-1], xd.draft_k,
+                         xd.draft_v, st.parents, out, st.ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    ref = O.sparse_attend(x.q, x.k_pool, x.v_pool, x.block_table, sel[:, :, :n_sel].long(),
+                          x.draft_k, x.draft_v, wl.parent_list())
+    U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_dense_attend(dtype):
+    over = dict(ctx=64 * 33) if dtype == "bf16" else dict(d=64, blk=16, ctx=16 * 70, T=5,
+                                                           parents=(-1, 0, 0, 1, 2))
+    wl = small_wl(dtype, **over)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, build_reps=False)
+    out = torch.zeros_like(xd.q)
+    api.sv_sparse_attend(st.shape, xd.q, st.kv, None, 0, 0, xd.draft_k, xd.draft_v, st.parents,
+                         out, st.ws)
+    torch.cuda.synchronize()
+    ref = O.dense_verify_attention(x.q, O.logical_kv(x.k_pool, x.block_table, wl.NB),
+                                   O.logical_kv(x.v_pool, x.block_table, wl.NB), x.draft_k,
+                                   x.draft_v, wl.parent_list())
+    U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
+
+
+def test_value_ones_gives_ones():
+    wl = small_wl(ctx=64 * 30)
+    x = W.make_layer(wl)
+    x.v_pool = torch.ones_like(x.v_pool)
+    x.draft_v = torch.ones_like(x.draft_v)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    out = st.verify()
+    torch.cuda.synchronize()
+    assert (out.float() - 1).abs().max().item() <= 2 ** -8
+
+
+# ------------------------------------------------------------------ verify layer
+def _verify_vs_oracle(wl, x, xd, pairs=None):
+    """Run sv_verify_layer on the device, recompute (b, h) pairs on the CPU
+    oracle (all pairs by default) and compare selection and outputs."""
+    st = api.LayerState(wl, xd)
+    out = st.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    k = st.k
+    if pairs is None:
+        pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+    gsel = st.sel.cpu()
+    gout = out.cpu()
+    by_b = {}
+    for b, h in pairs:
+        by_b.setdefault(b, []).append(h)
+    worst = 0.0
+    for b, hs in by_b.items():
+        qb = x.q[b:b + 1]
+        btb = x.block_table[b:b + 1]
+        reps = O.block_representatives(x.k_pool, btb, wl.NB, wl.blk)
+        scores = O.block_scores(qb, reps, wl.G)
+        sub_scores = scores[:, hs]
+        differ = U.compare_selection(gsel[b:b + 1, hs], sub_scores, k)
+        sel = O.select_all(scores, k)
+        ref = O.sparse_attend(qb, x.k_pool, x.v_pool, btb, sel, x.draft_k[b:b + 1],
+                              x.draft_v[b:b + 1], wl.parent_list())
+        for i, h in enumerate(hs):
+            if (0, i) in differ:
+                continue
+            cols = slice(h * wl.G, (h + 1) * wl.G)
+            err = (gout[b:b + 1, :, cols].double() - ref[:, :, cols]).abs().max().item()
+            worst = max(worst, err)
+            assert err <= U.out_atol(wl.torch_dtype), (b, h, err)
+    return worst
+
+
+def test_verify_tiny_f32():
+    wl = W.WORKLOADS["tiny_f32"]
+    x = W.make_layer(wl)
+    _verify_vs_oracle(wl, x, x.to("cuda"))
+
+
+def test_verify_llama8b_32k_full():
+    wl = W.WORKLOADS["llama8b_32k"]
+    x = W.make_layer(wl)
+    _verify_vs_oracle(wl, x, x.to("cuda"))
+
+
+def test_verify_empty_context():
+    wl = small_wl(ctx=0)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    out = st.verify()
+    torch.cuda.synchronize()
+    ref = O.sparse_attend(x.q, x.k_pool, x.v_pool, x.block_table,
+                          torch.zeros(wl.B, wl.Hkv, 0, dtype=torch.int64), x.draft_k, x.draft_v,
+                          wl.parent_list())
+    U.compare_out(out, ref, U.BF16_ATOL)
+
+
+def test_verify_short_context_keeps_all_blocks():
+    wl = small_wl(ctx=64 * 48, budget=W.PIECEWISE_6P25_ABOVE_32K)  # 3072 <= 4096: all blocks
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    out = st.verify()
+    torch.cuda.synchronize()
+    assert st.k == wl.NB
+    assert (st.sel.cpu()[:, :, :wl.NB] == torch.arange(wl.NB, dtype=torch.int32)).all()
+    ref = O.dense_verify_attention(x.q, O.logical_kv(x.k_pool, x.block_table, wl.NB),
+                                   O.logical_kv(x.v_pool, x.block_table, wl.NB), x.draft_k,
+                                   x.draft_v, wl.parent_list())
+    U.compare_out(out, ref, U.BF16_ATOL)
+
+
+@pytest.mark.slow
+def test_verify_llama8b_128k_b4_sampled():
+    wl = W.WORKLOADS["llama8b_128k_b4"]
+    xd = W.make_layer(wl, device="cuda")
+    x = xd.to("cpu")
+    _verify_vs_oracle(wl, x, xd, pairs=[(0, 0), (1, 5), (3, 7), (2, 2)])
+
+
+@pytest.mark.slow
+def test_verify_qwen3moe_tree_sampled():
+    wl = W.WORKLOADS["qwen3moe_64k_b8_tree16"]
+    xd = W.make_layer(wl, device="cuda")
+    x = xd.to("cpu")
+    _verify_vs_oracle(wl, x, xd, pairs=[(0, 0), (3, 1), (7, 3), (5, 2)])
+
+
+@pytest.mark.slow
+def test_stack_llama8b_60k_reuse():
+    """32-layer stack with selection recomputed every 2nd layer: reuse layers
+    attend to exactly the previous layer's selection; layers 0..3 against the
+    oracle stack, every layer's output finite."""
+    wl = W.WORKLOADS["llama8b_60k_32layer"]
+    ps = W.planted_sets(wl)
+    sels, outs, states = [], [], []
+    cpu_layers = []
+    prev = None
+    for l in range(wl.layers):
+        xd = W.make_layer(wl, l, device="cuda", planted=ps[l])
+        st = api.LayerState(wl, xd)
+        reuse = l % wl.compute_every != 0
+        if reuse:
+            st.sel = prev.sel.clone()
+        st.verify(reuse=int(reuse))
+        torch.cuda.synchronize()
+        sels.append(st.sel.cpu())
+        outs.append(st.out.cpu())
+        if l < 4:
+            x = xd.to("cpu")
+            cpu_layers.append((x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k, x.draft_v))
+        prev = st
+        del xd
+    for l in range(1, wl.layers, 2):
+        assert torch.equal(sels[l], sels[l - 1])
+    for o in outs:
+        assert torch.isfinite(o.float()).all()
+    ref_outs, ref_sels = O.verify_stack(cpu_layers, wl.parent_list(), wl.ctx, wl.blk, wl.budget,
+                                        wl.compute_every)
+    for l in range(4):
+        if l % 2 == 0:
+            reps = O.block_representatives(cpu_layers[l][1], cpu_layers[l][3], wl.NB, wl.blk)
+            scores = O.block_scores(cpu_layers[l][0], reps, wl.G)
+            differ = U.compare_selection(sels[l], scores, ref_sels[l].shape[-1])
+            assert not differ
+        U.compare_out(outs[l], ref_outs[l], U.BF16_ATOL)
+
+
+# ------------------------------------------------------------------ device-side checks
+def test_bad_indices_flagged_not_faulting():
+    """A selected block outside [0, NB) and a block-table entry outside the
+    pool are skipped and reported through the status word."""
+    wl = small_wl(ctx=64 * 20)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, kmax=4, build_reps=False)
+    sel = torch.tensor([[[0, 3, 5, wl.NB + 7]] * wl.Hkv] * wl.B, dtype=torch.int32).cuda()
+    out = torch.zeros_like(xd.q)
+    api.sv_sparse_attend(st.shape, xd.q, st.kv, sel, 4, 4, xd.draft_k, xd.draft_v, None, out, st.ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) & api.SV_FLAG_BAD_BLOCK_INDEX
+    api.sv_clear_status(st.ws)
+    bt = xd.block_table.clone()
+    bt[0, 3] = x.k_pool.shape[0] + 100
+    kv = api.make_kv(xd.k_pool, xd.v_pool, bt, wl.ctx)
+    sel2 = torch.tensor([[[0, 3, 5, 6]] * wl.Hkv] * wl.B, dtype=torch.int32).cuda()
+    api.sv_sparse_attend(st.shape, xd.q, kv, sel2, 4, 4, xd.draft_k, xd.draft_v, None, out, st.ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) & api.SV_FLAG_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
