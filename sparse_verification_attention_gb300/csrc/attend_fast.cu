@@ -399,6 +399,8 @@ int attend_fast_ctas_per_sm(const AttendArgs& a, int dtype) {
   if (!(a.d == 64 || a.d == 128)) return 0;
   if (!(a.blk == 32 || a.blk == 64)) return 0;
   if (a.rpad > 128 || a.T > a.blk) return 0;
+  // an empty cache (no pages) has no tensor map to encode
+  if (a.num_pages < 1 || !a.k_pool || !a.v_pool) return 0;
   if ((reinterpret_cast<uintptr_t>(a.k_pool) & 15) || (reinterpret_cast<uintptr_t>(a.v_pool) & 15))
     return 0;
   if ((long long)(a.num_pages + 1) * a.Hkv * a.blk >= (1ll << 31)) return 0;

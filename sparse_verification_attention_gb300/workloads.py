@@ -163,7 +163,8 @@ def planted_sets(wl: Workload) -> list[torch.Tensor]:
     cur = torch.empty(wl.B, wl.Hkv, n, dtype=torch.int64)
     for b in range(wl.B):
         for h in range(wl.Hkv):
-            cur[b, h] = 1 + torch.randperm(NB - 1, generator=g)[:n]
+            if n:
+                cur[b, h] = 1 + torch.randperm(NB - 1, generator=g)[:n]
     out.append(cur.clone())
     for _ in range(1, wl.layers):
         nxt = cur.clone()
