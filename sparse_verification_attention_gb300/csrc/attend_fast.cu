@@ -22,6 +22,8 @@
 //     kernel combines the splits with log-sum-exp weights.
 //   * every wait is bounded: on timeout a status flag is raised and the CTA
 //     drains its own copies before leaving; no spin can hang the GPU.
+#include <cooperative_groups.h>
+
 #include <atomic>
 
 #include "internal.h"
@@ -30,14 +32,22 @@
 namespace sva {
 namespace {
 
-template <int D, int BLK, int NWC, int NS>
+template <int D, int BLK, int NWC, int NS, bool CLUSTER>
 struct FastCfg {
   static constexpr int kBoxes = D / 64;           // 128-byte-wide TMA boxes per tile
   static constexpr int kBoxBytes = BLK * 128;     // BLK rows x 64 bf16
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
   static constexpr int kThreads = 32 * (NWC + 1);
-  static constexpr int kSmem = NS * kStageBytes + 1024 + 256;
+  // The cluster merge stages the partial (o, m, l) and merge weights in the
+  // ring once the ring is idle; the ring is sized to hold them.
+  static constexpr int kOst = D + 4;              // padded fp32 row stride of the staged o
+  static constexpr int kRows = 16 * NWC;
+  static constexpr int kMergeBytes = (kRows * kOst + kRows * 2 + kRows * 16) * 4;
+  static constexpr int kRingRaw = NS * kStageBytes;
+  static constexpr int kRing =
+      ((CLUSTER && kMergeBytes > kRingRaw ? kMergeBytes : kRingRaw) + 1023) / 1024 * 1024;
+  static constexpr int kSmem = kRing + 1024 + 256;  // + alignment slack + barriers
   static_assert(BLK % 16 == 0 && D % 64 == 0, "tile shape");
 };
 
@@ -149,26 +159,30 @@ struct Consumer {
   }
 };
 
-template <int D, int BLK, int NWC, int NS>
+template <int D, int BLK, int NWC, int NS, bool CLUSTER>
 __global__ void __launch_bounds__(32 * (NWC + 1))
     attend_fast_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ AttendArgs a) {
-  using C = FastCfg<D, BLK, NWC, NS>;
+  using C = FastCfg<D, BLK, NWC, NS, CLUSTER>;
+  constexpr int NT = 32 * (NWC + 1);
+  constexpr int OST = C::kOst;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);
   uint64_t* empty = full + NS;
   int* stage_ok = reinterpret_cast<int*>(empty + NS);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = b * a.Hkv + h;
-  const int j0 = split * a.bps;
-  const int j1 = min(a.n_sel, j0 + a.bps);
-  const int nblk = max(0, j1 - j0);
-  const bool has_draft = (split == a.n_splits - 1);
+  // Work units of this (b, h): the n_sel selected blocks, then the draft tile.
+  const int u0 = split * a.bps;
+  const int u1 = min(a.n_sel + 1, u0 + a.bps);
+  const int j0 = u0;
+  const int nblk = max(0, min(u1, a.n_sel) - u0);
+  const bool has_draft = (u0 <= a.n_sel && a.n_sel < u1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -176,18 +190,19 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
       mbar_init(smem_u32(&empty[s]), NWC);
     }
     fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
   }
   __syncthreads();
+  pdl_wait();  // everything below may read what earlier kernels wrote
 
+  Consumer<D, BLK, NWC> cs;
+  const int g = lane >> 2, t4 = lane & 3;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp resolves 32 selected blocks at a time (selection entry,
     // then block-table page) so that these dependent global loads overlap;
     // lane 0 then issues the copies in order.
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
     const int oob_row = a.num_pages * a.Hkv * BLK;  // past the end: TMA zero-fills
     int issued = 0;
     bool stop = false;
@@ -239,182 +254,281 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
         }
       }
     }
-    // Never leave with a bulk copy still writing into this CTA's memory.
+    // Never leave the ring with a bulk copy still writing into it.
     if (lane == 0)
       for (int i = max(0, issued - NS); i < issued; ++i)
         mbar_wait(smem_u32(&full[i % NS]), (i / NS) & 1, kSpinLimit);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;
-  const int g = lane >> 2, t4 = lane & 3;
-  Consumer<D, BLK, NWC> cs;
-  cs.r_lo = 16 * cw + g;
-  cs.r_hi = cs.r_lo + 8;
-  {
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* qlo = nullptr;
-    const __nv_bfloat16* qhi = nullptr;
-    if (cs.r_lo < a.R)
-      qlo = q + (((size_t)b * a.T + cs.r_lo / a.G) * a.Hq + h * a.G + cs.r_lo % a.G) * D;
-    if (cs.r_hi < a.R)
-      qhi = q + (((size_t)b * a.T + cs.r_hi / a.G) * a.Hq + h * a.G + cs.r_hi % a.G) * D;
+  } else {
+    // -------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    cs.r_lo = 16 * cw + g;
+    cs.r_hi = cs.r_lo + 8;
+    {
+      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+      const __nv_bfloat16* qlo = nullptr;
+      const __nv_bfloat16* qhi = nullptr;
+      if (cs.r_lo < a.R)
+        qlo = q + (((size_t)b * a.T + cs.r_lo / a.G) * a.Hq + h * a.G + cs.r_lo % a.G) * D;
+      if (cs.r_hi < a.R)
+        qhi = q + (((size_t)b * a.T + cs.r_hi / a.G) * a.Hq + h * a.G + cs.r_hi % a.G) * D;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int col = 16 * kk + 2 * t4;
-      cs.qf[kk][0] = qlo ? ld_bf16x2(qlo + col) : 0u;
-      cs.qf[kk][1] = qhi ? ld_bf16x2(qhi + col) : 0u;
-      cs.qf[kk][2] = qlo ? ld_bf16x2(qlo + col + 8) : 0u;
-      cs.qf[kk][3] = qhi ? ld_bf16x2(qhi + col + 8) : 0u;
-    }
-  }
-#pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) cs.o[nd][0] = cs.o[nd][1] = cs.o[nd][2] = cs.o[nd][3] = 0.f;
-  cs.m_lo = cs.m_hi = -INFINITY;
-  cs.l_lo = cs.l_hi = 0.f;
-
-  const uint32_t sbase = smem_u32(smem);
-  for (int i = 0; i < nblk; ++i) {
-    const int s = i % NS;
-    if (!mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit)) {
-      atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      break;
-    }
-    if (stage_ok[s]) {
-      const uint32_t kb = sbase + s * C::kStageBytes;
-      cs.tile(kb, kb + C::kTileBytes, a, false, lane);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-  }
-
-  if (has_draft) {
-    // Draft tile: draft K/V rows u < T (rows T..BLK-1 zero) copied into stage
-    // 0 in the same swizzled layout, then one masked tile.
-    asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
-    const int ctid = threadIdx.x - 32;
-    const uint4* dk = static_cast<const uint4*>(a.draft_k);
-    const uint4* dv = static_cast<const uint4*>(a.draft_v);
-    for (int idx = ctid; idx < BLK * (D / 8); idx += NWC * 32) {
-      const int u = idx / (D / 8), c = idx % (D / 8);
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (u < a.T) {
-        const size_t off = (((size_t)b * a.T + u) * a.Hkv + h) * (D / 8) + c;
-        kv = dk[off];
-        vv = dv[off];
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int col = 16 * kk + 2 * t4;
+        cs.qf[kk][0] = qlo ? ld_bf16x2(qlo + col) : 0u;
+        cs.qf[kk][1] = qhi ? ld_bf16x2(qhi + col) : 0u;
+        cs.qf[kk][2] = qlo ? ld_bf16x2(qlo + col + 8) : 0u;
+        cs.qf[kk][3] = qhi ? ld_bf16x2(qhi + col + 8) : 0u;
       }
-      const uint32_t o = swz<D, BLK>(u, 8 * c);
-      *reinterpret_cast<uint4*>(smem + o) = kv;
-      *reinterpret_cast<uint4*>(smem + C::kTileBytes + o) = vv;
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
-    cs.tile(sbase, sbase + C::kTileBytes, a, true, lane);
-  }
-
-  // Partial results: unnormalised o, running max m (log2 domain), sum l.
-  float l_lo = cs.l_lo, l_hi = cs.l_hi;
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    const int col = 8 * nd + 2 * t4;
-    if (cs.r_lo < a.rpad)
-      *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_lo) * D + col) =
-          make_float2(cs.o[nd][0], cs.o[nd][1]);
-    if (cs.r_hi < a.rpad)
-      *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_hi) * D + col) =
-          make_float2(cs.o[nd][2], cs.o[nd][3]);
+    for (int nd = 0; nd < D / 8; ++nd) cs.o[nd][0] = cs.o[nd][1] = cs.o[nd][2] = cs.o[nd][3] = 0.f;
+    cs.m_lo = cs.m_hi = -INFINITY;
+    cs.l_lo = cs.l_hi = 0.f;
+
+    const uint32_t sbase = smem_u32(smem);
+    for (int i = 0; i < nblk; ++i) {
+      const int s = i % NS;
+      if (!mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit)) {
+        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+        break;
+      }
+      if (stage_ok[s]) {
+        const uint32_t kb = sbase + s * C::kStageBytes;
+        cs.tile(kb, kb + C::kTileBytes, a, false, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+
+    if (has_draft) {
+      // Draft tile: draft K/V rows u < T (rows T..BLK-1 zero) written into
+      // stage 0 in the same swizzled layout, then one masked tile.
+      asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
+      const int ctid = threadIdx.x - 32;
+      const uint4* dk = static_cast<const uint4*>(a.draft_k);
+      const uint4* dv = static_cast<const uint4*>(a.draft_v);
+      for (int idx = ctid; idx < BLK * (D / 8); idx += NWC * 32) {
+        const int u = idx / (D / 8), c = idx % (D / 8);
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        if (u < a.T) {
+          const size_t off = (((size_t)b * a.T + u) * a.Hkv + h) * (D / 8) + c;
+          kv = dk[off];
+          vv = dv[off];
+        }
+        const uint32_t o = swz<D, BLK>(u, 8 * c);
+        *reinterpret_cast<uint4*>(smem + o) = kv;
+        *reinterpret_cast<uint4*>(smem + C::kTileBytes + o) = vv;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
+      cs.tile(sbase, sbase + C::kTileBytes, a, true, lane);
+    }
+    cs.l_lo += __shfl_xor_sync(0xffffffffu, cs.l_lo, 1);
+    cs.l_lo += __shfl_xor_sync(0xffffffffu, cs.l_lo, 2);
+    cs.l_hi += __shfl_xor_sync(0xffffffffu, cs.l_hi, 1);
+    cs.l_hi += __shfl_xor_sync(0xffffffffu, cs.l_hi, 2);
   }
-  if (t4 == 0) {
-    if (cs.r_lo < a.rpad)
-      *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_lo) * 2) = make_float2(cs.m_lo, l_lo);
-    if (cs.r_hi < a.rpad)
-      *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_hi) * 2) = make_float2(cs.m_hi, l_hi);
+  pdl_trigger();
+
+  if constexpr (CLUSTER) {
+    // ------------------------------------------------ in-cluster merge (DSMEM)
+    // Every CTA of the cluster holds one split of the same (b, h). Each stages
+    // its unnormalised partial (o, m, l) in its own shared memory; after a
+    // cluster barrier, CTA r combines rows [r*rows, (r+1)*rows) across all
+    // peers with log-sum-exp weights and writes the output.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int nsplit = (int)cl.num_blocks();
+    const int rank = (int)cl.block_rank();
+    float* po = reinterpret_cast<float*>(smem);                 // [rpad][OST]
+    float* pml = po + (size_t)a.rpad * OST;                     // [rpad][2]
+    float* wgt = pml + (size_t)a.rpad * 2;                      // [rows][nsplit]
+    __syncthreads();  // ring and draft tile no longer read by anyone
+    if (warp > 0) {
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int col = 8 * nd + 2 * t4;
+        if (cs.r_lo < a.rpad)
+          *reinterpret_cast<float2*>(po + cs.r_lo * OST + col) = make_float2(cs.o[nd][0], cs.o[nd][1]);
+        if (cs.r_hi < a.rpad)
+          *reinterpret_cast<float2*>(po + cs.r_hi * OST + col) = make_float2(cs.o[nd][2], cs.o[nd][3]);
+      }
+      if (t4 == 0) {
+        if (cs.r_lo < a.rpad) *reinterpret_cast<float2*>(pml + 2 * cs.r_lo) = make_float2(cs.m_lo, cs.l_lo);
+        if (cs.r_hi < a.rpad) *reinterpret_cast<float2*>(pml + 2 * cs.r_hi) = make_float2(cs.m_hi, cs.l_hi);
+      }
+    }
+    cl.sync();
+    const int rows = (a.R + nsplit - 1) / nsplit;
+    const int r0 = rank * rows;
+    const int r1 = min(a.R, r0 + rows);
+    for (int r = r0 + threadIdx.x; r < r1; r += NT) {
+      float M = -INFINITY;
+      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, cl.map_shared_rank(pml, s)[2 * r]);
+      float L = 0.f;
+      for (int s = 0; s < nsplit; ++s) {
+        const float2 ml = *reinterpret_cast<const float2*>(cl.map_shared_rank(pml, s) + 2 * r);
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        wgt[(r - r0) * nsplit + s] = w;
+        L += w * ml.y;
+      }
+      const float inv = 1.0f / L;
+      for (int s = 0; s < nsplit; ++s) wgt[(r - r0) * nsplit + s] *= inv;
+    }
+    __syncthreads();
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    for (int idx = threadIdx.x; idx < (r1 - r0) * (D / 4); idx += NT) {
+      const int r = r0 + idx / (D / 4), c = (idx % (D / 4)) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < nsplit; ++s) {
+        const float w = wgt[(r - r0) * nsplit + s];
+        const float4 o = *reinterpret_cast<const float4*>(cl.map_shared_rank(po, s) + r * OST + c);
+        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+      }
+      const int t = r / a.G, gq = r % a.G;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * D + c) = u;
+    }
+    cl.sync();  // peers may still be reading this CTA's shared memory
+  } else {
+    // -------------------------------------------- partials for the merge kernel
+    if (warp > 0) {
+      const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int col = 8 * nd + 2 * t4;
+        if (cs.r_lo < a.rpad)
+          *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_lo) * D + col) =
+              make_float2(cs.o[nd][0], cs.o[nd][1]);
+        if (cs.r_hi < a.rpad)
+          *reinterpret_cast<float2*>(a.part_o + (slot + cs.r_hi) * D + col) =
+              make_float2(cs.o[nd][2], cs.o[nd][3]);
+      }
+      if (t4 == 0) {
+        if (cs.r_lo < a.rpad)
+          *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_lo) * 2) = make_float2(cs.m_lo, cs.l_lo);
+        if (cs.r_hi < a.rpad)
+          *reinterpret_cast<float2*>(a.part_ml + (slot + cs.r_hi) * 2) = make_float2(cs.m_hi, cs.l_hi);
+      }
+    }
   }
 }
 
-template <int D, int BLK, int NWC>
-cudaError_t launch_cfg(const AttendArgs& a, cudaStream_t st) {
-  constexpr int NS = 3;
-  using C = FastCfg<D, BLK, NWC, NS>;
+template <int D, int BLK, int NWC, bool CLUSTER>
+struct FastKernel {
+  static constexpr int NS = 3;
+  using C = FastCfg<D, BLK, NWC, NS, CLUSTER>;
+  static void* fn() { return reinterpret_cast<void*>(attend_fast_kernel<D, BLK, NWC, NS, CLUSTER>); }
+};
+
+template <int D, int BLK, int NWC, bool CLUSTER>
+cudaError_t launch_cfg(const AttendArgs& a, int cluster, cudaStream_t st) {
+  using K = FastKernel<D, BLK, NWC, CLUSTER>;
   CUtensorMap mk, mv;
   const char* why = nullptr;
   if (!encode_pool_map(&mk, a.k_pool, a.num_pages, a.Hkv, BLK, D, &why) ||
       !encode_pool_map(&mv, a.v_pool, a.num_pages, a.Hkv, BLK, D, &why))
     return cudaErrorInvalidValue;
-  auto kern = attend_fast_kernel<D, BLK, NWC, NS>;  // attribute set by occupancy_cfg
-  dim3 grid(a.n_splits, a.Hkv, a.B);
-  kern<<<grid, C::kThreads, C::kSmem, st>>>(mk, mv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits, a.Hkv, a.B);
+  cfg.blockDim = dim3(K::C::kThreads);
+  cfg.dynamicSmemBytes = K::C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (CLUSTER) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, attend_fast_kernel<D, BLK, NWC, K::NS, CLUSTER>, mk, mv, a);
 }
 
-template <int D, int BLK>
-cudaError_t launch_rows(const AttendArgs& a, cudaStream_t st) {
+template <int D, int BLK, bool CLUSTER>
+cudaError_t launch_rows(const AttendArgs& a, int cluster, cudaStream_t st) {
   const int nwc = a.rpad / 16;
-  if (nwc <= 1) return launch_cfg<D, BLK, 1>(a, st);
-  if (nwc <= 2) return launch_cfg<D, BLK, 2>(a, st);
-  if (nwc <= 4) return launch_cfg<D, BLK, 4>(a, st);
-  return launch_cfg<D, BLK, 8>(a, st);
+  if (nwc <= 1) return launch_cfg<D, BLK, 1, CLUSTER>(a, cluster, st);
+  if (nwc <= 2) return launch_cfg<D, BLK, 2, CLUSTER>(a, cluster, st);
+  if (nwc <= 4) return launch_cfg<D, BLK, 4, CLUSTER>(a, cluster, st);
+  return launch_cfg<D, BLK, 8, CLUSTER>(a, cluster, st);
 }
 
 // Sets the kernel's shared-memory attribute and returns its resident CTAs per
 // SM; computed once per device and cached.
-template <int D, int BLK, int NWC>
+template <int D, int BLK, int NWC, bool CLUSTER>
 int occupancy_cfg() {
-  constexpr int NS = 3;
-  using C = FastCfg<D, BLK, NWC, NS>;
+  using K = FastKernel<D, BLK, NWC, CLUSTER>;
   static std::atomic<int> cached[kMaxDevices];
   const int dev = current_device();
   const int c = cached[dev].load();
   if (c > 0) return c;
-  auto kern = attend_fast_kernel<D, BLK, NWC, NS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+  const int smem = K::C::kSmem;
+  if (cudaFuncSetAttribute(K::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K::fn(), K::C::kThreads, smem) !=
       cudaSuccess)
     return 0;
   cached[dev].store(n);
   return n;
 }
 
-template <int D, int BLK>
+template <int D, int BLK, bool CLUSTER>
 int occupancy_rows(const AttendArgs& a) {
   const int nwc = a.rpad / 16;
-  if (nwc <= 1) return occupancy_cfg<D, BLK, 1>();
-  if (nwc <= 2) return occupancy_cfg<D, BLK, 2>();
-  if (nwc <= 4) return occupancy_cfg<D, BLK, 4>();
-  return occupancy_cfg<D, BLK, 8>();
+  if (nwc <= 1) return occupancy_cfg<D, BLK, 1, CLUSTER>();
+  if (nwc <= 2) return occupancy_cfg<D, BLK, 2, CLUSTER>();
+  if (nwc <= 4) return occupancy_cfg<D, BLK, 4, CLUSTER>();
+  return occupancy_cfg<D, BLK, 8, CLUSTER>();
+}
+
+template <bool CLUSTER>
+int occupancy_any(const AttendArgs& a) {
+  if (a.d == 128 && a.blk == 64) return occupancy_rows<128, 64, CLUSTER>(a);
+  if (a.d == 128 && a.blk == 32) return occupancy_rows<128, 32, CLUSTER>(a);
+  if (a.d == 64 && a.blk == 64) return occupancy_rows<64, 64, CLUSTER>(a);
+  return occupancy_rows<64, 32, CLUSTER>(a);
 }
 
 }  // namespace
 
-int attend_fast_ctas_per_sm(const AttendArgs& a, int dtype) {
-  if (dtype != SV_BF16) return 0;
-  if (!(a.d == 64 || a.d == 128)) return 0;
-  if (!(a.blk == 32 || a.blk == 64)) return 0;
-  if (a.rpad > 128 || a.T > a.blk) return 0;
+bool attend_fast_applies(const AttendArgs& a, int dtype) {
+  if (dtype != SV_BF16) return false;
+  if (!(a.d == 64 || a.d == 128)) return false;
+  if (!(a.blk == 32 || a.blk == 64)) return false;
+  if (a.rpad > 128 || a.T > a.blk) return false;
   // an empty cache (no pages) has no tensor map to encode
-  if (a.num_pages < 1 || !a.k_pool || !a.v_pool) return 0;
+  if (a.num_pages < 1 || !a.k_pool || !a.v_pool) return false;
   if ((reinterpret_cast<uintptr_t>(a.k_pool) & 15) || (reinterpret_cast<uintptr_t>(a.v_pool) & 15))
-    return 0;
-  if ((long long)(a.num_pages + 1) * a.Hkv * a.blk >= (1ll << 31)) return 0;
-  if (a.d == 128 && a.blk == 64) return occupancy_rows<128, 64>(a);
-  if (a.d == 128 && a.blk == 32) return occupancy_rows<128, 32>(a);
-  if (a.d == 64 && a.blk == 64) return occupancy_rows<64, 64>(a);
-  return occupancy_rows<64, 32>(a);
+    return false;
+  if ((long long)(a.num_pages + 1) * a.Hkv * a.blk >= (1ll << 31)) return false;
+  return true;
 }
 
-cudaError_t launch_attend_fast(const AttendArgs& a, cudaStream_t st) {
-  if (a.d == 128 && a.blk == 64) return launch_rows<128, 64>(a, st);
-  if (a.d == 128 && a.blk == 32) return launch_rows<128, 32>(a, st);
-  if (a.d == 64 && a.blk == 64) return launch_rows<64, 64>(a, st);
-  if (a.d == 64 && a.blk == 32) return launch_rows<64, 32>(a, st);
+int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster) {
+  return cluster ? occupancy_any<true>(a) : occupancy_any<false>(a);
+}
+
+cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st) {
+  const bool cl = cluster > 0;
+  if (a.d == 128 && a.blk == 64)
+    return cl ? launch_rows<128, 64, true>(a, cluster, st) : launch_rows<128, 64, false>(a, 0, st);
+  if (a.d == 128 && a.blk == 32)
+    return cl ? launch_rows<128, 32, true>(a, cluster, st) : launch_rows<128, 32, false>(a, 0, st);
+  if (a.d == 64 && a.blk == 64)
+    return cl ? launch_rows<64, 64, true>(a, cluster, st) : launch_rows<64, 64, false>(a, 0, st);
+  if (a.d == 64 && a.blk == 32)
+    return cl ? launch_rows<64, 32, true>(a, cluster, st) : launch_rows<64, 32, false>(a, 0, st);
   return cudaErrorInvalidValue;
 }
 

@@ -8,6 +8,7 @@
 // the one selected block set; drafts additionally see themselves and their
 // ancestors (tree or chain mask among drafts).
 #include "internal.h"
+#include "ptx.h"
 
 namespace sva {
 namespace {
@@ -61,15 +62,18 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int pair = b * a.Hkv + h;
-  const int j0 = split * a.bps;
-  const int j1 = min(a.n_sel, j0 + a.bps);
-  const bool has_draft = (split == a.n_splits - 1);
+  // work units: the n_sel selected blocks, then the draft tile (unit n_sel)
+  const int u0 = split * a.bps;
+  const int u1 = min(a.n_sel + 1, u0 + a.bps);
+  const int j0 = u0, j1 = min(u1, a.n_sel);
+  const bool has_draft = (u0 <= a.n_sel && a.n_sel < u1);
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
   const T* q = static_cast<const T*>(a.q);
   const T* dk = static_cast<const T*>(a.draft_k);
   const T* dv = static_cast<const T*>(a.draft_v);
   const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
+  pdl_wait();
 
   for (int r = warp; r < a.R; r += nw) {
     const int t = r / a.G, gq = r % a.G;
@@ -118,6 +122,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
       a.part_ml[(slot + r) * 2 + 1] = st.l;
     }
   }
+  pdl_trigger();
 }
 
 template <typename T>
@@ -141,51 +146,50 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v
 constexpr int kMergeWarps = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ AttendArgs a) {
   const int pair = blockIdx.y;
   const int b = pair / a.Hkv, h = pair % a.Hkv;
   const int r = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= a.R) return;
-  const size_t base = (size_t)pair * a.n_splits * a.rpad;
-  float M = -INFINITY;
-  for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, a.part_ml[(base + (size_t)s * a.rpad + r) * 2]);
-  const int t = r / a.G, gq = r % a.G;
-  T* out = static_cast<T*>(a.out) + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * a.d;
-  for (int c = lane * 4; c < a.d; c += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    for (int s = 0; s < a.n_splits; ++s) {
-      const size_t row = base + (size_t)s * a.rpad + r;
-      const float m = a.part_ml[row * 2], l = a.part_ml[row * 2 + 1];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      L += w * l;
-      const float4 o = *reinterpret_cast<const float4*>(a.part_o + row * a.d + c);
-      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+  pdl_wait();
+  if (r < a.R) {
+    const size_t base = (size_t)pair * a.n_splits * a.rpad;
+    float M = -INFINITY;
+    for (int s = 0; s < a.n_splits; ++s)
+      M = fmaxf(M, a.part_ml[(base + (size_t)s * a.rpad + r) * 2]);
+    const int t = r / a.G, gq = r % a.G;
+    T* out = static_cast<T*>(a.out) + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * a.d;
+    for (int c = lane * 4; c < a.d; c += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+      for (int s = 0; s < a.n_splits; ++s) {
+        const size_t row = base + (size_t)s * a.rpad + r;
+        const float m = a.part_ml[row * 2], l = a.part_ml[row * 2 + 1];
+        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+        L += w * l;
+        const float4 o = *reinterpret_cast<const float4*>(a.part_o + row * a.d + c);
+        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+      }
+      const float inv = 1.0f / L;
+      store4<T>(out + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
-    const float inv = 1.0f / L;
-    store4<T>(out + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
+  pdl_trigger();
 }
 
 }  // namespace
 
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st) {
   dim3 grid(a.n_splits, a.Hkv, a.B);
-  if (dtype == SV_BF16)
-    attend_generic_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(a);
-  else
-    attend_generic_kernel<float><<<grid, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  if (dtype == SV_BF16) return launch_pdl(attend_generic_kernel<__nv_bfloat16>, grid, dim3(128), 0, st, a);
+  return launch_pdl(attend_generic_kernel<float>, grid, dim3(128), 0, st, a);
 }
 
-cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st) {
+cudaError_t launch_merge(const AttendArgs& a, int dtype, cudaStream_t st) {
   dim3 grid((a.R + kMergeWarps - 1) / kMergeWarps, a.B * a.Hkv);
   if (dtype == SV_BF16)
-    merge_kernel<__nv_bfloat16><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  else
-    merge_kernel<float><<<grid, kMergeWarps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeWarps * 32), 0, st, a);
+  return launch_pdl(merge_kernel<float>, grid, dim3(kMergeWarps * 32), 0, st, a);
 }
 
 }  // namespace sva

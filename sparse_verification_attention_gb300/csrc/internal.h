@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "sva.h"
 
 namespace sva {
@@ -20,12 +22,32 @@ constexpr int kStatusBytes = 256;  // workspace head: device status word
 // sets SV_FLAG_WAIT_TIMEOUT and gives up instead of hanging the GPU.
 constexpr uint32_t kSpinLimit = 1u << 22;
 
+// Every kernel is launched with programmatic stream serialization: it may
+// begin launching while the previous kernel in the stream drains, and calls
+// pdl_wait() before it touches any global memory that a predecessor might
+// read or write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace carve-up (offsets in bytes from the workspace base).
 struct WsLayout {
-  size_t status, scores, part_o, part_ml, total;
+  size_t status, ctr_score, ctr_attend, scores, part_o, part_ml, total;
   int rpad, slots;
 };
 WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax);
@@ -45,6 +67,11 @@ struct ScoreArgs {
   const float* reps;
   float* scores;
   int B, T, Hq, Hkv, G, d, nb, nb_max;
+  // fused selection (sel == nullptr: scores only): the last scoring CTA of
+  // each (b, h) selects k blocks into sel[b][h][0..kmax)
+  int32_t* sel;
+  int k, kmax;
+  unsigned* counters;  // [B*Hkv], zero between calls
 };
 cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st);
 
@@ -65,28 +92,31 @@ struct AttendArgs {
   const int32_t* sel;   // null: identity selection over NB blocks
   float* part_o;        // [B,Hkv,S,Rpad,d]
   float* part_ml;       // [B,Hkv,S,Rpad,2]
+  void* out;            // [B,T,Hq,d]
   unsigned* status;
   int B, T, Hq, Hkv, G, d, blk, R, rpad;
   int nb, nb_max, num_pages, n_sel, sel_stride;
-  int n_splits, bps;    // split s covers selected blocks [s*bps, min(n_sel,(s+1)*bps))
+  // Work units of a (b, h): the n_sel selected blocks, then the draft tile
+  // (unit n_sel). Split s covers units [s*bps, min(n_sel+1, (s+1)*bps)).
+  int n_splits, bps;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
 };
 
-// Fast path availability: bf16, d in {64,128}, blk in {32,64}, rpad <= 128,
-// T <= blk, 16-byte aligned pools. Returns the number of CTAs per SM the
-// fast path keeps resident (0 when it does not apply).
-int attend_fast_ctas_per_sm(const AttendArgs& a, int dtype);
-cudaError_t launch_attend_fast(const AttendArgs& a, cudaStream_t st);
+// Tensor-core path availability: bf16, d in {64,128}, blk in {32,64},
+// rpad <= 128, T <= blk, 16-byte aligned pools, a non-empty pool.
+bool attend_fast_applies(const AttendArgs& a, int dtype);
+// Resident CTAs per SM of the tensor-core kernel (cluster-merge variant or
+// global-partials variant) for this row count.
+int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster);
+// cluster > 0: splits of one (b, h) form a thread-block cluster of that size
+// (== n_splits) and merge through distributed shared memory; cluster == 0:
+// splits write global partials for launch_merge.
+cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st);
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
+// Log-sum-exp merge of the global split partials into out (any path).
+cudaError_t launch_merge(const AttendArgs& a, int dtype, cudaStream_t st);
 
-struct MergeArgs {
-  const float* part_o;
-  const float* part_ml;
-  void* out;  // [B,T,Hq,d]
-  int B, T, Hq, Hkv, G, d, R, rpad, n_splits;
-};
-cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st);
 
 // Per-device once-only setup results (kernel attributes, occupancy), so that
 // steady-state calls only launch kernels and can be captured in CUDA graphs.

@@ -5,7 +5,11 @@
 // the dot product between the first draft token's query and a representative
 // value of each KV block. The representative is read here as the mean of the
 // block's keys, accumulated in fp32.
+#include <atomic>
+
 #include "internal.h"
+#include "ptx.h"
+#include "topk.cuh"
 
 namespace sva {
 namespace {
@@ -26,30 +30,59 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 }
 
 // ------------------------------------------------------------------ reps
-// One CTA per (logical block, kv head, sequence); thread i of the CTA owns
-// 4 consecutive dims and walks the blk tokens of the page in order.
+// One CTA of kRepThreads per (logical block, kv head, sequence). Thread t owns
+// one 16-byte chunk of the head dimension (c = t % chunks) and one group of
+// tokens (g = t / chunks); each group sums its tokens in order, then the
+// groups are added in order through shared memory. All of a page's 16-byte
+// loads are independent, so the block is read in one memory round trip.
+constexpr int kRepThreads = 128;
+
 template <typename T>
-__global__ void build_reps_kernel(RepsArgs a) {
+__global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
+  constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte chunk
+  __shared__ float part[kRepThreads * VEC];
   const int j = a.first_block + blockIdx.x;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int i4 = threadIdx.x * 4;
-  if (i4 >= a.d) return;
+  const int chunks = a.d / VEC;
+  const int groups = kRepThreads / chunks;  // >= 1 since d <= 256
+  const int c = threadIdx.x % chunks, g = threadIdx.x / chunks;
+  pdl_wait();
   const int page = a.block_table[(size_t)b * a.nb_max + j];
-  float* dst = a.reps + (((size_t)b * a.Hkv + h) * a.nb_max + j) * a.d + i4;
+  float* dst = a.reps + (((size_t)b * a.Hkv + h) * a.nb_max + j) * a.d;
   if (page < 0 || page >= a.num_pages) {
     if (a.status && threadIdx.x == 0) atomicOr(a.status, SV_FLAG_BAD_PAGE);
-    *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = threadIdx.x; i < a.d; i += kRepThreads) dst[i] = 0.f;
     return;
   }
-  const T* src = static_cast<const T*>(a.k_pool) + ((size_t)page * a.Hkv + h) * a.blk * a.d + i4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int t = 0; t < a.blk; ++t) {
-    float4 v = load4<T>(src + (size_t)t * a.d);
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  if (g < groups) {
+    const T* src = static_cast<const T*>(a.k_pool) + ((size_t)page * a.Hkv + h) * a.blk * a.d;
+    const int per = (a.blk + groups - 1) / groups;
+    const int t0 = g * per, t1 = min(a.blk, t0 + per);
+    for (int t = t0; t < t1; ++t) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + (size_t)t * a.d) + c);
+      const T* v = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        if constexpr (sizeof(T) == 2) acc[e] += __bfloat162float(v[e]);
+        else acc[e] += v[e];
+      }
+    }
   }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) part[threadIdx.x * VEC + e] = acc[e];
+  __syncthreads();
   const float inv = 1.0f / (float)a.blk;
-  *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  for (int i = threadIdx.x; i < a.d; i += kRepThreads) {
+    const int ci = i / VEC, ei = i % VEC;
+    float sum = 0.f;
+    for (int gg = 0; gg < groups; ++gg) sum += part[(gg * chunks + ci) * VEC + ei];
+    dst[i] = sum * inv;
+  }
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------------ scores
@@ -65,11 +98,12 @@ constexpr int kRowsPerCta = kScoreWarps * kRowsPerWarp;
 constexpr int kMaxChunks = kMaxD / 4 / 32;  // float4 chunks per lane (d <= 256)
 
 template <typename T>
-__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const __grid_constant__ ScoreArgs a) {
   const int pair = blockIdx.y;  // b * Hkv + h
   const int b = pair / a.Hkv, h = pair % a.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nchunk = a.d / 4;
+  pdl_wait();
 
   // qhat = sum over the G query heads of KV head h of draft 0's query.
   float4 qh[kMaxChunks];
@@ -117,6 +151,29 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(ScoreArgs a) {
       if (lane == 0 && j < a.nb) a.scores[(size_t)pair * a.nb + j] = acc[u];
     }
   }
+  if (!a.sel) {
+    pdl_trigger();
+    return;
+  }
+
+  // Fused selection: the last CTA to finish scoring this (b, h) selects.
+  __shared__ unsigned s_last;
+  __shared__ TopkSmem<kScoreWarps * 32> tsm;
+  extern __shared__ uint32_t keys[];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&a.counters[pair], 1u);
+    s_last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    cta_topk<kScoreWarps * 32>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
+                               a.sel + (size_t)pair * a.kmax, a.kmax, keys, tsm);
+    if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
+  }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -124,22 +181,26 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(ScoreArgs a) {
 cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st) {
   if (a.n_blocks == 0) return cudaSuccess;
   dim3 grid(a.n_blocks, a.Hkv, a.B);
-  dim3 block(round_up(a.d / 4, 32));
   if (dtype == SV_BF16)
-    build_reps_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(a);
-  else
-    build_reps_kernel<float><<<grid, block, 0, st>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(build_reps_kernel<__nv_bfloat16>, grid, dim3(kRepThreads), 0, st, a);
+  return launch_pdl(build_reps_kernel<float>, grid, dim3(kRepThreads), 0, st, a);
 }
 
 cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st) {
   if (a.nb == 0) return cudaSuccess;
   dim3 grid((a.nb + kRowsPerCta - 1) / kRowsPerCta, a.B * a.Hkv);
-  if (dtype == SV_BF16)
-    score_kernel<__nv_bfloat16><<<grid, kScoreWarps * 32, 0, st>>>(a);
-  else
-    score_kernel<float><<<grid, kScoreWarps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  const size_t smem = a.sel ? (size_t)a.nb * sizeof(uint32_t) : 0;
+  auto kern = (dtype == SV_BF16) ? score_kernel<__nv_bfloat16> : score_kernel<float>;
+  static std::atomic<int> attr_set[kMaxDevices][2];
+  const int dev = current_device();
+  const int which = dtype == SV_BF16 ? 0 : 1;
+  if (!attr_set[dev][which].load()) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kMaxNB * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
+    attr_set[dev][which].store(1);
+  }
+  return launch_pdl(kern, grid, dim3(kScoreWarps * 32), smem, st, a);
 }
 
 }  // namespace sva

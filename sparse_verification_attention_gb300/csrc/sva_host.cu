@@ -103,22 +103,32 @@ int sm_count() {
   return n;
 }
 
-// Split planning: enough CTAs to fill every SM `per_sm` deep in one wave,
-// never more than one split per selected block, at most kMaxSplits.
-void plan_splits(int pairs, int n_sel, int per_sm, int* n_splits, int* bps) {
-  if (n_sel <= 0) {
-    *n_splits = 1;
-    *bps = 1;
-    return;
-  }
+// Split planning for the global-partials path: enough CTAs to fill every SM
+// `per_sm` deep in one wave, at most one split per work unit (a selected
+// block or the draft tile), at most `max_splits`.
+void plan_splits(int pairs, int n_units, int per_sm, int max_splits, int* n_splits, int* bps) {
   const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
   int s = slots / (pairs > 0 ? pairs : 1);
   if (s < 1) s = 1;
-  if (s > kMaxSplits) s = kMaxSplits;
-  if (s > n_sel) s = n_sel;
-  const int per = (n_sel + s - 1) / s;
+  if (s > max_splits) s = max_splits;
+  if (s > n_units) s = n_units;
+  const int per = (n_units + s - 1) / s;
   *bps = per;
-  *n_splits = (n_sel + per - 1) / per;
+  *n_splits = (n_units + per - 1) / per;
+}
+
+// Cluster size for the in-cluster merge path, or 0 when that path would leave
+// more than half of the GPU idle (few (b, h) pairs): the largest cluster of
+// at most 8 CTAs whose grid still fits in one wave.
+int plan_cluster(int pairs, int n_units, int per_sm, int* bps) {
+  const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
+  int c = 8;
+  while (c > 1 && pairs * c > slots) c >>= 1;
+  if (c > n_units) c = n_units;
+  if ((long long)pairs * c * 2 < slots) return 0;
+  const int per = (n_units + c - 1) / c;
+  *bps = per;
+  return (n_units + per - 1) / per;
 }
 
 void fill_ancestors(const int32_t* parent, int T, unsigned long long* anc) {
@@ -169,14 +179,16 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   WsLayout L;
   const int G = s.Hq / s.Hkv;
   L.rpad = round_up(s.T * G, 16);
-  int slots = kmax < 1 ? 1 : (kmax > kMaxSplits ? kMaxSplits : kmax);
-  L.slots = slots;
+  const int units = (kmax < 0 ? 0 : kmax) + 1;  // selected blocks + the draft tile
+  L.slots = units > kMaxSplits ? kMaxSplits : units;
   const size_t pairs = (size_t)s.B * s.Hkv;
   L.status = 0;
-  L.scores = kStatusBytes;
+  L.ctr_score = kStatusBytes;
+  L.ctr_attend = L.ctr_score + align256(pairs * sizeof(uint32_t));
+  L.scores = L.ctr_attend + align256(pairs * sizeof(uint32_t));
   L.part_o = L.scores + align256(pairs * (size_t)(nb_max > 0 ? nb_max : 1) * sizeof(float));
-  L.part_ml = L.part_o + align256(pairs * slots * (size_t)L.rpad * s.d * sizeof(float));
-  L.total = L.part_ml + align256(pairs * slots * (size_t)L.rpad * 2 * sizeof(float));
+  L.part_ml = L.part_o + align256(pairs * L.slots * (size_t)L.rpad * s.d * sizeof(float));
+  L.total = L.part_ml + align256(pairs * L.slots * (size_t)L.rpad * 2 * sizeof(float));
   return L;
 }
 
@@ -235,26 +247,24 @@ static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, c
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s->d));
   fill_ancestors(parent, s->T, a.anc);
 
-  const int fast = attend_fast_ctas_per_sm(a, s->dtype);
-  plan_splits(s->B * s->Hkv, n_sel, fast > 0 ? fast : 4, &a.n_splits, &a.bps);
-  if (a.n_splits > L.slots)
-    return fail(SV_ERR_WORKSPACE, "workspace sized for %d splits, plan needs %d", L.slots, a.n_splits);
-  cudaError_t e = (fast > 0) ? launch_attend_fast(a, st) : launch_attend_generic(a, s->dtype, st);
+  a.out = out;
+  const int pairs = s->B * s->Hkv;
+  const int n_units = n_sel + 1;
+  const bool fast = attend_fast_applies(a, s->dtype);
+  int cluster = 0;
+  if (fast) cluster = plan_cluster(pairs, n_units, attend_fast_ctas_per_sm(a, true), &a.bps);
+  cudaError_t e;
+  if (cluster > 0) {
+    a.n_splits = cluster;
+    e = launch_attend_fast(a, cluster, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+    return SV_OK;
+  }
+  const int per_sm = fast ? attend_fast_ctas_per_sm(a, false) : 4;
+  plan_splits(pairs, n_units, per_sm, L.slots, &a.n_splits, &a.bps);
+  e = fast ? launch_attend_fast(a, 0, st) : launch_attend_generic(a, s->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "attend launch");
-  MergeArgs m{};
-  m.part_o = a.part_o;
-  m.part_ml = a.part_ml;
-  m.out = out;
-  m.B = a.B;
-  m.T = a.T;
-  m.Hq = a.Hq;
-  m.Hkv = a.Hkv;
-  m.G = a.G;
-  m.d = a.d;
-  m.R = a.R;
-  m.rpad = a.rpad;
-  m.n_splits = a.n_splits;
-  e = launch_merge(m, s->dtype, st);
+  e = launch_merge(a, s->dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return SV_OK;
 }
@@ -273,13 +283,19 @@ static sv_status do_score_select(const sv_shape* s, const void* q, const float* 
                                  const sv_kv* kv, int k, int32_t* sel, int kmax, void* ws,
                                  const WsLayout& L, cudaStream_t st) {
   const int nb = kv->ctx / s->blk;
-  float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
-  ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max};
-  cudaError_t e = launch_score(sa, s->dtype, st);
-  if (e != cudaSuccess) return cuda_fail(e, "score launch");
-  SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax};
-  e = launch_select(se, st);
-  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(w + L.scores);
+  cudaError_t e;
+  if (nb == 0) {
+    // nothing to score: the selection is empty
+    SelectArgs se{scores, sel, s->B * s->Hkv, 0, 0, kmax};
+    e = launch_select(se, st);
+  } else {
+    ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max,
+                 sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score)};
+    e = launch_score(sa, s->dtype, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "score/select launch");
   return SV_OK;
 }
 
@@ -348,7 +364,7 @@ sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* rep
   if (!aligned(q, 16) || !aligned(reps, 16))
     return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
   ScoreArgs sa{q, reps, scores, shape->B, shape->T, shape->Hq, shape->Hkv,
-               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max};
+               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, nullptr, 0, 0, nullptr};
   cudaError_t e = launch_score(sa, shape->dtype, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "score launch");
 }

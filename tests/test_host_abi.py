@@ -79,12 +79,17 @@ def test_budget_rejects_invalid(L):
 def test_workspace_sizes(L):
     s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
     n = api.sv_workspace_bytes(s, 2048, 128)
-    # status + scores + partial o + partial (m, l), each 256-aligned
-    scores = 4 * 8 * 2048 * 4
-    part = 4 * 8 * 64 * 32 * 128 * 4
-    ml = 4 * 8 * 64 * 32 * 2 * 4
-    assert n == 256 + scores + part + ml
-    assert api.sv_workspace_bytes(s, 2048, 8) < n
+    # status + two per-(b,h) counter arrays + scores + split partials o and
+    # (m, l); 129 work units (128 blocks + the draft tile) capped at 64 splits
+    pairs = 4 * 8
+    ctrs = 2 * 256
+    scores = pairs * 2048 * 4
+    part = pairs * 64 * 32 * 128 * 4
+    ml = pairs * 64 * 32 * 2 * 4
+    assert n == 256 + ctrs + scores + part + ml
+    # 8 selected blocks + the draft tile = 9 split slots
+    n8 = api.sv_workspace_bytes(s, 2048, 8)
+    assert n8 == 256 + ctrs + scores + pairs * 9 * 32 * 128 * 4 + pairs * 9 * 32 * 2 * 4
     bad = api.make_shape(4, 30, 8, 128, 64, 8, torch.bfloat16)  # Hq % Hkv != 0
     assert api.sv_workspace_bytes(bad, 2048, 128) == 0
     assert api.sv_workspace_bytes(api.make_shape(1, 4, 2, 12, 16, 4, 1), 64, 8) == 0  # d % 8

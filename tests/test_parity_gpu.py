@@ -135,6 +135,14 @@ ATTEND_CASES = [
     ("fast_T1_G1", dict(Hq=2, Hkv=2, T=1), 5),
     ("fast_nsel0_drafts_only", dict(), 0),
     ("fast_all_blocks", dict(ctx=64 * 24), 24),
+    # many (b, h) pairs: splits of a pair form a thread-block cluster and merge
+    # through distributed shared memory
+    ("cluster_B8_H8_R32", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 13),
+    ("cluster_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                                 ctx=64 * 20), 11),
+    ("cluster_size3", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 2),
+    ("cluster_d64_blk32_R16", dict(B=8, Hq=16, Hkv=8, d=64, blk=32, ctx=32 * 40), 9),
+    ("cluster_all_blocks", dict(B=8, Hq=32, Hkv=8, ctx=64 * 10), 10),
     ("generic_f32", dict(dtype="f32", d=64, blk=16, ctx=16 * 64, Hq=4, Hkv=2, T=4), 8),
     ("generic_d96", dict(d=96, blk=32, ctx=32 * 40), 11),
     ("generic_T_gt_blk", dict(T=40, Hq=2, Hkv=1, blk=32, ctx=32 * 30), 7),
@@ -162,10 +170,14 @@ def test_sparse_attend(name, over, n_sel):
     U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "bf16_many_pairs"])
 def test_dense_attend(dtype):
-    over = dict(ctx=64 * 33) if dtype == "bf16" else dict(d=64, blk=16, ctx=16 * 70, T=5,
-                                                           parents=(-1, 0, 0, 1, 2))
+    if dtype == "bf16":
+        over = dict(ctx=64 * 33)
+    elif dtype == "bf16_many_pairs":
+        dtype, over = "bf16", dict(B=8, Hq=32, Hkv=8, ctx=64 * 21)
+    else:
+        over = dict(d=64, blk=16, ctx=16 * 70, T=5, parents=(-1, 0, 0, 1, 2))
     wl = small_wl(dtype, **over)
     x = W.make_layer(wl)
     xd = x.to("cuda")
@@ -227,6 +239,26 @@ def _verify_vs_oracle(wl, x, xd, pairs=None):
             worst = max(worst, err)
             assert err <= U.out_atol(wl.torch_dtype), (b, h, err)
     return worst
+
+
+def test_repeated_calls_identical():
+    """Scoring, selection and attention leave the workspace ready for the
+    next call: repeated calls give bit-identical selections and outputs."""
+    for over in (dict(), dict(B=8, Hq=32, Hkv=8, ctx=64 * 40)):
+        wl = small_wl(**over)
+        x = W.make_layer(wl)
+        st = api.LayerState(wl, x.to("cuda"))
+        outs, sels = [], []
+        for _ in range(3):
+            st.out.zero_()
+            st.sel.fill_(-7)
+            st.verify()
+            torch.cuda.synchronize()
+            outs.append(st.out.clone())
+            sels.append(st.sel.clone())
+        assert all(torch.equal(outs[0], o) for o in outs[1:])
+        assert all(torch.equal(sels[0], s) for s in sels[1:])
+        assert api.sv_read_status(st.ws) == 0
 
 
 def test_verify_tiny_f32():
