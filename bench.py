@@ -158,6 +158,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+_T0 = time.perf_counter()
+
+
+def log(msg: str):
+    print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
+def check_status(sets, where: str):
+    """Raise if any kernel of the bench raised a device-side status flag."""
+    from sparse_verification_attention_gb300 import api
+    for ss in sets:
+        for st in ss.layers:
+            flags = api.sv_read_status(st.ws)
+            if flags:
+                words = st.ws[:8].view(torch.int32).tolist()
+                raise RuntimeError(f"device status flags {flags:#x} after {where} (words {words})")
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -329,6 +347,7 @@ def run_gpu(args, wl, rank, world, dist):
     ps = W.planted_sets(wl)
     sets = [StepSet(wl, i, ps) for i in range(n_sets)]
     torch.cuda.synchronize()
+    log(f"{n_sets} input sets resident")
     stream = torch.cuda.current_stream()
 
     # one CUDA graph per input set, each holding one whole step
@@ -346,11 +365,8 @@ def run_gpu(args, wl, rank, world, dist):
             run_step(wl, ss)
         graphs.append(g)
     torch.cuda.synchronize()
-    for s in sets:
-        for st in s.layers:
-            flags = api.sv_read_status(st.ws)
-            if flags:
-                raise RuntimeError(f"device status flags {flags:#x}")
+    check_status(sets, "graph capture")
+    log("graphs captured")
 
     clocks = ClockSampler(dev)
     clocks.start()
@@ -367,6 +383,8 @@ def run_gpu(args, wl, rank, world, dist):
     barrier(dist)
     ms_total = e0.elapsed_time(e1)
     clk = clocks.stop()
+    check_status(sets, "timed steps")
+    log(f"timed steps done: {ms_total / args.steps * 1e3:.1f} us/step")
     ms_total = max_over_ranks(dist, ms_total)
     ms_step = ms_total / args.steps
     tokens = sum_over_ranks(dist, wl.B * wl.T * args.steps)
@@ -394,6 +412,8 @@ def run_gpu(args, wl, rank, world, dist):
     a1.record()
     torch.cuda.synchronize()
     attend_ms = a0.elapsed_time(a1) / (n_rep * wl.layers)
+    check_status(sets, "attention-only replays")
+    log(f"attention launches: {attend_ms * 1e3:.1f} us")
     peak, peak_kind = read_peaks()
     achieved = abytes / (attend_ms / 1e3) / 1e9
 
@@ -420,6 +440,8 @@ def run_gpu(args, wl, rank, world, dist):
 
     # e2e: the public call with host buffers, copies inside the timed region
     e2e = run_e2e(args, wl, sets, dist)
+    check_status(sets, "e2e")
+    log("e2e done")
 
     # CPU oracle baseline on a bounded sample (rank 0, N=1 only)
     cpu = None

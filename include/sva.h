@@ -189,6 +189,27 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
                            const int32_t* draft_parent, void* out, void* workspace,
                            size_t ws_bytes, void* stream);
 
+/* Which attention kernel and split plan sv_sparse_attend (and sv_verify_layer)
+ * uses for this shape, cache and number of selected blocks: path
+ * SV_PATH_TCGEN05 (bf16, d = 128, blk = 64, T*G <= 128: 5th-generation tensor
+ * cores with TMEM accumulators), SV_PATH_MMA_SYNC (bf16, d in {64,128},
+ * blk in {32,64}, T*G <= 128, T <= blk), else SV_PATH_CUDA_CORES; cluster > 0
+ * when the splits of one (b, h) merge inside a thread-block cluster of that
+ * size; split_extra > 0 when that many (b, h) pairs get n_splits + 1 splits.
+ * Queries the current device (occupancy); launches nothing. */
+#define SV_PATH_CUDA_CORES 0
+#define SV_PATH_MMA_SYNC 1
+#define SV_PATH_TCGEN05 2
+typedef struct {
+  int path;
+  int cluster;
+  int n_splits;          /* CTAs per (b, h)                            */
+  int blocks_per_split;  /* work units (selected blocks, draft tile)   */
+  int ctas_per_sm;       /* resident CTAs per SM the plan assumed      */
+  int split_extra;       /* pairs [0, split_extra) have n_splits + 1   */
+} sv_plan;
+sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_plan* out);
+
 /* One layer of sparse verification [SV-Fig1], [SV-Tut1], [SV-Abs]:
  *   reuse == 0: sv_score_select into sel_cache, then sv_sparse_attend on it;
  *   reuse == 1: inter-layer retrieval reuse -- no scoring or selection; the

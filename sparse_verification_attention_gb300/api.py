@@ -24,9 +24,12 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE, SV_ERR_CUDA, \
 SV_BF16, SV_F32 = 0, 1
 SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
 
+SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
+
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
-            "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_verify_layer")
+            "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
+            "sv_verify_layer")
 
 
 class SvError(RuntimeError):
@@ -49,6 +52,12 @@ class BudgetC(C.Structure):
 class KV(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("block_table", C.c_void_p),
                 ("nb_max", C.c_int), ("num_pages", C.c_int), ("ctx", C.c_int)]
+
+
+class Plan(C.Structure):
+    _fields_ = [("path", C.c_int), ("cluster", C.c_int), ("n_splits", C.c_int),
+                ("blocks_per_split", C.c_int), ("ctas_per_sm", C.c_int),
+                ("split_extra", C.c_int)]
 
 
 _lib = None
@@ -77,6 +86,7 @@ def lib() -> C.CDLL:
                                     vp, i, C.POINTER(C.c_int), vp, sz, vp]),
             "sv_sparse_attend": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, i, i, vp, vp,
                                      C.POINTER(C.c_int32), vp, vp, sz, vp]),
+            "sv_attend_plan": (i, [C.POINTER(Shape), C.POINTER(KV), i, C.POINTER(Plan)]),
             "sv_verify_layer": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, C.POINTER(BudgetC),
                                     vp, vp, C.POINTER(C.c_int32), i, vp, i, C.POINTER(C.c_int),
                                     vp, vp, sz, vp]),
@@ -198,6 +208,12 @@ def sv_sparse_attend(shape: Shape, q, kv: KV, sel, n_sel: int, sel_stride: int, 
                                   sel_stride, _ptr(draft_k), _ptr(draft_v), _parents(parents),
                                   _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(),
                                   _stream(stream)))
+
+
+def sv_attend_plan(shape: Shape, kv: KV, n_sel: int) -> Plan:
+    p = Plan()
+    _check(lib().sv_attend_plan(C.byref(shape), C.byref(kv), n_sel, C.byref(p)))
+    return p
 
 
 def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: W.Budget, draft_k, draft_v, parents,

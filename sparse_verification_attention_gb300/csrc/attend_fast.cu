@@ -71,6 +71,7 @@ struct Consumer {
   float o[D / 8][4];
   float m_lo, m_hi, l_lo, l_hi;
   int r_lo, r_hi;
+  unsigned long long vis_lo, vis_hi;  // visible drafts of rows r_lo, r_hi
 
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const AttendArgs& a,
                                        bool masked, int lane) {
@@ -102,11 +103,10 @@ struct Consumer {
       for (int e = 0; e < 4; ++e) {
         float v = s[nt][e] * a.scale_log2;
         if (masked) {
-          const int row = (e < 2) ? r_lo : r_hi;
+          // bit u of the row's ancestor mask (zero for padding rows)
           const int u = 8 * nt + 2 * t4 + (e & 1);
-          bool ok = false;
-          if (u < a.T && row < a.R) ok = (a.anc[row / a.G] >> u) & 1ull;
-          if (!ok) v = -INFINITY;
+          const unsigned long long vis = (e < 2) ? vis_lo : vis_hi;
+          if (!((vis >> u) & 1ull)) v = -INFINITY;
         }
         s[nt][e] = v;
       }
@@ -263,6 +263,12 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
     const int cw = warp - 1;
     cs.r_lo = 16 * cw + g;
     cs.r_hi = cs.r_lo + 8;
+    cs.vis_lo = cs.vis_hi = 0ull;
+    for (int t = 0; t < a.T; ++t) {  // warp-uniform index into the parameters
+      const unsigned long long m = a.anc[t];
+      if (cs.r_lo < a.R && cs.r_lo / a.G == t) cs.vis_lo = m;
+      if (cs.r_hi < a.R && cs.r_hi / a.G == t) cs.vis_hi = m;
+    }
     {
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
       const __nv_bfloat16* qlo = nullptr;
@@ -288,7 +294,8 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
     const uint32_t sbase = smem_u32(smem);
     for (int i = 0; i < nblk; ++i) {
       const int s = i % NS;
-      if (!mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit)) {
+      // warp-uniform outcome: ldmatrix/mma.sync below need all 32 lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit))) {
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
         break;
       }
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
   } else {
     // -------------------------------------------- partials for the merge kernel
     if (warp > 0) {
-      const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
+      const size_t slot = ((size_t)pair * a.slot_stride + split) * a.rpad;
 #pragma unroll
       for (int nd = 0; nd < D / 8; ++nd) {
         const int col = 8 * nd + 2 * t4;
@@ -473,7 +480,9 @@ int occupancy_cfg() {
   if (c > 0) return c;
   const int smem = K::C::kSmem;
   if (cudaFuncSetAttribute(K::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(K::fn(), cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K::fn(), K::C::kThreads, smem) !=

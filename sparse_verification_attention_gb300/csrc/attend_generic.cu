@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
   const T* q = static_cast<const T*>(a.q);
   const T* dk = static_cast<const T*>(a.draft_k);
   const T* dv = static_cast<const T*>(a.draft_v);
-  const size_t slot = ((size_t)pair * a.n_splits + split) * a.rpad;
+  const size_t slot = ((size_t)pair * a.slot_stride + split) * a.rpad;
   pdl_wait();
 
   for (int r = warp; r < a.R; r += nw) {
@@ -141,38 +141,45 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// Log-sum-exp merge of the split partials of one stacked row per warp:
+// Log-sum-exp merge of the split partials, one thread per 4 output columns
+// of one stacked row (a warp covers 128 columns of one row, so the (m, l)
+// loads are warp broadcasts):
 //   M = max_s m_s,  w_s = 2^(m_s - M),  out = sum_s w_s o_s / sum_s w_s l_s.
-constexpr int kMergeWarps = 8;
+// The split loops are unrolled so the independent loads overlap.
+constexpr int kMergeThreads = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ AttendArgs a) {
-  const int pair = blockIdx.y;
-  const int b = pair / a.Hkv, h = pair % a.Hkv;
-  const int r = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ AttendArgs a) {
+  const int c4n = a.d / 4;
+  const long long gid = (long long)blockIdx.x * kMergeThreads + threadIdx.x;
+  const long long total = (long long)a.B * a.Hkv * a.R * c4n;
   pdl_wait();
-  if (r < a.R) {
-    const size_t base = (size_t)pair * a.n_splits * a.rpad;
+  if (gid < total) {
+    const int c = (int)(gid % c4n) * 4;
+    const long long pr = gid / c4n;
+    const int r = (int)(pr % a.R);
+    const int pair = (int)(pr / a.R);
+    const int b = pair / a.Hkv, h = pair % a.Hkv;
+    const int nsp = a.n_splits + (pair < a.split_extra ? 1 : 0);
+    const size_t base = (size_t)pair * a.slot_stride * a.rpad + r;
     float M = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s)
-      M = fmaxf(M, a.part_ml[(base + (size_t)s * a.rpad + r) * 2]);
+#pragma unroll 8
+    for (int s = 0; s < nsp; ++s) M = fmaxf(M, a.part_ml[(base + (size_t)s * a.rpad) * 2]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < nsp; ++s) {
+      const size_t row = base + (size_t)s * a.rpad;
+      const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + row * 2);
+      const float4 o = *reinterpret_cast<const float4*>(a.part_o + row * a.d + c);
+      const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+      L += w * ml.y;
+      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    }
+    const float inv = 1.0f / L;
     const int t = r / a.G, gq = r % a.G;
     T* out = static_cast<T*>(a.out) + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * a.d;
-    for (int c = lane * 4; c < a.d; c += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float L = 0.f;
-      for (int s = 0; s < a.n_splits; ++s) {
-        const size_t row = base + (size_t)s * a.rpad + r;
-        const float m = a.part_ml[row * 2], l = a.part_ml[row * 2 + 1];
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-        L += w * l;
-        const float4 o = *reinterpret_cast<const float4*>(a.part_o + row * a.d + c);
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-      }
-      const float inv = 1.0f / L;
-      store4<T>(out + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-    }
+    store4<T>(out + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
   pdl_trigger();
 }
@@ -186,10 +193,11 @@ cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t s
 }
 
 cudaError_t launch_merge(const AttendArgs& a, int dtype, cudaStream_t st) {
-  dim3 grid((a.R + kMergeWarps - 1) / kMergeWarps, a.B * a.Hkv);
+  const long long total = (long long)a.B * a.Hkv * a.R * (a.d / 4);
+  dim3 grid((unsigned)((total + kMergeThreads - 1) / kMergeThreads));
   if (dtype == SV_BF16)
-    return launch_pdl(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeWarps * 32), 0, st, a);
-  return launch_pdl(merge_kernel<float>, grid, dim3(kMergeWarps * 32), 0, st, a);
+    return launch_pdl(merge_kernel<__nv_bfloat16>, grid, dim3(kMergeThreads), 0, st, a);
+  return launch_pdl(merge_kernel<float>, grid, dim3(kMergeThreads), 0, st, a);
 }
 
 }  // namespace sva

@@ -93,15 +93,37 @@ struct AttendArgs {
   float* part_o;        // [B,Hkv,S,Rpad,d]
   float* part_ml;       // [B,Hkv,S,Rpad,2]
   void* out;            // [B,T,Hq,d]
+  unsigned* counters;   // [B*Hkv] split arrivals (tcgen05 path), zero between calls
   unsigned* status;
   int B, T, Hq, Hkv, G, d, blk, R, rpad;
   int nb, nb_max, num_pages, n_sel, sel_stride;
   // Work units of a (b, h): the n_sel selected blocks, then the draft tile
   // (unit n_sel). Split s covers units [s*bps, min(n_sel+1, (s+1)*bps)).
   int n_splits, bps;
+  // Non-uniform split map (1-D grids): pairs [0, split_extra) have
+  // n_splits + 1 splits, the others n_splits; partial slots of a pair are
+  // slot_stride apart. Uniform plans: split_extra = 0, slot_stride = n_splits.
+  int split_extra, slot_stride;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
 };
+
+// CTA c of a 1-D grid under the non-uniform split map -> (pair, split, splits
+// of that pair).
+__host__ __device__ inline void split_of_cta(int c, int S, int extra, int* pair, int* split,
+                                             int* nsp) {
+  const int big = extra * (S + 1);
+  if (c < big) {
+    *pair = c / (S + 1);
+    *split = c % (S + 1);
+    *nsp = S + 1;
+  } else {
+    c -= big;
+    *pair = extra + c / S;
+    *split = c % S;
+    *nsp = S;
+  }
+}
 
 // Tensor-core path availability: bf16, d in {64,128}, blk in {32,64},
 // rpad <= 128, T <= blk, 16-byte aligned pools, a non-empty pool.
@@ -113,8 +135,16 @@ int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster);
 // (== n_splits) and merge through distributed shared memory; cluster == 0:
 // splits write global partials for launch_merge.
 cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st);
+// tcgen05 path: bf16, d == 128, blk == 64, R <= 128, T <= 64.
+// Writes global split partials (split map above, 1-D grid of pairs *
+// n_splits + split_extra CTAs); the last CTA of each (b, h) to finish merges
+// them into out (no separate merge launch).
+bool attend_tc_applies(const AttendArgs& a, int dtype);
+int attend_tc_ctas_per_sm(const AttendArgs& a);
+cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t st);
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
-// Log-sum-exp merge of the global split partials into out (any path).
+// Log-sum-exp merge of the global split partials into out (any path; honours
+// the non-uniform split map).
 cudaError_t launch_merge(const AttendArgs& a, int dtype, cudaStream_t st);
 
 
@@ -126,5 +156,9 @@ constexpr int kMaxDevices = 64;
 // TMA descriptor encoding through the driver entry point (no -lcuda).
 bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv, int blk,
                      int d, const char** why);
+// Q [B, T, Hq, d] bf16 viewed as (d, Hq, B*T) with boxes of (64, G, T): one
+// box is the T*G stacked query rows of one kv head, 64 dims wide.
+bool encode_q_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
+                  const char** why);
 
 }  // namespace sva

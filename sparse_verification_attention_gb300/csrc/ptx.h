@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "sva.h"
+
 namespace sva {
 
 // Programmatic dependent launch: wait until the preceding grid in the stream
@@ -55,6 +57,47 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wall-clock-bounded wait on a phase of an mbarrier with a CTA-wide abort
+// flag: returns false once *abort is set by any thread of the CTA, or after
+// kWaitBudgetNs of waiting (then it sets *abort itself and records `site` in
+// status[1]), so a CTA whose pipeline stalls gives up after one budget
+// instead of once per wait.
+constexpr uint64_t kWaitBudgetNs = 200ull * 1000 * 1000;
+__device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity,
+                                                    volatile int* abort, unsigned* status,
+                                                    unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      *abort = 1;
+      if (status) {
+        atomicOr(status, SV_FLAG_WAIT_TIMEOUT);
+        atomicMax(status + 1, site);
+      }
+      return false;
+    }
+  }
+}
+
+// Wall-clock-bounded wait that ignores the abort flag: used to drain copies
+// and MMAs still in flight before the CTA releases its memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 <= kWaitBudgetNs)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
@@ -66,6 +109,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 3-D tiled bulk tensor copy global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
 // across the warp. Rows are processed kUnroll at a time so that every lane
 // keeps several independent 16-byte loads in flight.
 constexpr int kScoreWarps = 8;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 constexpr int kRowsPerWarp = 8;
 constexpr int kRowsPerCta = kScoreWarps * kRowsPerWarp;
 constexpr int kMaxChunks = kMaxD / 4 / 32;  // float4 chunks per lane (d <= 256)
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const __grid_co
   __syncthreads();
   if (s_last) {
     __threadfence();
-    cta_topk<kScoreWarps * 32>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
-                               a.sel + (size_t)pair * a.kmax, a.kmax, keys, tsm);
+    cta_topk<kScoreWarps * 32, 16>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
+                                   a.sel + (size_t)pair * a.kmax, a.kmax, keys, tsm);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
   pdl_trigger();

@@ -29,8 +29,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ TopkSmem<kSelThreads> tsm;
   pdl_wait();
   const int pair = blockIdx.x;
-  cta_topk<kSelThreads>(a.scores + (size_t)pair * a.nb, a.nb, a.k, a.sel + (size_t)pair * a.kmax,
-                        a.kmax, keys, tsm);
+  cta_topk<kSelThreads, 8>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
+                           a.sel + (size_t)pair * a.kmax, a.kmax, keys, tsm);
   pdl_trigger();
 }
 

@@ -120,12 +120,17 @@ void plan_splits(int pairs, int n_units, int per_sm, int max_splits, int* n_spli
 // Cluster size for the in-cluster merge path, or 0 when that path would leave
 // more than half of the GPU idle (few (b, h) pairs): the largest cluster of
 // at most 8 CTAs whose grid still fits in one wave.
-int plan_cluster(int pairs, int n_units, int per_sm, int* bps) {
+// The whole grid must be resident at once: max_clusters(c) is how many
+// clusters of c CTAs fit on the GPU.
+template <typename MaxClusters>
+int plan_cluster(int pairs, int n_units, int per_sm, int* bps, MaxClusters max_clusters) {
   const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
   int c = 8;
   while (c > 1 && pairs * c > slots) c >>= 1;
   if (c > n_units) c = n_units;
   if ((long long)pairs * c * 2 < slots) return 0;
+  while (c > 1 && max_clusters(c) < pairs) --c;
+  if (c <= 1) return 0;
   const int per = (n_units + c - 1) / c;
   *bps = per;
   return (n_units + per - 1) / per;
@@ -213,12 +218,115 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
   return true;
 }
 
-// Shared by sv_sparse_attend and sv_verify_layer once arguments are valid.
+bool encode_q_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
+                  const char** why) {
+  auto enc = get_encode();
+  if (!enc) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)B * T};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hq * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)T};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (q) failed";
+    return false;
+  }
+  return true;
+}
+
+// Path and split plan of one attention call (shared by the launch and by
+// sv_attend_plan).
+struct AttendPlan {
+  int path;      // SV_PATH_*
+  int cluster;   // > 0: in-cluster merge with this many CTAs per (b, h)
+  int n_splits, bps, per_sm;
+  int extra, slot_stride;  // non-uniform split map (tcgen05 path)
+};
+
+static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int max_slots) {
+  AttendPlan p{};
+  const int n_units = n_sel + 1;
+  const bool tcp = attend_tc_applies(a, dtype);
+  const bool fast = !tcp && attend_fast_applies(a, dtype);
+  p.path = tcp ? SV_PATH_TCGEN05 : fast ? SV_PATH_MMA_SYNC : SV_PATH_CUDA_CORES;
+  if (tcp) {
+    // one CTA per SM: spread exactly one wave of CTAs over the (b, h) pairs,
+    // some pairs getting one split more than others
+    p.per_sm = attend_tc_ctas_per_sm(a);
+    const int slots = sm_count() * (p.per_sm > 0 ? p.per_sm : 1);
+    int S = slots / pairs, extra = slots % pairs;
+    if (S < 1) {
+      S = 1;
+      extra = 0;
+    }
+    const int cap = n_units < max_slots ? n_units : max_slots;
+    if (S + (extra ? 1 : 0) > cap) {
+      S = cap;
+      extra = 0;
+    }
+    p.n_splits = S;
+    p.extra = extra;
+    p.slot_stride = S + (extra ? 1 : 0);
+    p.bps = (n_units + S - 1) / S;
+    return p;
+  }
+  auto per_sm = [&](bool cl) { return fast ? attend_fast_ctas_per_sm(a, cl) : 4; };
+  if (fast) {
+    p.per_sm = per_sm(true);
+    p.cluster = plan_cluster(pairs, n_units, p.per_sm, &p.bps, [](int) { return 1 << 30; });
+  }
+  if (p.cluster > 0) {
+    p.n_splits = p.cluster;
+  } else {
+    p.per_sm = per_sm(false);
+    plan_splits(pairs, n_units, p.per_sm, max_slots, &p.n_splits, &p.bps);
+  }
+  p.slot_stride = p.n_splits;
+  return p;
+}
+
+static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_kv* kv,
+                      const int32_t* sel, int n_sel, int sel_stride, const void* dk,
+                      const void* dv, const int32_t* parent, void* ws, const WsLayout& L);
+
 static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, const int32_t* sel,
                             int n_sel, int sel_stride, const void* dk, const void* dv,
                             const int32_t* parent, void* out, void* ws, const WsLayout& L,
                             cudaStream_t st) {
   AttendArgs a{};
+  fill_args(a, s, q, kv, sel, n_sel, sel_stride, dk, dv, parent, ws, L);
+  a.out = out;
+  const AttendPlan p = make_plan(a, s->dtype, s->B * s->Hkv, n_sel, L.slots);
+  a.n_splits = p.n_splits;
+  a.bps = p.bps;
+  a.split_extra = p.extra;
+  a.slot_stride = p.slot_stride;
+  cudaError_t e;
+  if (p.cluster > 0) {
+    e = launch_attend_fast(a, p.cluster, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+    return SV_OK;
+  }
+  if (p.path == SV_PATH_TCGEN05) {  // merges in its last CTA per (b, h)
+    e = launch_attend_tc(a, st);
+    return e == cudaSuccess ? SV_OK : cuda_fail(e, "attend launch");
+  }
+  e = p.path == SV_PATH_MMA_SYNC ? launch_attend_fast(a, 0, st)
+                                 : launch_attend_generic(a, s->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+  e = launch_merge(a, s->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SV_OK;
+}
+
+static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_kv* kv,
+                      const int32_t* sel, int n_sel, int sel_stride, const void* dk,
+                      const void* dv, const int32_t* parent, void* ws, const WsLayout& L) {
   a.q = q;
   a.k_pool = kv->k_pool;
   a.v_pool = kv->v_pool;
@@ -227,9 +335,10 @@ static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, c
   a.block_table = kv->block_table;
   a.sel = sel;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  a.part_o = reinterpret_cast<float*>(w + L.part_o);
-  a.part_ml = reinterpret_cast<float*>(w + L.part_ml);
-  a.status = reinterpret_cast<unsigned*>(w + L.status);
+  a.part_o = w ? reinterpret_cast<float*>(w + L.part_o) : nullptr;
+  a.part_ml = w ? reinterpret_cast<float*>(w + L.part_ml) : nullptr;
+  a.status = w ? reinterpret_cast<unsigned*>(w + L.status) : nullptr;
+  a.counters = w ? reinterpret_cast<unsigned*>(w + L.ctr_attend) : nullptr;
   a.B = s->B;
   a.T = s->T;
   a.Hq = s->Hq;
@@ -246,27 +355,6 @@ static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, c
   a.sel_stride = sel_stride;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s->d));
   fill_ancestors(parent, s->T, a.anc);
-
-  a.out = out;
-  const int pairs = s->B * s->Hkv;
-  const int n_units = n_sel + 1;
-  const bool fast = attend_fast_applies(a, s->dtype);
-  int cluster = 0;
-  if (fast) cluster = plan_cluster(pairs, n_units, attend_fast_ctas_per_sm(a, true), &a.bps);
-  cudaError_t e;
-  if (cluster > 0) {
-    a.n_splits = cluster;
-    e = launch_attend_fast(a, cluster, st);
-    if (e != cudaSuccess) return cuda_fail(e, "attend launch");
-    return SV_OK;
-  }
-  const int per_sm = fast ? attend_fast_ctas_per_sm(a, false) : 4;
-  plan_splits(pairs, n_units, per_sm, L.slots, &a.n_splits, &a.bps);
-  e = fast ? launch_attend_fast(a, 0, st) : launch_attend_generic(a, s->dtype, st);
-  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
-  e = launch_merge(a, s->dtype, st);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return SV_OK;
 }
 
 static sv_status check_ws(const sv_shape* s, int nb_max, int kmax, const void* ws, size_t bytes,
@@ -426,6 +514,25 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
   if ((r = check_ws(shape, kv->nb_max, n_sel, workspace, ws_bytes, &L)) != SV_OK) return r;
   return run_attend(shape, q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent, out,
                     workspace, L, (cudaStream_t)stream);
+}
+
+sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_plan* out) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
+  if (!out) return fail(SV_ERR_INVALID_ARG, "out is NULL");
+  if (n_sel < 0) return fail(SV_ERR_INVALID_ARG, "n_sel=%d is negative", n_sel);
+  const WsLayout L = ws_layout(*shape, kv->nb_max, n_sel);
+  AttendArgs a{};
+  fill_args(a, shape, nullptr, kv, nullptr, n_sel, n_sel, nullptr, nullptr, nullptr, nullptr, L);
+  const AttendPlan p = make_plan(a, shape->dtype, shape->B * shape->Hkv, n_sel, L.slots);
+  out->path = p.path;
+  out->cluster = p.cluster;
+  out->n_splits = p.n_splits;
+  out->blocks_per_split = p.bps;
+  out->ctas_per_sm = p.per_sm;
+  out->split_extra = p.extra;
+  return SV_OK;
 }
 
 sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,

@@ -126,23 +126,28 @@ def test_score_select_vs_oracle():
 
 # ------------------------------------------------------------------ attend
 ATTEND_CASES = [
-    # name, workload overrides, n_sel
-    ("fast_d128_blk64_R32", dict(), 13),
-    ("fast_d128_blk64_R32_ragged", dict(B=3, ctx=64 * 77), 61),
-    ("fast_tree16_G8_R128", dict(Hq=16, Hkv=2, T=16, parents=W.TREE16_PARENTS), 29),
-    ("fast_R16_pad", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), 17),
-    ("fast_R48_rows_pad", dict(Hq=8, Hkv=2, T=12, blk=32, ctx=32 * 45), 9),
-    ("fast_T1_G1", dict(Hq=2, Hkv=2, T=1), 5),
-    ("fast_nsel0_drafts_only", dict(), 0),
-    ("fast_all_blocks", dict(ctx=64 * 24), 24),
-    # many (b, h) pairs: splits of a pair form a thread-block cluster and merge
-    # through distributed shared memory
-    ("cluster_B8_H8_R32", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 13),
-    ("cluster_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
-                                 ctx=64 * 20), 11),
-    ("cluster_size3", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 2),
-    ("cluster_d64_blk32_R16", dict(B=8, Hq=16, Hkv=8, d=64, blk=32, ctx=32 * 40), 9),
-    ("cluster_all_blocks", dict(B=8, Hq=32, Hkv=8, ctx=64 * 10), 10),
+    # name (path prefix: tc = tcgen05, mma = legacy mma.sync, generic = CUDA
+    # cores), workload overrides, number of selected blocks
+    ("tc_d128_blk64_R32", dict(), 13),
+    ("tc_R32_ragged", dict(B=3, ctx=64 * 77), 61),
+    ("tc_tree16_G8_R128", dict(Hq=16, Hkv=2, T=16, parents=W.TREE16_PARENTS), 29),
+    ("tc_R48", dict(Hq=8, Hkv=2, T=12, ctx=64 * 45), 9),
+    ("tc_T1_G1", dict(Hq=2, Hkv=2, T=1), 5),
+    ("tc_nsel0_drafts_only", dict(), 0),
+    ("tc_all_blocks", dict(ctx=64 * 24), 24),
+    ("tc_T64_chain", dict(T=64, Hq=2, Hkv=1, ctx=64 * 30), 7),
+    # many (b, h) pairs: non-uniform split map (some pairs get one more split)
+    ("tc_many_pairs_B8_H8_R32", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 13),
+    ("tc_many_pairs_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                                       ctx=64 * 20), 11),
+    ("tc_many_pairs_few_units", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 2),
+    ("tc_many_pairs_all_blocks", dict(B=8, Hq=32, Hkv=8, ctx=64 * 10), 10),
+    ("tc_more_pairs_than_sms", dict(B=40, Hq=16, Hkv=4, ctx=64 * 6), 3),
+    ("mma_R16_pad", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), 17),
+    ("mma_R48_rows_pad", dict(Hq=8, Hkv=2, T=12, blk=32, ctx=32 * 45), 9),
+    ("mma_d64_blk64", dict(d=64, ctx=64 * 30), 11),
+    ("mma_cluster_d64_blk32_R16", dict(B=16, Hq=16, Hkv=8, d=64, blk=32, ctx=32 * 40), 9),
+    ("mma_cluster_blk32_R32", dict(B=8, Hq=32, Hkv=8, blk=32, ctx=32 * 40), 9),
     ("generic_f32", dict(dtype="f32", d=64, blk=16, ctx=16 * 64, Hq=4, Hkv=2, T=4), 8),
     ("generic_d96", dict(d=96, blk=32, ctx=32 * 40), 11),
     ("generic_T_gt_blk", dict(T=40, Hq=2, Hkv=1, blk=32, ctx=32 * 30), 7),
@@ -160,14 +165,52 @@ def test_sparse_attend(name, over, n_sel):
     xd = x.to("cuda")
     st = api.LayerState(wl, xd, kmax=max(n_sel, 1), build_reps=False)
     sel = random_sel(wl.B, wl.Hkv, wl.NB, n_sel, seed=len(name))
+    plan = api.sv_attend_plan(st.shape, st.kv, n_sel)
+    want_path = {"tc": api.SV_PATH_TCGEN05, "mma": api.SV_PATH_MMA_SYNC,
+                 "generic": api.SV_PATH_CUDA_CORES}[name.split("_")[0]]
+    assert plan.path == want_path, (plan.path, want_path)
+    if "cluster" in name and want_path == api.SV_PATH_MMA_SYNC:
+        assert plan.cluster > 0
     out = torch.zeros_like(xd.q)
     api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, sel.shape[-1], xd.draft_k,
                          xd.draft_v, st.parents, out, st.ws)
     torch.cuda.synchronize()
-    assert api.sv_read_status(st.ws) == 0
+    words = st.ws[:8].view(torch.int32).tolist()
+    assert api.sv_read_status(st.ws) == 0, f"status words {words} plan {plan.cluster} {plan.n_splits}"
     ref = O.sparse_attend(x.q, x.k_pool, x.v_pool, x.block_table, sel[:, :, :n_sel].long(),
                           x.draft_k, x.draft_v, wl.parent_list())
     U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
+
+
+def test_tc_late_rescale_divergent_rows():
+    """One CTA per (b, h) walks 41 work units; a late selected block has keys
+    boosted along the group's query, so the running max of some rows (not
+    all) jumps by far more than 2^8 mid-stream: the accumulator rescale must
+    be taken by the whole warp and stay exact."""
+    wl = small_wl(B=19, Hq=32, Hkv=8, ctx=64 * 48, n_planted=0, sink_alpha=None)
+    x = W.make_layer(wl)
+    G = wl.G
+    n_sel = 40
+    sel = random_sel(wl.B, wl.Hkv, wl.NB, n_sel, seed=99)
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            j = int(sel[b, h, 33])  # a late block of this pair's selection
+            page = int(x.block_table[b, j])
+            q0 = x.q[b, :, h * G].float().mean(0)  # the group's mean query direction
+            boost = (x.k_pool[page, h].float() + 6.0 * q0).to(x.k_pool.dtype)
+            x.k_pool[page, h] = boost
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, kmax=n_sel, build_reps=False)
+    plan = api.sv_attend_plan(st.shape, st.kv, n_sel)
+    assert plan.path == api.SV_PATH_TCGEN05 and plan.n_splits == 1
+    out = torch.zeros_like(xd.q)
+    api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, sel.shape[-1], xd.draft_k,
+                         xd.draft_v, None, out, st.ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    ref = O.sparse_attend(x.q, x.k_pool, x.v_pool, x.block_table, sel.long(), x.draft_k,
+                          x.draft_v, wl.parent_list())
+    U.compare_out(out, ref, U.BF16_ATOL)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "bf16_many_pairs"])
