@@ -119,9 +119,12 @@ int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
 
 /* Bytes of workspace that score/select/attend/verify calls with this shape
  * need, for selections of up to kmax blocks over up to nb_max blocks. The
- * first 256 bytes hold the device status word, which must be zero before the
- * first call (allocate zeroed, or call sv_clear_status). Returns 0 on an
- * invalid shape. Host only. */
+ * first 256 bytes hold the device status word; after it come two arrays of
+ * per-(b, h) arrival counters (the last CTA of a pair to arrive does that
+ * pair's selection or split merge). The whole workspace must be zero before
+ * its first use (allocate it zeroed). Every call returns the counters to
+ * zero; the status word keeps its flags until sv_clear_status. Returns 0 on
+ * an invalid shape. Host only. */
 size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax);
 
 /* Zero the workspace status word (async on stream). */
