@@ -228,6 +228,38 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           int kmax, int* k_out, void* out, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* sv_sparse_attend without a workspace. The paper has no counterpart: this
+ * entry exists for callers that cannot allocate device memory, such as an
+ * operation hosted by another runtime (a plugin or callback handed only its
+ * tensors) after that runtime's memory planner has claimed the device; such
+ * a caller has no allocator to ask for a workspace, and a cudaMalloc at call
+ * time would synchronise the device under the host runtime's schedule.
+ *
+ * Arguments q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent
+ * and out are those of sv_sparse_attend, and the result is the same (same
+ * kernels, same split plan). flags_out: DEVICE uint32 (may be NULL) that
+ * receives this call's device status flags (SV_FLAG_*), written on stream
+ * after the attention.
+ *
+ * Scratch: a 16 MiB array in the library's device code, which every device
+ * that loads the library holds until the process exits. No call allocates
+ * (no cudaMalloc, no cudaFree, no allocating library routine). A call whose
+ * split partials need more than 16 MiB returns SV_ERR_WORKSPACE and launches
+ * nothing; sv_sparse_attend with a workspace handles it instead.
+ * Set-up: the first call made with a given device current looks up the
+ * array's device address there (cudaGetSymbolAddress), which may load the
+ * library's device code; make that first call before any stream capture.
+ * Every call zeroes the status word and arrival counters it uses on
+ * `stream`. All calls on one device share the one array: two calls whose
+ * work overlaps on the GPU (different streams, or different host threads,
+ * without ordering between them) race and corrupt each other's results;
+ * order them on one stream or with events. */
+sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const sv_kv* kv,
+                                   const int32_t* sel, int n_sel, int sel_stride,
+                                   const void* draft_k, const void* draft_v,
+                                   const int32_t* draft_parent, void* out, uint32_t* flags_out,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

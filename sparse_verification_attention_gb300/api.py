@@ -29,7 +29,7 @@ SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
             "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
-            "sv_verify_layer")
+            "sv_verify_layer", "sv_sparse_attend_noalloc")
 
 
 class SvError(RuntimeError):
@@ -90,6 +90,8 @@ def lib() -> C.CDLL:
             "sv_verify_layer": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, C.POINTER(BudgetC),
                                     vp, vp, C.POINTER(C.c_int32), i, vp, i, C.POINTER(C.c_int),
                                     vp, vp, sz, vp]),
+            "sv_sparse_attend_noalloc": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, i, i, vp,
+                                             vp, C.POINTER(C.c_int32), vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -208,6 +210,18 @@ def sv_sparse_attend(shape: Shape, q, kv: KV, sel, n_sel: int, sel_stride: int, 
                                   sel_stride, _ptr(draft_k), _ptr(draft_v), _parents(parents),
                                   _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(),
                                   _stream(stream)))
+
+
+def sv_sparse_attend_noalloc(shape: Shape, q, kv: KV, sel, n_sel: int, sel_stride: int, draft_k,
+                             draft_v, parents, out, flags_out=None, stream=None):
+    """sv_sparse_attend with the library's static scratch instead of a
+    workspace, for callers that cannot allocate device memory. flags_out: an
+    optional device uint32/int32 tensor of one element that receives the
+    call's status flags. Calls whose GPU work overlaps race on the scratch."""
+    _check(lib().sv_sparse_attend_noalloc(C.byref(shape), _ptr(q), C.byref(kv), _ptr(sel), n_sel,
+                                          sel_stride, _ptr(draft_k), _ptr(draft_v),
+                                          _parents(parents), _ptr(out), _ptr(flags_out),
+                                          _stream(stream)))
 
 
 def sv_attend_plan(shape: Shape, kv: KV, n_sel: int) -> Plan:

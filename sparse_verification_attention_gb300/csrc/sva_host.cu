@@ -387,6 +387,58 @@ static sv_status do_score_select(const sv_shape* s, const void* q, const float* 
   return SV_OK;
 }
 
+// ------------------------------------------------------------ allocation-free attend
+// Scratch of sv_sparse_attend_noalloc. It is for callers that cannot hand the
+// library a workspace: an operation hosted inside another runtime (a plugin
+// or callback that receives only its input and output tensors) after that
+// runtime's memory planner has claimed the device memory. Such a caller has
+// no allocator to draw scratch from, and a cudaMalloc at call time would
+// synchronise the whole device inside the host runtime's schedule. The
+// scratch is module memory, reserved on each device when the library's
+// device code is loaded there and held until the process exits; no call
+// allocates anything. In host code the array's name is only a host-side
+// stand-in for the symbol: kernels get its device address, looked up below.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static std::atomic<void*> g_noalloc_ptr[kMaxDevices];
+
+// Device address of the scratch on the current device, looked up on the
+// first call made with that device current and cached.
+static sv_status noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(SV_ERR_UNSUPPORTED, "device %d: at most %d devices", dev, kMaxDevices);
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (static scratch)");
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  *ptr = p;
+  return SV_OK;
+}
+
+// Status word, attend arrival counters (both zeroed by every call: the
+// prefix [0, part_o)), then the split partials of the plan actually launched:
+// slot_stride splits per pair rather than a workspace's worst case.
+static WsLayout noalloc_layout(const sv_shape& s, int rpad, int slot_stride) {
+  WsLayout L{};
+  const size_t pairs = (size_t)s.B * s.Hkv;
+  const size_t rows = pairs * (size_t)slot_stride * rpad;
+  L.rpad = rpad;
+  L.slots = slot_stride;
+  L.status = 0;
+  L.ctr_attend = kStatusBytes;
+  L.ctr_score = L.ctr_attend;  // unused: this entry does not score
+  L.part_o = L.ctr_attend + align256(pairs * sizeof(uint32_t));
+  L.scores = L.part_o;  // unused
+  L.part_ml = L.part_o + align256(rows * s.d * sizeof(float));
+  L.total = L.part_ml + align256(rows * 2 * sizeof(float));
+  return L;
+}
+
 }  // namespace sva
 
 using namespace sva;
@@ -565,6 +617,73 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   if (k_out) *k_out = k;
   return run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out,
                     workspace, L, st);
+}
+
+sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const sv_kv* kv,
+                                   const int32_t* sel, int n_sel, int sel_stride,
+                                   const void* draft_k, const void* draft_v,
+                                   const int32_t* draft_parent, void* out, uint32_t* flags_out,
+                                   void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
+  const int nb = kv->ctx / shape->blk;
+  if (!sel) {
+    n_sel = nb;
+    sel_stride = nb;
+  } else if (n_sel < 0 || n_sel > sel_stride) {
+    return fail(SV_ERR_INVALID_ARG, "n_sel=%d outside [0, sel_stride=%d]", n_sel, sel_stride);
+  }
+  if (!q || !draft_k || !draft_v || !out)
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out is NULL");
+  if (!aligned(q, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16) || !aligned(out, 16))
+    return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out must be 16-byte aligned");
+  if (flags_out && !aligned(flags_out, 4))
+    return fail(SV_ERR_INVALID_ARG, "flags_out must be 4-byte aligned");
+  if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
+  // the same plan sv_sparse_attend makes for this call
+  const WsLayout W = ws_layout(*shape, kv->nb_max, n_sel);
+  AttendArgs a{};
+  fill_args(a, shape, q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent, nullptr, W);
+  a.out = out;
+  const AttendPlan p = make_plan(a, shape->dtype, shape->B * shape->Hkv, n_sel, W.slots);
+  const WsLayout L = noalloc_layout(*shape, W.rpad, p.slot_stride);
+  if (L.total > kNoAllocScratchBytes)
+    return fail(SV_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch; the static scratch holds %zu "
+                "(use sv_sparse_attend with a workspace)",
+                L.total, kNoAllocScratchBytes);
+  void* base = nullptr;
+  if ((r = noalloc_scratch(&base)) != SV_OK) return r;
+  uint8_t* w = static_cast<uint8_t*>(base);
+  a.status = reinterpret_cast<unsigned*>(w + L.status);
+  a.counters = reinterpret_cast<unsigned*>(w + L.ctr_attend);
+  a.part_o = reinterpret_cast<float*>(w + L.part_o);
+  a.part_ml = reinterpret_cast<float*>(w + L.part_ml);
+  a.n_splits = p.n_splits;
+  a.bps = p.bps;
+  a.split_extra = p.extra;
+  a.slot_stride = p.slot_stride;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: zero the status word and
+  // the arrival counters (the partials are fully written before being read)
+  cudaError_t e = cudaMemsetAsync(base, 0, L.part_o, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (static scratch)");
+  if (p.cluster > 0) {
+    e = launch_attend_fast(a, p.cluster, st);
+  } else if (p.path == SV_PATH_TCGEN05) {
+    e = launch_attend_tc(a, st);
+  } else {
+    e = p.path == SV_PATH_MMA_SYNC ? launch_attend_fast(a, 0, st)
+                                   : launch_attend_generic(a, shape->dtype, st);
+    if (e == cudaSuccess) e = launch_merge(a, shape->dtype, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+  if (flags_out) {
+    e = cudaMemcpyAsync(flags_out, base, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy");
+  }
+  return SV_OK;
 }
 
 }  // extern "C"
