@@ -86,7 +86,8 @@ def read_peaks():
 
 def attend_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attend_fast.cu", "attend_generic.cu", "ptx.h", "internal.h"):
+    for f in ("attend_tc.cu", "attend_fast.cu", "attend_generic.cu", "tc.h", "ptx.h",
+              "internal.h"):
         with open(os.path.join(ROOT, "sparse_verification_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -452,8 +453,13 @@ def run_gpu(args, wl, rank, world, dist):
                "cores": torch.get_num_threads(), "kind": "oracle", "sample": o.describe(n, el)}
 
     traffic = traffic_from_profile(wl.name)
-    launches_per_step = sum(1 + (1 if l % wl.compute_every == 0 else 0) * 2 + 2
-                            for l in range(wl.layers))
+    # kernels per layer: the incremental rep build, the fused score+select on
+    # computing layers, the attention (plus a merge kernel on paths that do
+    # not merge in-kernel)
+    plan = api.sv_attend_plan(st0.shape, st0.kv, k)
+    att_launches = 1 if (plan.path == api.SV_PATH_TCGEN05 or plan.cluster > 0) else 2
+    launches_per_step = sum((1 if wl.NB else 0) + (1 if l % wl.compute_every == 0 else 0)
+                            + att_launches for l in range(wl.layers))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -465,7 +471,11 @@ def run_gpu(args, wl, rank, world, dist):
         "step_bytes": sbytes, "step_gbs": sbytes / (ms_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "sv_sparse_attend (split-KV attend, cluster LSE merge)",
+                     "kernel": {api.SV_PATH_TCGEN05: "attend_tc_kernel (tcgen05 split-KV "
+                                "attention, in-kernel LSE merge)",
+                                api.SV_PATH_MMA_SYNC: "attend_fast_kernel (mma.sync split-KV)",
+                                api.SV_PATH_CUDA_CORES: "attend_generic_kernel + merge_kernel"
+                                }[plan.path],
                      "bytes_per_launch": abytes, "launch_ms": attend_ms,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                      "frac_of_nominal_8tbs": achieved / 8000.0},

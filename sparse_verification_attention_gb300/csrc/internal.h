@@ -67,13 +67,17 @@ struct ScoreArgs {
   const float* reps;
   float* scores;
   int B, T, Hq, Hkv, G, d, nb, nb_max;
+  int rows_per_cta;  // blocks scored by one CTA (set by launch_score)
   // fused selection (sel == nullptr: scores only): the last scoring CTA of
   // each (b, h) selects k blocks into sel[b][h][0..kmax)
   int32_t* sel;
   int k, kmax;
   unsigned* counters;  // [B*Hkv], zero between calls
 };
-cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_score(ScoreArgs a, int dtype, cudaStream_t st);
+// Largest block count whose selection the score kernel fuses (its 256
+// threads hold 32 keys each); beyond it scoring and selection are two launches.
+constexpr int kFusedSelectMaxNB = 8192;
 
 struct SelectArgs {
   const float* scores;
@@ -151,6 +155,7 @@ cudaError_t launch_merge(const AttendArgs& a, int dtype, cudaStream_t st);
 // Per-device once-only setup results (kernel attributes, occupancy), so that
 // steady-state calls only launch kernels and can be captured in CUDA graphs.
 int current_device();
+int sm_count();  // SMs of the current device (cached per device)
 constexpr int kMaxDevices = 64;
 
 // TMA descriptor encoding through the driver entry point (no -lcuda).

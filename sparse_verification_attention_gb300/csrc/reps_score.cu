@@ -86,91 +86,114 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
 }
 
 // ------------------------------------------------------------------ scores
-// grid = (ceil(nb / kRowsPerCta), B*Hkv). Each warp streams whole fp32
-// representative rows with 128-bit loads (lane c holds dims 4c..4c+3), dots
-// them with the group-summed draft-0 query held in registers, and reduces
-// across the warp. Rows are processed kUnroll at a time so that every lane
-// keeps several independent 16-byte loads in flight.
-constexpr int kScoreWarps = 8;
-constexpr int kUnroll = 8;
-constexpr int kRowsPerWarp = 8;
-constexpr int kRowsPerCta = kScoreWarps * kRowsPerWarp;
-constexpr int kMaxChunks = kMaxD / 4 / 32;  // float4 chunks per lane (d <= 256)
+// grid = (CTAs per pair, B*Hkv); CTA x of a pair scores blocks
+// [x*rows_per_cta, (x+1)*rows_per_cta), sized on the host so that the whole
+// grid is resident at once. Each warp streams whole fp32 representative rows
+// with 128-bit loads (lane c holds dims 4c..4c+3 of each 128-dim chunk),
+// R rows at a time: all of a group's loads are issued before its dot
+// products, and the first group's loads are in flight while the warp forms
+// the group-summed draft-0 query. The R row sums are reduced together by a
+// transposing butterfly (each exchange halves the values a lane holds).
+constexpr int kScoreThreads = 256;
+constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kScoreKeys = kFusedSelectMaxNB / kScoreThreads;  // top-k keys per thread
 
-template <typename T>
-__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const __grid_constant__ ScoreArgs a) {
-  const int pair = blockIdx.y;  // b * Hkv + h
+template <int CH>
+__host__ __device__ constexpr int score_rows() { return 16 / CH; }
+
+template <typename T, int CH>  // CH: 128-dim chunks per row (d <= 128 * CH)
+__global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_constant__ ScoreArgs a) {
+  constexpr int R = score_rows<CH>();  // rows in flight per warp
+  constexpr int S = 32 / R;            // lanes per row after the butterfly
+  const int pair = blockIdx.y;         // b * Hkv + h
   const int b = pair / a.Hkv, h = pair % a.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nchunk = a.d / 4;
+  const int r0 = blockIdx.x * a.rows_per_cta;
+  const int r1 = min(a.nb, r0 + a.rows_per_cta);
+  const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
+  float* srow = a.scores + (size_t)pair * a.nb;
   pdl_wait();
 
-  // qhat = sum over the G query heads of KV head h of draft 0's query.
-  float4 qh[kMaxChunks];
+  float4 qh[CH];
+  bool have_q = false;
+  for (int base = r0 + warp * R; base < r1; base += kScoreWarps * R) {
+    float4 rv[R][CH];
 #pragma unroll
-  for (int c = 0; c < kMaxChunks; ++c) {
-    qh[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int ch = lane + 32 * c;
-    if (ch < nchunk) {
-      const T* q0 = static_cast<const T*>(a.q) + ((size_t)b * a.T * a.Hq + (size_t)h * a.G) * a.d;
-      for (int g = 0; g < a.G; ++g) {
-        float4 v = load4<T>(q0 + (size_t)g * a.d + ch * 4);
-        qh[c].x += v.x; qh[c].y += v.y; qh[c].z += v.z; qh[c].w += v.w;
+    for (int u = 0; u < R; ++u) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int ch = lane + 32 * c;
+        rv[u][c] = (base + u < r1 && ch < nchunk)
+                       ? __ldg(reinterpret_cast<const float4*>(rep0 + (size_t)(base + u) * a.d) + ch)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  }
-
-  const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
-  const int row0 = blockIdx.x * kRowsPerCta + warp * kRowsPerWarp;
+    if (!have_q) {  // qhat = sum over the G query heads of kv head h, draft 0
+      const T* q0 = static_cast<const T*>(a.q) + ((size_t)b * a.T * a.Hq + (size_t)h * a.G) * a.d;
 #pragma unroll
-  for (int it = 0; it < kRowsPerWarp; it += kUnroll) {
-    float acc[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      acc[u] = 0.f;
-      const int j = row0 + it + u;
-      if (j < a.nb) {
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) {
-          const int ch = lane + 32 * c;
-          if (ch < nchunk) {
-            float4 r = __ldg(reinterpret_cast<const float4*>(rep0 + (size_t)j * a.d) + ch);
-            acc[u] = fmaf(qh[c].x, r.x, acc[u]);
-            acc[u] = fmaf(qh[c].y, r.y, acc[u]);
-            acc[u] = fmaf(qh[c].z, r.z, acc[u]);
-            acc[u] = fmaf(qh[c].w, r.w, acc[u]);
+      for (int c = 0; c < CH; ++c) {
+        qh[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int ch = lane + 32 * c;
+        if (ch < nchunk) {
+          for (int g = 0; g < a.G; ++g) {
+            const float4 v = load4<T>(q0 + (size_t)g * a.d + ch * 4);
+            qh[c].x += v.x; qh[c].y += v.y; qh[c].z += v.z; qh[c].w += v.w;
           }
         }
       }
+      have_q = true;
+    }
+    float acc[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      acc[u] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        acc[u] = fmaf(qh[c].x, rv[u][c].x, acc[u]);
+        acc[u] = fmaf(qh[c].y, rv[u][c].y, acc[u]);
+        acc[u] = fmaf(qh[c].z, rv[u][c].z, acc[u]);
+        acc[u] = fmaf(qh[c].w, rv[u][c].w, acc[u]);
+      }
+    }
+    // transposing butterfly: after the exchange at offset o a lane keeps the
+    // half of its values selected by bit o of its lane index; lane l ends
+    // with row l / S summed over the lanes that share l / S
+#pragma unroll
+    for (int n = R, o = 16; n > 1; n >>= 1, o >>= 1) {
+      const bool hi = lane & o;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = hi ? acc[i] : acc[i + n / 2];
+        const float keep = hi ? acc[i + n / 2] : acc[i];
+        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
-      const int j = row0 + it + u;
-      if (lane == 0 && j < a.nb) a.scores[(size_t)pair * a.nb + j] = acc[u];
-    }
+    for (int o = S / 2; o > 0; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+    const int j = base + lane / S;
+    if ((lane % S) == 0 && j < r1) srow[j] = acc[0];
   }
-  if (!a.sel) {
+  if (!a.sel || a.nb > kFusedSelectMaxNB) {
     pdl_trigger();
     return;
   }
 
-  // Fused selection: the last CTA to finish scoring this (b, h) selects.
+  // Fused selection: the last CTA to finish scoring this (b, h) selects. The
+  // barrier orders every thread's score stores before thread 0's device-scope
+  // fence and arrival; the last arrival fences again before reading.
   __shared__ unsigned s_last;
-  __shared__ TopkSmem<kScoreWarps * 32> tsm;
-  extern __shared__ uint32_t keys[];
-  __threadfence();
+  __shared__ TopkSmem<kScoreThreads> tsm;
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(&a.counters[pair], 1u);
-    s_last = (prev == gridDim.x - 1);
+    __threadfence();
+    const bool last = atomicAdd(&a.counters[pair], 1u) == gridDim.x - 1;
+    if (last) __threadfence();
+    s_last = last;
   }
   __syncthreads();
   if (s_last) {
-    __threadfence();
-    cta_topk<kScoreWarps * 32, 16>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
-                                   a.sel + (size_t)pair * a.kmax, a.kmax, keys, tsm);
+    cta_topk<kScoreThreads, kScoreKeys>(srow, a.nb, a.k, a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
   pdl_trigger();
@@ -186,21 +209,36 @@ cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st) {
   return launch_pdl(build_reps_kernel<float>, grid, dim3(kRepThreads), 0, st, a);
 }
 
-cudaError_t launch_score(const ScoreArgs& a, int dtype, cudaStream_t st) {
-  if (a.nb == 0) return cudaSuccess;
-  dim3 grid((a.nb + kRowsPerCta - 1) / kRowsPerCta, a.B * a.Hkv);
-  const size_t smem = a.sel ? (size_t)a.nb * sizeof(uint32_t) : 0;
-  auto kern = (dtype == SV_BF16) ? score_kernel<__nv_bfloat16> : score_kernel<float>;
-  static std::atomic<int> attr_set[kMaxDevices][2];
+template <typename T, int CH>
+static cudaError_t launch_score_t(ScoreArgs a, cudaStream_t st) {
+  auto kern = score_kernel<T, CH>;
+  // resident CTAs per SM, queried once per device
+  static std::atomic<int> occ_cache[kMaxDevices];
   const int dev = current_device();
-  const int which = dtype == SV_BF16 ? 0 : 1;
-  if (!attr_set[dev][which].load()) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kMaxNB * sizeof(uint32_t)));
+  int occ = occ_cache[dev].load();
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kScoreThreads, 0);
     if (e != cudaSuccess) return e;
-    attr_set[dev][which].store(1);
+    if (occ < 1) occ = 1;
+    occ_cache[dev].store(occ);
   }
-  return launch_pdl(kern, grid, dim3(kScoreWarps * 32), smem, st, a);
+  // one resident wave: spread sm_count * occ CTAs over the pairs
+  const int pairs = a.B * a.Hkv;
+  constexpr int R = score_rows<CH>();
+  int cpp = sm_count() * occ / pairs;
+  const int max_cpp = (a.nb + kScoreWarps * R - 1) / (kScoreWarps * R);
+  cpp = cpp < 1 ? 1 : cpp > max_cpp ? max_cpp : cpp;
+  a.rows_per_cta = (a.nb + cpp - 1) / cpp;
+  cpp = (a.nb + a.rows_per_cta - 1) / a.rows_per_cta;
+  return launch_pdl(kern, dim3(cpp, pairs), dim3(kScoreThreads), 0, st, a);
+}
+
+cudaError_t launch_score(ScoreArgs a, int dtype, cudaStream_t st) {
+  if (a.nb == 0) return cudaSuccess;
+  const bool wide = a.d > 128;
+  if (dtype == SV_BF16)
+    return wide ? launch_score_t<__nv_bfloat16, 2>(a, st) : launch_score_t<__nv_bfloat16, 1>(a, st);
+  return wide ? launch_score_t<float, 2>(a, st) : launch_score_t<float, 1>(a, st);
 }
 
 }  // namespace sva

@@ -12,6 +12,22 @@
 #include "internal.h"
 
 namespace sva {
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64) {
+    int c = cached[dev].load();
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev].store(n);
+  return n;
+}
+
 namespace {
 
 thread_local std::string g_err;
@@ -88,20 +104,6 @@ int budget_blocks(const sv_budget* bd, int ctx, int nb) {
   return (int)(k < nb ? k : nb);
 }
 
-int sm_count() {
-  static std::atomic<int> cached[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64) {
-    int c = cached[dev].load();
-    if (c > 0) return c;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  if (dev < 64) cached[dev].store(n);
-  return n;
-}
 
 // Split planning for the global-partials path: enough CTAs to fill every SM
 // `per_sm` deep in one wave, at most one split per work unit (a selected
@@ -380,8 +382,12 @@ static sv_status do_score_select(const sv_shape* s, const void* q, const float* 
     e = launch_select(se, st);
   } else {
     ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max,
-                 sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score)};
+                 0, sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score)};
     e = launch_score(sa, s->dtype, st);
+    if (e == cudaSuccess && nb > kFusedSelectMaxNB) {  // too many keys to fuse
+      SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax};
+      e = launch_select(se, st);
+    }
   }
   if (e != cudaSuccess) return cuda_fail(e, "score/select launch");
   return SV_OK;
@@ -504,7 +510,7 @@ sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* rep
   if (!aligned(q, 16) || !aligned(reps, 16))
     return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
   ScoreArgs sa{q, reps, scores, shape->B, shape->T, shape->Hq, shape->Hkv,
-               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, nullptr, 0, 0, nullptr};
+               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, 0, nullptr, 0, 0, nullptr};
   cudaError_t e = launch_score(sa, shape->dtype, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "score launch");
 }
