@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 1
+#define SV_ABI_VERSION 2
 
 typedef enum {
   SV_OK = 0,
@@ -198,7 +198,10 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
  * cores with TMEM accumulators), SV_PATH_MMA_SYNC (bf16, d in {64,128},
  * blk in {32,64}, T*G <= 128, T <= blk), else SV_PATH_CUDA_CORES; cluster > 0
  * when the splits of one (b, h) merge inside a thread-block cluster of that
- * size; split_extra > 0 when that many (b, h) pairs get n_splits + 1 splits.
+ * size; split_extra > 0 when that many (b, h) pairs get n_splits + 1 splits;
+ * streamk = 1 when n_splits CTAs instead share the work units of all pairs
+ * in equal runs (the tcgen05 path when there are at least as many units as
+ * CTAs and a run fits in one pair).
  * Queries the current device (occupancy); launches nothing. */
 #define SV_PATH_CUDA_CORES 0
 #define SV_PATH_MMA_SYNC 1
@@ -210,6 +213,9 @@ typedef struct {
   int blocks_per_split;  /* work units (selected blocks, draft tile)   */
   int ctas_per_sm;       /* resident CTAs per SM the plan assumed      */
   int split_extra;       /* pairs [0, split_extra) have n_splits + 1   */
+  int streamk;           /* 1: n_splits CTAs each take an equal run of
+                            the flattened (pair, unit) sequence, at
+                            most two pairs per CTA (tcgen05 path)      */
 } sv_plan;
 sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_plan* out);
 

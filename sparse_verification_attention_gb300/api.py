@@ -25,6 +25,7 @@ SV_BF16, SV_F32 = 0, 1
 SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
 
 SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
+ABI_VERSION = 2  # SV_ABI_VERSION the structures below match
 
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
@@ -57,7 +58,7 @@ class KV(C.Structure):
 class Plan(C.Structure):
     _fields_ = [("path", C.c_int), ("cluster", C.c_int), ("n_splits", C.c_int),
                 ("blocks_per_split", C.c_int), ("ctas_per_sm", C.c_int),
-                ("split_extra", C.c_int)]
+                ("split_extra", C.c_int), ("streamk", C.c_int)]
 
 
 _lib = None
@@ -96,6 +97,9 @@ def lib() -> C.CDLL:
         for name, (res, args) in sig.items():
             f = getattr(L, name)
             f.restype, f.argtypes = res, args
+        if L.sv_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{LIB_PATH} has ABI {L.sv_abi_version()}, the binding expects "
+                               f"{ABI_VERSION}: rebuild it")
         _lib = L
     return _lib
 

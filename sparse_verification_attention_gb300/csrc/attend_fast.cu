@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
   }
   __syncthreads();
   pdl_wait();  // everything below may read what earlier kernels wrote
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
 
   Consumer<D, BLK, NWC> cs;
   const int g = lane >> 2, t4 = lane & 3;
@@ -334,7 +335,6 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
     cs.l_hi += __shfl_xor_sync(0xffffffffu, cs.l_hi, 1);
     cs.l_hi += __shfl_xor_sync(0xffffffffu, cs.l_hi, 2);
   }
-  pdl_trigger();
 
   if constexpr (CLUSTER) {
     // ------------------------------------------------ in-cluster merge (DSMEM)

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
   const T* dv = static_cast<const T*>(a.draft_v);
   const size_t slot = ((size_t)pair * a.slot_stride + split) * a.rpad;
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
 
   for (int r = warp; r < a.R; r += nw) {
     const int t = r / a.G, gq = r % a.G;
@@ -122,7 +123,6 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
       a.part_ml[(slot + r) * 2 + 1] = st.l;
     }
   }
-  pdl_trigger();
 }
 
 template <typename T>
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const long long gid = (long long)blockIdx.x * kMergeThreads + threadIdx.x;
   const long long total = (long long)a.B * a.Hkv * a.R * c4n;
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   if (gid < total) {
     const int c = (int)(gid % c4n) * 4;
     const long long pr = gid / c4n;
@@ -181,7 +182,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     T* out = static_cast<T*>(a.out) + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * a.d;
     store4<T>(out + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
-  pdl_trigger();
 }
 
 }  // namespace

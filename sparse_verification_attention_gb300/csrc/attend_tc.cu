@@ -7,31 +7,38 @@
 // one KV head are stacked into one MMA tile and each selected page is read
 // from HBM once for all of them.
 //
-// CTA roles (one CTA per SM, since tcgen05 kernels are scheduled one per SM
-// here; a 6-stage ring keeps ~192 KB of K/V in flight per SM):
-//   * producer warp: resolves selected block -> page through the block table
-//     (32 at a time, one lane each) and issues 2-D TMA copies (128-byte
-//     swizzle) of the page's K and V tiles into the ring; the draft tile (this
-//     pair's draft K/V) is written into a ring stage directly.
+// Work split (one CTA per SM, since tcgen05 kernels are scheduled one per SM
+// here): the work units of a (b, h) pair are its selected blocks plus one
+// draft tile. Stream-K plans cut the flattened (pair, unit) sequence into one
+// equal run per CTA, so a CTA covers the tail of one pair and the head of the
+// next at most (two segments, each with its own Q in shared memory); plans
+// that cannot (fewer units than CTAs) give each pair whole splits.
+//
+// CTA roles (a 6-stage ring keeps ~192 KB of K/V in flight per SM):
+//   * producer warp: loads the first segment's Q by 3-D TMA, resolves selected
+//     block -> page through the block table (32 at a time, one lane each) and
+//     issues 2-D TMA copies (128-byte swizzle) of the page's K and V tiles
+//     into the ring; the draft tile (the pair's draft K/V rows) comes the
+//     same way, through a 3-D map over the draft tensors.
 //   * MMA warp (one elected lane): S_i = Q K_i^T into TMEM (M=128 rows, N=64
 //     tokens, K=128), then after softmax O += P_i V_i with P read from TMEM
-//     (M=128, N=128, K=64, V as an MN-major operand); stages are released by
-//     tcgen05 commits.
-//   * two softmax sets: set A takes the even work units, set B the odd ones,
-//     each with its own S, P and O in TMEM, so two independent softmax
-//     chains overlap. In each set the warp owning TMEM lane quarter q holds
-//     stacked rows 32q..32q+31, one row per thread (quarters past ceil(R/32)
-//     hold only zero padding rows and stay idle). Each set keeps its own
-//     running max (log2 domain; the accumulator is rescaled only when some
-//     row's max grows by more than 2^8, decided per warp so that the
-//     warp-collective TMEM loads/stores are taken by all lanes) and sum: the
-//     two sets are independent partials, folded with log-sum-exp weights in
-//     the epilogue.
-//   * epilogue: the split's unnormalised (o, m, l) rows go to the workspace;
-//     the last CTA of each (b, h) to finish (an atomic arrival count in the
-//     workspace, reset by that CTA) merges the pair's splits with log-sum-exp
-//     weights and writes the output. The grid is 1-D with a non-uniform split
-//     map so that every SM holds one CTA.
+//     (M=128, N=128, K=64, V as an MN-major operand); the first P.V of each
+//     softmax set in a segment starts a fresh accumulator; stages are
+//     released by tcgen05 commits.
+//   * two softmax sets: set A takes the even tiles, set B the odd ones, each
+//     with its own S, P and O in TMEM, so two independent softmax chains
+//     overlap. In each set the warp owning TMEM lane quarter q holds stacked
+//     rows 32q..32q+31, one row per thread (quarters past ceil(R/32) hold
+//     only zero padding rows and stay idle). Each set keeps its own running
+//     max (log2 domain; the accumulator is rescaled only when some row's max
+//     grows by more than 2^8, decided per warp so that the warp-collective
+//     TMEM loads/stores are taken by all lanes) and sum.
+//   * partials: a segment that ends mid-stream writes each set's unnormalised
+//     (o, m, l) rows from registers; the final segment folds the two sets in
+//     shared memory first. At the end of the CTA every segment counts one
+//     atomic arrival in the workspace; the CTA that arrives last for a pair
+//     merges all of its partials with log-sum-exp weights, writes the output
+//     and resets the count.
 // Rows past R are padding: zero query rows whose outputs are never read.
 #include <atomic>
 
@@ -52,8 +59,12 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int x) { return x ? 64u : 0u; }
 __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 256u : 128u; }
 __host__ __device__ constexpr uint32_t col_p(int x) { return x ? 416u : 384u; }
+// TMEM columns 448..511: the second segment's Q (128 rows x 128 bf16, two per
+// column), the A operand of that segment's S = Q K^T
+constexpr uint32_t kColQ1 = 448;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kMaxMergeSplits = 8;  // splits merged with all loads in flight
+constexpr int kMaxMergeSplits = 8;  // partials merged with all loads in flight
+constexpr int kMaxSeg = 2;          // pair segments per CTA
 
 constexpr int r1024(int x) { return (x + 1023) / 1024 * 1024; }
 
@@ -62,9 +73,10 @@ struct TcCfg {
   static constexpr int kThreads = 32 * 10;        // 8 softmax + producer + MMA
   static constexpr int kRows = 32 * NSW;          // stacked rows held in TMEM lanes (>= R)
   static constexpr int kQBox = 128 * 128;         // one 64-column Q box, 128 rows
-  static constexpr int kRingOff = 2 * kQBox;
+  static constexpr int kQBytes = 2 * kQBox;       // the first segment's Q operand
+  static constexpr int kRingOff = kQBytes;
   static constexpr int kOst = TD + 4;
-  static constexpr int kMergeBytes = (2 * kRows * kOst + 2 * kRows * 2) * 4;
+  static constexpr int kMergeBytes = (2 * kRows * kOst + 3 * kRows * 2) * 4;
   static constexpr int kRingRaw = NS * kStageBytes;
   static constexpr int kRing = r1024(kMergeBytes > kRingRaw ? kMergeBytes : kRingRaw);
   static constexpr int kCtrlOff = kRingOff + kRing;
@@ -80,42 +92,98 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
   return row * 128 + ((chunk16 ^ (row & 7)) << 4);
 }
 
+// The work of one CTA: up to kMaxSeg segments, each a run of consecutive work
+// units [u0, u1) of one (b, h) pair (units 0..n_sel-1 are the selected
+// blocks, unit n_sel the draft tile).
+struct SegPlan {
+  int n;
+  int pair[kMaxSeg], u0[kMaxSeg], u1[kMaxSeg];
+  int slot[kMaxSeg];  // this CTA's partial slot among the pair's segments
+  int nseg[kMaxSeg];  // segments of the pair (over all CTAs)
+  int mid[kMaxSeg];   // the pair's last segment ends mid-stream in its CTA
+};
+
+// Partial results of a pair: final segments (the CTA's last) fold both
+// softmax sets and use their slot; a segment that ends mid-stream writes its
+// two sets separately, set B in the extra slot nseg. Every segment counts one
+// arrival at the end of its CTA.
+__device__ SegPlan plan_segments(const AttendArgs& a) {
+  SegPlan sp{};
+  const int W = a.n_sel + 1;
+  const int c = blockIdx.x;
+  if (a.streamk) {
+    // stream-K: the flattened (pair, unit) sequence cut into gridDim.x equal
+    // runs; the host guarantees every run is non-empty and no longer than a
+    // pair, so a run spans at most two pairs
+    const long long G = gridDim.x, U = (long long)a.B * a.Hkv * W;
+    const long long f0 = (long long)c * U / G, f1 = (long long)(c + 1) * U / G;
+    auto cta_of = [&](long long f) { return (int)(((f + 1) * G - 1) / U); };
+    long long f = f0;
+    while (f < f1 && sp.n < kMaxSeg) {
+      const int p = (int)(f / W);
+      const long long pbeg = (long long)p * W, pend = pbeg + W;
+      const long long e = f1 < pend ? f1 : pend;
+      const int first = cta_of(pbeg), last = cta_of(pend - 1);
+      sp.pair[sp.n] = p;
+      sp.u0[sp.n] = (int)(f - pbeg);
+      sp.u1[sp.n] = (int)(e - pbeg);
+      sp.slot[sp.n] = c - first;
+      sp.nseg[sp.n] = last - first + 1;
+      // the pair's last CTA carries on into the next pair
+      sp.mid[sp.n] = ((long long)(last + 1) * U / G > pend) ? 1 : 0;
+      ++sp.n;
+      f = e;
+    }
+  } else {
+    int pair, split, nsp;
+    split_of_cta(c, a.n_splits, a.split_extra, &pair, &split, &nsp);
+    const int bps = (W + nsp - 1) / nsp;
+    sp.n = 1;
+    sp.pair[0] = pair;
+    sp.u0[0] = min(W, split * bps);
+    sp.u1[0] = min(W, sp.u0[0] + bps);
+    sp.slot[0] = split;
+    sp.nseg[0] = nsp;
+    sp.mid[0] = 0;
+  }
+  return sp;
+}
+
 template <int NSW, int NS>
 __global__ void __launch_bounds__(32 * 10, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttendArgs a) {
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDK,
+                     const __grid_constant__ CUtensorMap tmDV, const __grid_constant__ AttendArgs a) {
   using C = TcCfg<NSW, NS>;
   constexpr int PRODUCER = 8, MMAW = 9;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* qs = smem;
+  uint8_t* qs = smem;  // [kMaxSeg][2 boxes]
   uint8_t* ring = smem + C::kRingOff;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kCtrlOff);
   uint64_t* empty = full + NS;
   uint64_t* s_full = empty + NS;   // [2] per set
-  uint64_t* p_ready = s_full + 2;  // [2] per set, 4 warps each
+  uint64_t* p_ready = s_full + 2;  // [2] per set, NSW warps each
   uint64_t* o_done = p_ready + 2;  // [2] per set
   uint64_t* mma_done = o_done + 2; // drain: every issued MMA has completed
   uint64_t* q_ready = mma_done + 1; // Q landed (TMA) and padding rows zeroed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+  uint64_t* q1_ready = q_ready + 1; // second segment's Q written into TMEM
+  uint64_t* mrg_bar = q1_ready + 1; // a merge's partials landed in the ring
+  uint64_t* mid_done = mrg_bar + 1; // the mid-stream segment's partials are written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mid_done + 1);
   int* stage_info = reinterpret_cast<int*>(tmem_slot + 1);  // bit0 valid, bit1 draft tile
   volatile int* abort_flag = stage_info + NS;
-  volatile int* last_flag = abort_flag + 1;
+  volatile int* merge_flag = abort_flag + 1;  // [kMaxSeg]: this CTA merges that pair
   // ancestor masks of the drafts, copied out of the parameter space with
   // warp-uniform indices (per-lane indices into it would serialize)
   __shared__ unsigned long long s_anc[kMaxT];
 
-  int pair, split, nsp;
-  split_of_cta(blockIdx.x, a.n_splits, a.split_extra, &pair, &split, &nsp);
-  const int b = pair / a.Hkv, h = pair % a.Hkv;
+  const SegPlan sp = plan_segments(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bps = (a.n_sel + 1 + nsp - 1) / nsp;
-  const int u0 = split * bps;
-  const int u1 = min(a.n_sel + 1, u0 + bps);
-  const int nunits = max(0, u1 - u0);
-  const int nblk = max(0, min(u1, a.n_sel) - u0);
-  const bool has_draft = (u0 <= a.n_sel && a.n_sel < u1);
+  const int n0 = sp.n > 0 ? sp.u1[0] - sp.u0[0] : 0;
+  const int ntot = n0 + (sp.n > 1 ? sp.u1[1] - sp.u0[1] : 0);
+  auto seg_of = [&](int i) { return i < n0 ? 0 : 1; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -129,11 +197,17 @@ __global__ void __launch_bounds__(32 * 10, 1)
     }
     mbar_init(smem_u32(mma_done), 1);
     mbar_init(smem_u32(q_ready), 5);  // producer's expect_tx + 4 zeroing warps
+    mbar_init(smem_u32(q1_ready), 4);
+    mbar_init(smem_u32(mrg_bar), 1);
+    mbar_init(smem_u32(mid_done), 2 * NSW);
     *abort_flag = 0;
+    for (int j = 0; j < kMaxSeg; ++j) merge_flag[j] = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmDK);
+    prefetch_tensormap(&tmDV);
   }
   if (warp == MMAW) {
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
@@ -146,11 +220,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // everything below may read what earlier kernels wrote
+  pdl_wait();     // everything below may read what earlier kernels wrote
+  pdl_trigger();  // let the next kernel launch and run its prologue
 
   // Q operand, 128 rows: rows r < R = the stacked query rows (draft t, head
-  // g) = Q[b, t, h*G + g] in order r = t*G + g, brought by one 3-D TMA box per
-  // 64 dims (issued first by the producer); rows R..127 are zeroed here.
+  // g) = Q[b, t, h*G + g] in order r = t*G + g. The first segment's Q comes by
+  // one 3-D TMA box per 64 dims (issued first by the producer) with rows
+  // R..127 zeroed here; the second segment's Q is written by these four warps
+  // into TMEM (lane = row), where the MMA reads it as a tensor-memory A operand.
   if (warp < 4) {
     const int r = threadIdx.x;
     if (r >= a.R) {
@@ -161,121 +238,166 @@ __global__ void __launch_bounds__(32 * 10, 1)
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(q_ready));
+    if (sp.n > 1) {
+      const int b1 = sp.pair[1] / a.Hkv, h1 = sp.pair[1] % a.Hkv;
+      const uint4* q1 = static_cast<const uint4*>(a.q) +
+                        (((size_t)b1 * a.T + r / a.G) * a.Hq + h1 * a.G + r % a.G) * (TD / 8);
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = (r < a.R) ? q1[half * 8 + c] : make_uint4(0, 0, 0, 0);
+          qv[4 * c] = u.x;
+          qv[4 * c + 1] = u.y;
+          qv[4 * c + 2] = u.z;
+          qv[4 * c + 3] = u.w;
+        }
+        tc::st32(tmem + lane_base + kColQ1 + 32 * half, qv);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(q1_ready));
+    }
   }
 
-  // per-thread results for the epilogue (softmax threads)
+  // per-thread results of the final segment for the epilogue (softmax threads)
   float o_row[TD];
   float m_run = -INFINITY, l_run = 0.f;
 
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // the query rows first, ahead of the K/V stream
+    if (lane == 0 && sp.n > 0) {
+      // the first segment's query rows first, ahead of the K/V stream
       const uint32_t qb = smem_u32(q_ready);
-      mbar_arrive_expect_tx(qb, (uint32_t)a.R * TD * 2);
+      mbar_arrive_expect_tx(qb, (uint32_t)(a.R * TD * 2));
+      const int b = sp.pair[0] / a.Hkv, h = sp.pair[0] % a.Hkv;
       tma_load_3d(smem_u32(qs), &tmQ, 0, h * a.G, b * a.T, qb);
       tma_load_3d(smem_u32(qs) + C::kQBox, &tmQ, 64, h * a.G, b * a.T, qb);
     }
     const int oob_row = a.num_pages * a.Hkv * TBLK;  // past the end: TMA zero-fills
     int issued = 0;
     bool stop = false;
-    for (int base = 0; base < nblk && !stop; base += 32) {
-      int row = oob_row, ok = 0;
-      if (base + lane < nblk) {
-        const int j = a.sel ? a.sel[(size_t)pair * a.sel_stride + u0 + base + lane] : u0 + base + lane;
-        if (j < 0 || j >= a.nb) {
-          atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
-        } else {
-          const int page = a.block_table[(size_t)b * a.nb_max + j];
-          if (page < 0 || page >= a.num_pages) {
-            atomicOr(a.status, SV_FLAG_BAD_PAGE);
+    int i = 0;  // tile index over all segments
+    for (int j = 0; j < sp.n && !stop; ++j) {
+      const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+      const int ub = sp.u0[j];
+      const int nblk = max(0, min(sp.u1[j], a.n_sel) - ub);
+      for (int base = 0; base < nblk && !stop; base += 32) {
+        int row = oob_row, ok = 0;
+        if (base + lane < nblk) {
+          const int jb = a.sel ? a.sel[(size_t)pair * a.sel_stride + ub + base + lane] : ub + base + lane;
+          if (jb < 0 || jb >= a.nb) {
+            atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
           } else {
-            row = (page * a.Hkv + h) * TBLK;
-            ok = 1;
+            const int page = a.block_table[(size_t)b * a.nb_max + jb];
+            if (page < 0 || page >= a.num_pages) {
+              atomicOr(a.status, SV_FLAG_BAD_PAGE);
+            } else {
+              row = (page * a.Hkv + h) * TBLK;
+              ok = 1;
+            }
+          }
+        }
+        const int cnt = min(32, nblk - base);
+        for (int qq = 0; qq < cnt; ++qq, ++i) {
+          const int rq = __shfl_sync(0xffffffffu, row, qq);
+          const int okq = __shfl_sync(0xffffffffu, ok, qq);
+          int fail = 0;
+          if (lane == 0) {
+            const int s = i % NS;
+            if (i >= NS &&
+                !mbar_wait_abortable(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, abort_flag, a.status, 1u)) {
+              fail = 1;
+            } else {
+              stage_info[s] = okq;
+              const uint32_t fb = smem_u32(&full[s]);
+              mbar_arrive_expect_tx(fb, kStageBytes);
+              const uint32_t kdst = smem_u32(ring + s * kStageBytes);
+              const uint32_t vdst = kdst + kTileBytes;
+              tma_load_2d(kdst, &tmK, 0, rq, fb);
+              tma_load_2d(kdst + kBoxBytes, &tmK, 64, rq, fb);
+              tma_load_2d(vdst, &tmV, 0, rq, fb);
+              tma_load_2d(vdst + kBoxBytes, &tmV, 64, rq, fb);
+              issued = i + 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, fail, 0)) {
+            stop = true;
+            break;
           }
         }
       }
-      const int cnt = min(32, nblk - base);
-      for (int qq = 0; qq < cnt; ++qq) {
-        const int i = base + qq;
-        const int rq = __shfl_sync(0xffffffffu, row, qq);
-        const int okq = __shfl_sync(0xffffffffu, ok, qq);
+      if (sp.u0[j] <= a.n_sel && a.n_sel < sp.u1[j] && !stop) {
+        // draft tile: this pair's draft rows t < T by TMA like any page; rows
+        // T..63 lie outside the draft tensor and arrive as zeros (the softmax
+        // masks them as well)
         int fail = 0;
         if (lane == 0) {
           const int s = i % NS;
           if (i >= NS &&
-              !mbar_wait_abortable(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, abort_flag, a.status, 1u)) {
+              !mbar_wait_abortable(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, abort_flag, a.status, 2u)) {
             fail = 1;
           } else {
-            stage_info[s] = okq;
+            stage_info[s] = 3;
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, kStageBytes);
             const uint32_t kdst = smem_u32(ring + s * kStageBytes);
             const uint32_t vdst = kdst + kTileBytes;
-            tma_load_2d(kdst, &tmK, 0, rq, fb);
-            tma_load_2d(kdst + kBoxBytes, &tmK, 64, rq, fb);
-            tma_load_2d(vdst, &tmV, 0, rq, fb);
-            tma_load_2d(vdst + kBoxBytes, &tmV, 64, rq, fb);
+            tma_load_4d(kdst, &tmDK, 0, h, 0, b, fb);
+            tma_load_4d(kdst + kBoxBytes, &tmDK, 64, h, 0, b, fb);
+            tma_load_4d(vdst, &tmDV, 0, h, 0, b, fb);
+            tma_load_4d(vdst + kBoxBytes, &tmDV, 64, h, 0, b, fb);
             issued = i + 1;
           }
         }
-        if (__shfl_sync(0xffffffffu, fail, 0)) {
-          stop = true;
-          break;
-        }
-      }
-    }
-    if (has_draft && !stop) {
-      // draft tile: rows u < T from this pair's draft K/V, rows T..63 zero
-      const int i = nblk, s = i % NS;
-      int fail = 0;
-      if (lane == 0 && i >= NS &&
-          !mbar_wait_abortable(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, abort_flag, a.status, 2u))
-        fail = 1;
-      if (!__shfl_sync(0xffffffffu, fail, 0)) {
-        uint8_t* st = ring + s * kStageBytes;
-        const uint4* dk = static_cast<const uint4*>(a.draft_k);
-        const uint4* dv = static_cast<const uint4*>(a.draft_v);
-        for (int idx = lane; idx < TBLK * 16; idx += 32) {
-          const int u = idx >> 4, c = idx & 15;
-          uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-          if (u < a.T) {
-            const size_t off = (((size_t)b * a.T + u) * a.Hkv + h) * (TD / 8) + c;
-            kv = dk[off];
-            vv = dv[off];
-          }
-          const uint32_t o = (c >> 3) * kBoxBytes + swz128(u, c & 7);
-          *reinterpret_cast<uint4*>(st + o) = kv;
-          *reinterpret_cast<uint4*>(st + kTileBytes + o) = vv;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          stage_info[s] = 3;
-          mbar_arrive(smem_u32(&full[s]));
-        }
-        issued = i + 1;
+        if (__shfl_sync(0xffffffffu, fail, 0)) stop = true;
+        ++i;
       }
     }
     // never leave with a bulk copy still writing into the ring
     if (lane == 0)
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        mbar_wait_drain(smem_u32(&full[i % NS]), (i / NS) & 1);
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        mbar_wait_drain(smem_u32(&full[t % NS]), (t / NS) & 1);
+    // The mid-stream segment's arrival, counted here while the CTA finishes
+    // its last tiles: the softmax warps' mbarrier arrivals order their
+    // partial stores before this thread's device-scope fence.
+    if (lane == 0 && sp.n > 1) {
+      if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
+        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+      __threadfence();
+      if (atomicAdd(&a.counters[sp.pair[0]], 1u) == (unsigned)sp.nseg[0] - 1u) {
+        __threadfence();
+        merge_flag[0] = 1;
+      }
+    }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0 && nunits > 0) {
+    if (lane == 0 && ntot > 0) {
       constexpr uint32_t idq = tc::idesc_bf16(128, 64, false, false);
       constexpr uint32_t idp = tc::idesc_bf16(128, TD, false, true);
-      const uint32_t qb = smem_u32(qs);
       const uint32_t rb = smem_u32(ring);
+      const uint32_t qb = smem_u32(qs);
+      bool q1_seen = false;
       auto issue_qk = [&](int i) {
         const uint32_t kb = rb + (i % NS) * kStageBytes;
         const uint32_t d = tmem + col_s(i & 1);
+        if (seg_of(i) == 0) {
 #pragma unroll
-        for (int kk = 0; kk < TD / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc(qb + (kk >> 2) * C::kQBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::smem_desc(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(d, ad, bd, idq, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < TD / 16; ++kk) {
+            const uint64_t ad = tc::smem_desc(qb + (kk >> 2) * C::kQBox + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = tc::smem_desc(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            tc::mma_ss(d, ad, bd, idq, kk > 0 ? 1u : 0u);
+          }
+        } else {
+          // second segment: A = Q from TMEM (16 dims = 8 columns per k-step)
+#pragma unroll
+          for (int kk = 0; kk < TD / 16; ++kk) {
+            const uint64_t bd = tc::smem_desc(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            tc::mma_ts(d, tmem + kColQ1 + kk * 8, bd, idq, kk > 0 ? 1u : 0u);
+          }
         }
         tc::commit(smem_u32(&s_full[i & 1]));
       };
@@ -283,22 +405,33 @@ __global__ void __launch_bounds__(32 * 10, 1)
                 mbar_wait_abortable(smem_u32(&full[0]), 0, abort_flag, a.status, 4u);
       tc::fence_after();
       if (ok) issue_qk(0);
-      for (int i = 0; ok && i < nunits; ++i) {
+      for (int i = 0; ok && i < ntot; ++i) {
         // S buffer of unit i+1's set is free: its previous reader (softmax of
         // unit i-1) arrived on p_ready before PV(i-1) was issued
-        if (i + 1 < nunits) {
+        if (i + 1 < ntot) {
           if (!mbar_wait_abortable(smem_u32(&full[(i + 1) % NS]), ((i + 1) / NS) & 1, abort_flag,
                                    a.status, 5u)) {
             ok = false;
             break;
           }
+          if (seg_of(i + 1) == 1 && !q1_seen) {
+            if (!mbar_wait_abortable(smem_u32(q1_ready), 0, abort_flag, a.status, 7u)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+            q1_seen = true;
+          }
           issue_qk(i + 1);
         }
+        // p_ready also says the set has read out its previous segment's O, so
+        // the first P.V of a segment may overwrite it
         if (!mbar_wait_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
           ok = false;
           break;
         }
         tc::fence_after();
+        const int first = seg_of(i) ? n0 : 0;  // the segment's first tile
         const uint32_t vb = rb + (i % NS) * kStageBytes + kTileBytes;
         const uint32_t pa = tmem + col_p(i & 1);
 #pragma unroll
@@ -307,7 +440,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
           // next 64 dims one box further, LBO), 8 tokens per 1024-byte group
           // (SBO); each k-step covers 16 tokens = two groups.
           const uint64_t bd = tc::smem_desc(vb + kt * 2048, kBoxBytes, 1024);
-          tc::mma_ts(tmem + col_o(i & 1), pa + kt * 8, bd, idp, (i >= 2 || kt > 0) ? 1u : 0u);
+          tc::mma_ts(tmem + col_o(i & 1), pa + kt * 8, bd, idp, (i - first >= 2 || kt > 0) ? 1u : 0u);
         }
         tc::commit(smem_u32(&empty[i % NS]));
         tc::commit(smem_u32(&o_done[i & 1]));
@@ -318,126 +451,156 @@ __global__ void __launch_bounds__(32 * 10, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // set X = warp / 4 takes units X, X+2, ...; the warp with lane quarter q
-    // owns stacked rows 32q..32q+31 (quarters >= NSW hold only padding rows
-    // and stay idle)
+    // set X = warp / 4 takes tiles X, X+2, ... over all segments; the warp
+    // with lane quarter q owns stacked rows 32q..32q+31 (quarters >= NSW hold
+    // only padding rows and stay idle)
     const int X = warp >> 2;
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
+    const bool active = q4 < NSW;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const uint32_t colS = col_s(X), colO = col_o(X), colP = col_p(X);
     // visible drafts of this row (bits < T only); padding rows see none
     const unsigned long long vis = (r < a.R) ? s_anc[r / a.G] : 0ull;
-    const int nmine = (q4 < NSW && nunits > X) ? (nunits - X + 1) / 2 : 0;
     bool ok = true;
-    for (int k = 0; k < nmine; ++k) {
-      const int i = X + 2 * k;
-      const int s = i % NS;
-      // every branch that guards a warp-collective tcgen05 instruction must be
-      // taken by all 32 lanes together: wait outcomes are made warp-uniform
-      const bool got =
-          mbar_wait_abortable(smem_u32(&s_full[X]), k & 1, abort_flag, a.status, 8u) &&
-          mbar_wait_abortable(smem_u32(&full[s]), (i / NS) & 1, abort_flag, a.status, 9u);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after();
-      float v[64];
-#pragma unroll
-      for (int h32 = 0; h32 < 2; ++h32) {
-        uint32_t sr[32];
-        tc::ld32(tmem + lane_base + colS + 32 * h32, sr);
-        tc::wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[32 * h32 + j] = __uint_as_float(sr[j]);
-      }
-      const int info = stage_info[s];
-      if (info != 1) {
-        // invalid tile: nothing kept; draft tile: the row's visible drafts
-        // (branch-free: one 64-bit keep mask, one select per column)
-        const unsigned long long keepb = (info & 1) ? ((info & 2) ? vis : ~0ull) : 0ull;
-        const uint32_t klo = (uint32_t)keepb, khi = (uint32_t)(keepb >> 32);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = ((klo >> j) & 1u) ? v[j] : -INFINITY;
-          v[32 + j] = ((khi >> j) & 1u) ? v[32 + j] : -INFINITY;
-        }
-      }
-      float mraw = v[0];
-#pragma unroll
-      for (int j = 1; j < 64; ++j) mraw = fmaxf(mraw, v[j]);
-      const float mx = mraw * a.scale_log2;  // scale > 0: max commutes with it
-      // This set's previous P.V must be done before P and (on a rescale) O are
-      // touched again.
-      if (k > 0) {
-        const bool got2 = mbar_wait_abortable(smem_u32(&o_done[X]), (k - 1) & 1, abort_flag,
-                                              a.status, 10u);
-        if (!__all_sync(0xffffffffu, got2)) {
+    int i = X;  // this set's next tile
+    int k = 0;  // this set's tiles so far (all segments): barrier phases
+    for (int j = 0; j < sp.n && active; ++j) {
+      const int seg_end = j == 0 ? n0 : ntot;
+      m_run = -INFINITY;
+      l_run = 0.f;
+      int kseg = 0;  // this set's tiles in segment j
+      for (; ok && i < seg_end; i += 2, ++k, ++kseg) {
+        const int s = i % NS;
+        // every branch that guards a warp-collective tcgen05 instruction must be
+        // taken by all 32 lanes together: wait outcomes are made warp-uniform
+        const bool got =
+            mbar_wait_abortable(smem_u32(&s_full[X]), k & 1, abort_flag, a.status, 8u) &&
+            mbar_wait_abortable(smem_u32(&full[s]), (i / NS) & 1, abort_flag, a.status, 9u);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc::fence_after();
-      }
-      // Lazy rescale, decided per warp: when any row's max grew by more than
-      // 2^8, every lane moves its reference to max(m_run, mx) (alpha = 1 for
-      // rows whose max did not grow).
-      if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);  // 0 if m_run = -inf
-        if (k > 0) {
+        float v[64];
 #pragma unroll
-          for (int cc = 0; cc < TD / 32; ++cc) {
-            uint32_t ov[32];
-            tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
-            tc::wait_ld();
+        for (int h32 = 0; h32 < 2; ++h32) {
+          uint32_t sr[32];
+          tc::ld32(tmem + lane_base + colS + 32 * h32, sr);
+          tc::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tc::st32(tmem + lane_base + colO + 32 * cc, ov);
+          for (int jj = 0; jj < 32; ++jj) v[32 * h32 + jj] = __uint_as_float(sr[jj]);
+        }
+        const int info = stage_info[s];
+        if (info != 1) {
+          // invalid tile: nothing kept; draft tile: the row's visible drafts
+          // (branch-free: one 64-bit keep mask, one select per column)
+          const unsigned long long keepb = (info & 1) ? ((info & 2) ? vis : ~0ull) : 0ull;
+          const uint32_t klo = (uint32_t)keepb, khi = (uint32_t)(keepb >> 32);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            v[jj] = ((klo >> jj) & 1u) ? v[jj] : -INFINITY;
+            v[32 + jj] = ((khi >> jj) & 1u) ? v[32 + jj] : -INFINITY;
           }
         }
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
-      uint32_t pk[32];
-      float ls = 0.f;
+        float mraw = v[0];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p0 = exp2f(fmaf(v[2 * j], a.scale_log2, nbase));
-        const float p1 = exp2f(fmaf(v[2 * j + 1], a.scale_log2, nbase));
-        ls += p0 + p1;
-        pk[j] = pack_bf16(p0, p1);
+        for (int jj = 1; jj < 64; ++jj) mraw = fmaxf(mraw, v[jj]);
+        const float mx = mraw * a.scale_log2;  // scale > 0: max commutes with it
+        // This set's previous P.V must be done before P and (on a rescale) O
+        // are touched again.
+        if (k > 0) {
+          const bool got2 = mbar_wait_abortable(smem_u32(&o_done[X]), (k - 1) & 1, abort_flag,
+                                                a.status, 10u);
+          if (!__all_sync(0xffffffffu, got2)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+        }
+        // Lazy rescale, decided per warp: when any row's max grew by more than
+        // 2^8, every lane moves its reference to max(m_run, mx) (alpha = 1 for
+        // rows whose max did not grow). A segment's first tile has no O yet.
+        if (__any_sync(0xffffffffu, mx > m_run + kRescaleLog2)) {
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);  // 0 if m_run = -inf
+          if (kseg > 0) {
+#pragma unroll
+            for (int cc = 0; cc < TD / 32; ++cc) {
+              uint32_t ov[32];
+              tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tc::st32(tmem + lane_base + colO + 32 * cc, ov);
+            }
+          }
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
+        uint32_t pk[32];
+        float ls = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const float p0 = exp2f(fmaf(v[2 * jj], a.scale_log2, nbase));
+          const float p1 = exp2f(fmaf(v[2 * jj + 1], a.scale_log2, nbase));
+          ls += p0 + p1;
+          pk[jj] = pack_bf16(p0, p1);
+        }
+        l_run += ls;
+        tc::st32(tmem + lane_base + colP, pk);
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_ready[X]));
       }
-      l_run += ls;
-      tc::st32(tmem + lane_base + colP, pk);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_ready[X]));
+      // read out this set's O of segment j (its last P.V must have finished)
+      bool fin = ok && kseg > 0;
+      if (fin)
+        fin = mbar_wait_abortable(smem_u32(&o_done[X]), (k - 1) & 1, abort_flag, a.status, 11u);
+      if (__all_sync(0xffffffffu, fin)) {
+        tc::fence_after();
+#pragma unroll
+        for (int cc = 0; cc < TD / 32; ++cc) {
+          uint32_t ov[32];
+          tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o_row[32 * cc + e] = __uint_as_float(ov[e]);
+        }
+      } else {
+        if (kseg > 0 || !ok) atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+#pragma unroll
+        for (int e = 0; e < TD; ++e) o_row[e] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
+      if (j + 1 < sp.n) {
+        // Mid-stream segment: this set's partial goes straight to the
+        // workspace (set A in the segment's slot, set B in the pair's extra
+        // slot nseg); the producer warp counts its arrival once every warp
+        // has signalled mid_done. The next segment's first P.V overwrites O
+        // only after this set's next p_ready arrival.
+        const int pair = sp.pair[j];
+        const int pslot = X == 0 ? sp.slot[j] : sp.nseg[j];
+        const size_t row = ((size_t)pair * a.slot_stride + pslot) * a.rpad + r;
+        if (r < a.R) {
+#pragma unroll
+          for (int c = 0; c < TD; c += 4)
+            *reinterpret_cast<float4*>(a.part_o + row * TD + c) =
+                make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
+          *reinterpret_cast<float2*>(a.part_ml + row * 2) = make_float2(m_run, l_run);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(mid_done));
+      }
     }
-    bool fin = ok && nmine > 0;
-    if (fin)
-      fin = mbar_wait_abortable(smem_u32(&o_done[X]), (nmine - 1) & 1, abort_flag, a.status, 11u);
-    if (__all_sync(0xffffffffu, fin)) {
-      tc::fence_after();
-#pragma unroll
-      for (int cc = 0; cc < TD / 32; ++cc) {
-        uint32_t ov[32];
-        tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o_row[32 * cc + e] = __uint_as_float(ov[e]);
-      }
-    } else {
-      if (nmine > 0) atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+    if (!active) {
 #pragma unroll
       for (int e = 0; e < TD; ++e) o_row[e] = 0.f;
-      m_run = -INFINITY;
-      l_run = 0.f;
     }
   }
-  pdl_trigger();
 
   tc::fence_before();
   __syncthreads();  // all TMEM reads and MMAs done; the ring is idle
@@ -447,103 +610,87 @@ __global__ void __launch_bounds__(32 * 10, 1)
   }
 
   // ---------------------------------------------------------------- epilogue
-  // Stage both sets' (o, m, l) for the kRows real lanes; fold set B into set A
-  // with log-sum-exp weights (row r of set X staged at X*kRows + r).
+  // The final segment: stage both sets' (o, m, l) for the kRows real lanes and
+  // fold set B into set A with log-sum-exp weights (row r of set X staged at
+  // X*kRows + r).
   constexpr int NT = 32 * 10;
   constexpr int OST = C::kOst;
   constexpr int KR = C::kRows;
   float* po = reinterpret_cast<float*>(ring);   // [2*KR][OST]
-  float* pml = po + (size_t)2 * KR * OST;       // [2*KR][2]
-  if (warp < 8 && (warp & 3) < NSW) {
-    const int row = (warp >> 2) * KR + 32 * (warp & 3) + lane;
+  float* pml = po + (size_t)2 * KR * OST;       // [2*KR][2], then [KR][2] weights
+  const int jf = sp.n - 1;  // final segment (none when the CTA has no work)
+  if (jf >= 0) {
+    const int pair = sp.pair[jf];
+    const size_t slot = ((size_t)pair * a.slot_stride + sp.slot[jf]) * a.rpad;
+    if (warp < 8 && (warp & 3) < NSW) {
+      const int row = (warp >> 2) * KR + 32 * (warp & 3) + lane;
 #pragma unroll
-    for (int c = 0; c < TD; c += 4)
-      *reinterpret_cast<float4*>(po + row * OST + c) =
-          make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
-    *reinterpret_cast<float2*>(pml + 2 * row) = make_float2(m_run, l_run);
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < KR * (TD / 4); idx += NT) {
-    const int r = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
-    const float2 ma = *reinterpret_cast<const float2*>(pml + 2 * r);
-    const float2 mb = *reinterpret_cast<const float2*>(pml + 2 * (KR + r));
-    const float M = fmaxf(ma.x, mb.x);
-    const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
-    const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
-    const float4 oa = *reinterpret_cast<const float4*>(po + r * OST + c4);
-    const float4 ob = *reinterpret_cast<const float4*>(po + (KR + r) * OST + c4);
-    // (r, c4) is read and written by this thread only
-    *reinterpret_cast<float4*>(po + r * OST + c4) =
-        make_float4(wa * oa.x + wb * ob.x, wa * oa.y + wb * ob.y, wa * oa.z + wb * ob.z,
-                    wa * oa.w + wb * ob.w);
-  }
-  __syncthreads();
-  for (int r = threadIdx.x; r < KR; r += NT) {
-    const float2 ma = *reinterpret_cast<const float2*>(pml + 2 * r);
-    const float2 mb = *reinterpret_cast<const float2*>(pml + 2 * (KR + r));
-    const float M = fmaxf(ma.x, mb.x);
-    const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
-    const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
-    *reinterpret_cast<float2*>(pml + 2 * r) = make_float2(M, wa * ma.y + wb * mb.y);
+      for (int c = 0; c < TD; c += 4)
+        *reinterpret_cast<float4*>(po + row * OST + c) =
+            make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
+      *reinterpret_cast<float2*>(pml + 2 * row) = make_float2(m_run, l_run);
+    }
+    __syncthreads();
+    // per-row weights of the two sets (w_X = 2^(m_X - M)) and the folded (M, L)
+    float* pw = pml + (size_t)4 * KR;  // [KR][2]
+    for (int rr = threadIdx.x; rr < KR; rr += NT) {
+      const float2 ma = *reinterpret_cast<const float2*>(pml + 2 * rr);
+      const float2 mb = *reinterpret_cast<const float2*>(pml + 2 * (KR + rr));
+      const float M = fmaxf(ma.x, mb.x);
+      const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
+      const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
+      *reinterpret_cast<float2*>(pw + 2 * rr) = make_float2(wa, wb);
+      if (rr < a.rpad)
+        *reinterpret_cast<float2*>(a.part_ml + (slot + rr) * 2) = make_float2(M, wa * ma.y + wb * mb.y);
+    }
+    __syncthreads();
+    // folded rows straight to the workspace (rows past kRows are zero padding)
+    for (int idx = threadIdx.x; idx < a.rpad * (TD / 4); idx += NT) {
+      const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rr < KR) {
+        const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
+        const float4 oa = *reinterpret_cast<const float4*>(po + rr * OST + c4);
+        const float4 ob = *reinterpret_cast<const float4*>(po + (KR + rr) * OST + c4);
+        v = make_float4(w.x * oa.x + w.y * ob.x, w.x * oa.y + w.y * ob.y, w.x * oa.z + w.y * ob.z,
+                        w.x * oa.w + w.y * ob.w);
+      }
+      *reinterpret_cast<float4*>(a.part_o + (slot + rr) * TD + c4) = v;
+    }
+    // CTA barrier, then one thread's device-scope fence publishes every
+    // thread's partial writes before the final segment's arrival (the
+    // barrier orders them before the fence); the last arrival for a pair
+    // fences again before the merge reads. (A mid-stream segment arrived
+    // from the producer warp.)
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(&a.counters[pair], 1u) == (unsigned)sp.nseg[jf] - 1u) {
+        __threadfence();
+        merge_flag[jf] = 1;
+      }
+    }
   }
   __syncthreads();
 
-  // ---------------------------------------- split partial, then last-CTA merge
-  const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-  const size_t slot = pbase + (size_t)split * a.rpad;
-  for (int idx = threadIdx.x; idx < a.rpad * (TD / 4); idx += NT) {
-    const int r = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-    *reinterpret_cast<float4*>(a.part_o + (slot + r) * TD + c) =
-        *reinterpret_cast<const float4*>(po + r * OST + c);
-  }
-  for (int r = threadIdx.x; r < a.rpad; r += NT)
-    *reinterpret_cast<float2*>(a.part_ml + (slot + r) * 2) = *reinterpret_cast<const float2*>(pml + 2 * r);
-  // The last split of this (b, h) to arrive combines all of them:
+  // ------------------------------------------------------- merge of a pair
+  // The CTA that arrived last for a pair combines all of its partials:
   //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s.
-  // CTA barrier, then one thread's device-scope fence publishes every
-  // thread's partial writes before the arrival count (the barrier orders
-  // them before the fence); the last arrival fences again before reading.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const bool last = atomicAdd(&a.counters[pair], 1u) == (unsigned)nsp - 1u;
-    if (last) __threadfence();
-    *last_flag = last;
-  }
-  __syncthreads();
-  if (*last_flag) {
+  // When they fit in the (now idle) ring, the partials arrive by bulk copies
+  // in one round trip and are combined from shared memory; otherwise each
+  // thread loads its items' partials from global memory, kMaxMergeSplits at
+  // a time.
+  int mrg_uses = 0;
+  for (int j = 0; j < sp.n; ++j) {
+    if (!merge_flag[j]) continue;
+    const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+    const int ns = sp.nseg[j] + sp.mid[j];
+    const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    // this CTA's own split is still staged in shared memory (rows < KR)
-    auto merge_item = [&](int idx, float2 (&ml)[kMaxMergeSplits], float4 (&o)[kMaxMergeSplits]) {
-      const int r = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-      float M = -INFINITY;
-#pragma unroll
-      for (int s = 0; s < kMaxMergeSplits; ++s) M = fmaxf(M, ml[s].x);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float Lsum = 0.f;
-#pragma unroll
-      for (int s = 0; s < kMaxMergeSplits; ++s) {
-        const float w = (ml[s].x == -INFINITY) ? 0.f : exp2f(ml[s].x - M);
-        Lsum += w * ml[s].y;
-        acc.x += w * o[s].x; acc.y += w * o[s].y; acc.z += w * o[s].z; acc.w += w * o[s].w;
-      }
-      // pairs with more splits than the unrolled window add the rest
-      for (int s = kMaxMergeSplits; s < nsp; ++s) {
-        const size_t row = pbase + (size_t)s * a.rpad + r;
-        const float2 m2 = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
-        const float4 o2 = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
-        if (m2.x > M) {
-          const float sc = (M == -INFINITY) ? 0.f : exp2f(M - m2.x);
-          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-          Lsum *= sc;
-          M = m2.x;
-        }
-        const float w = (m2.x == -INFINITY) ? 0.f : exp2f(m2.x - M);
-        Lsum += w * m2.y;
-        acc.x += w * o2.x; acc.y += w * o2.y; acc.z += w * o2.z; acc.w += w * o2.w;
-      }
-      const float inv = 1.0f / Lsum;
-      const int t = r / a.G, gq = r % a.G;
+    const int nitems = a.R * (TD / 4);
+    auto store = [&](int idx, float inv, float4 acc) {
+      const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+      const int t = rr / a.G, gq = rr % a.G;
       __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
       __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
       uint2 u;
@@ -551,32 +698,95 @@ __global__ void __launch_bounds__(32 * 10, 1)
       u.y = *reinterpret_cast<uint32_t*>(&hi);
       *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
     };
-    auto load_item = [&](int idx, float2 (&ml)[kMaxMergeSplits], float4 (&o)[kMaxMergeSplits]) {
-      const int r = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-#pragma unroll
-      for (int s = 0; s < kMaxMergeSplits; ++s) {
-        ml[s] = make_float2(-INFINITY, 0.f);
-        o[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s == split) {
-          ml[s] = *reinterpret_cast<const float2*>(pml + 2 * r);
-          o[s] = *reinterpret_cast<const float4*>(po + r * OST + c);
-        } else if (s < nsp) {
-          const size_t row = pbase + (size_t)s * a.rpad + r;
-          ml[s] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
-          o[s] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
+    const uint32_t ob = (uint32_t)a.rpad * TD * 4, mb = (uint32_t)a.rpad * 8;
+    // partials, their (m, l), then per-(partial, row) weights and per-row 1/L
+    const size_t need = (size_t)ns * (ob + mb) + ((size_t)ns + 1) * a.rpad * 4;
+    if (need <= (size_t)C::kRing) {
+      float* so = reinterpret_cast<float*>(ring);           // [ns][rpad][TD]
+      float* sml = so + (size_t)ns * a.rpad * TD;            // [ns][rpad][2]
+      float* sw = sml + (size_t)ns * a.rpad * 2;             // [ns][rpad]
+      float* sli = sw + (size_t)ns * a.rpad;                 // [rpad]
+      if (threadIdx.x == 0) {
+        fence_proxy_async_shared();  // earlier generic use of the ring
+        fence_proxy_async_global();  // the partial stores this CTA has acquired
+        const uint32_t bar = smem_u32(mrg_bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)ns * (ob + mb));
+        for (int s = 0; s < ns; ++s) {
+          const size_t row = pbase + (size_t)s * a.rpad;
+          bulk_load(smem_u32(so + (size_t)s * a.rpad * TD), a.part_o + row * TD, ob, bar);
+          bulk_load(smem_u32(sml + (size_t)s * a.rpad * 2), a.part_ml + row * 2, mb, bar);
         }
       }
-    };
-    const int nitems = a.R * (TD / 4);
-    for (int idx = threadIdx.x; idx < nitems; idx += 2 * NT) {
-      // two items' loads in flight before either is combined
-      float2 ml0[kMaxMergeSplits], ml1[kMaxMergeSplits];
-      float4 o0[kMaxMergeSplits], o1[kMaxMergeSplits];
-      const int idx1 = idx + NT;
-      load_item(idx, ml0, o0);
-      if (idx1 < nitems) load_item(idx1, ml1, o1);
-      merge_item(idx, ml0, o0);
-      if (idx1 < nitems) merge_item(idx1, ml1, o1);
+      const bool got = mbar_wait_drain(smem_u32(mrg_bar), mrg_uses & 1);
+      ++mrg_uses;
+      if (got) {
+        // the weights depend on (partial, row) only: computed once per row
+        for (int rr = threadIdx.x; rr < a.R; rr += NT) {
+          float M = -INFINITY;
+          for (int s = 0; s < ns; ++s) M = fmaxf(M, sml[((size_t)s * a.rpad + rr) * 2]);
+          float Lsum = 0.f;
+          for (int s = 0; s < ns; ++s) {
+            const float2 ml = *reinterpret_cast<const float2*>(sml + ((size_t)s * a.rpad + rr) * 2);
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            sw[(size_t)s * a.rpad + rr] = w;
+            Lsum += w * ml.y;
+          }
+          sli[rr] = 1.0f / Lsum;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < nitems; idx += NT) {
+          const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s = 0; s < ns; ++s) {
+            const float w = sw[(size_t)s * a.rpad + rr];
+            const float4 o = *reinterpret_cast<const float4*>(so + ((size_t)s * a.rpad + rr) * TD + c);
+            acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+          }
+          store(idx, sli[rr], acc);
+        }
+      } else if (threadIdx.x == 0) {
+        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+      }
+      __syncthreads();  // the ring is read before a second merge refills it
+    } else {
+      auto load = [&](int idx, int s0, float2 (&ml)[kMaxMergeSplits], float4 (&o)[kMaxMergeSplits]) {
+        const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+#pragma unroll
+        for (int q = 0; q < kMaxMergeSplits; ++q) {
+          ml[q] = make_float2(-INFINITY, 0.f);
+          o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s0 + q < ns) {
+            const size_t row = pbase + (size_t)(s0 + q) * a.rpad + rr;
+            ml[q] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
+            o[q] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
+          }
+        }
+      };
+      for (int idx = threadIdx.x; idx < nitems; idx += NT) {
+        float M = -INFINITY, Lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
+          float2 ml[kMaxMergeSplits];
+          float4 o[kMaxMergeSplits];
+          load(idx, s0, ml, o);
+          float Mc = M;
+#pragma unroll
+          for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
+          if (Mc > M) {
+            const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
+            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+            Lsum *= sc;
+            M = Mc;
+          }
+#pragma unroll
+          for (int q = 0; q < kMaxMergeSplits; ++q) {
+            const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
+            Lsum += w * ml[q].y;
+            acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
+          }
+        }
+        store(idx, 1.0f / Lsum, acc);
+      }
     }
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
@@ -594,14 +804,16 @@ cudaError_t launch_tc_cfg(const AttendArgs& a, cudaStream_t st) {
   using K = TcKernel<NSW>;
   CUtensorMap mk, mv;
   const char* why = nullptr;
-  CUtensorMap mq;
+  CUtensorMap mq, mdk, mdv;
   if (!encode_pool_map(&mk, a.k_pool, a.num_pages, a.Hkv, TBLK, TD, &why) ||
       !encode_pool_map(&mv, a.v_pool, a.num_pages, a.Hkv, TBLK, TD, &why) ||
-      !encode_q_map(&mq, a.q, a.B, a.T, a.Hq, a.G, TD, &why))
+      !encode_q_map(&mq, a.q, a.B, a.T, a.Hq, a.G, TD, &why) ||
+      !encode_draft_map(&mdk, a.draft_k, a.B, a.T, a.Hkv, TD, TBLK, &why) ||
+      !encode_draft_map(&mdv, a.draft_v, a.B, a.T, a.Hkv, TD, TBLK, &why))
     return cudaErrorInvalidValue;
-  const int ctas = a.B * a.Hkv * a.n_splits + a.split_extra;
+  const int ctas = a.streamk ? a.n_splits : a.B * a.Hkv * a.n_splits + a.split_extra;
   return launch_pdl(attend_tc_kernel<NSW, K::NS>, dim3(ctas), dim3(K::C::kThreads), K::C::kSmem,
-                    st, mk, mv, mq, a);
+                    st, mk, mv, mq, mdk, mdv, a);
 }
 
 // Sets the kernel's shared-memory attributes and returns its resident CTAs

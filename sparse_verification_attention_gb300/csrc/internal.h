@@ -108,6 +108,9 @@ struct AttendArgs {
   // n_splits + 1 splits, the others n_splits; partial slots of a pair are
   // slot_stride apart. Uniform plans: split_extra = 0, slot_stride = n_splits.
   int split_extra, slot_stride;
+  // tcgen05 path: 1 = stream-K (n_splits CTAs, each an equal run of the
+  // flattened (pair, unit) sequence; split_extra unused)
+  int streamk;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
 };
@@ -163,6 +166,8 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
                      int d, const char** why);
 // Q [B, T, Hq, d] bf16 viewed as (d, Hq, B*T) with boxes of (64, G, T): one
 // box is the T*G stacked query rows of one kv head, 64 dims wide.
+bool encode_draft_map(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d, int rows,
+                      const char** why);
 bool encode_q_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
                   const char** why);
 

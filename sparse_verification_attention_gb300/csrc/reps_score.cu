@@ -33,9 +33,11 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 // One CTA of kRepThreads per (logical block, kv head, sequence). Thread t owns
 // one 16-byte chunk of the head dimension (c = t % chunks) and one group of
 // tokens (g = t / chunks); each group sums its tokens in order, then the
-// groups are added in order through shared memory. All of a page's 16-byte
-// loads are independent, so the block is read in one memory round trip.
+// groups are added in order through shared memory. A thread issues the loads
+// of up to kRepBatch tokens before summing them, so a block of up to
+// kRepBatch tokens per group is read in one memory round trip.
 constexpr int kRepThreads = 128;
+constexpr int kRepBatch = 8;  // token loads in flight per thread
 
 template <typename T>
 __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
   const int groups = kRepThreads / chunks;  // >= 1 since d <= 256
   const int c = threadIdx.x % chunks, g = threadIdx.x / chunks;
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   const int page = a.block_table[(size_t)b * a.nb_max + j];
   float* dst = a.reps + (((size_t)b * a.Hkv + h) * a.nb_max + j) * a.d;
   if (page < 0 || page >= a.num_pages) {
@@ -62,13 +65,23 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
     const T* src = static_cast<const T*>(a.k_pool) + ((size_t)page * a.Hkv + h) * a.blk * a.d;
     const int per = (a.blk + groups - 1) / groups;
     const int t0 = g * per, t1 = min(a.blk, t0 + per);
-    for (int t = t0; t < t1; ++t) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src + (size_t)t * a.d) + c);
-      const T* v = reinterpret_cast<const T*>(&u);
+    // kRepBatch tokens' loads are issued before any is summed, so a group
+    // of up to kRepBatch tokens costs one memory round trip
+    for (int tb = t0; tb < t1; tb += kRepBatch) {
+      uint4 u[kRepBatch];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if constexpr (sizeof(T) == 2) acc[e] += __bfloat162float(v[e]);
-        else acc[e] += v[e];
+      for (int i = 0; i < kRepBatch; ++i)
+        u[i] = (tb + i < t1) ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)(tb + i) * a.d) + c)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < kRepBatch; ++i) {
+        if (tb + i >= t1) break;
+        const T* v = reinterpret_cast<const T*>(&u[i]);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          if constexpr (sizeof(T) == 2) acc[e] += __bfloat162float(v[e]);
+          else acc[e] += v[e];
+        }
       }
     }
   }
@@ -82,7 +95,6 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
     for (int gg = 0; gg < groups; ++gg) sum += part[(gg * chunks + ci) * VEC + ei];
     dst[i] = sum * inv;
   }
-  pdl_trigger();
 }
 
 // ------------------------------------------------------------------ scores
@@ -114,6 +126,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
   float* srow = a.scores + (size_t)pair * a.nb;
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
 
   float4 qh[CH];
   bool have_q = false;
@@ -175,7 +188,6 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
     if ((lane % S) == 0 && j < r1) srow[j] = acc[0];
   }
   if (!a.sel || a.nb > kFusedSelectMaxNB) {
-    pdl_trigger();
     return;
   }
 
@@ -196,7 +208,6 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
     cta_topk<kScoreThreads, kScoreKeys>(srow, a.nb, a.k, a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
-  pdl_trigger();
 }
 
 }  // namespace

@@ -24,10 +24,10 @@ static_assert(kSelThreads * kSelKeys >= kMaxNB, "select must hold every score");
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const __grid_constant__ SelectArgs a) {
   __shared__ TopkSmem<kSelThreads> tsm;
   pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   const int pair = blockIdx.x;
   cta_topk<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
                                   a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
-  pdl_trigger();
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 // planning and kernel launches. Declarations and contracts: include/sva.h.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -186,8 +187,10 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   WsLayout L;
   const int G = s.Hq / s.Hkv;
   L.rpad = round_up(s.T * G, 16);
-  const int units = (kmax < 0 ? 0 : kmax) + 1;  // selected blocks + the draft tile
-  L.slots = units > kMaxSplits ? kMaxSplits : units;
+  // one partial slot per work unit (selected blocks + the draft tile), plus
+  // one for a stream-K run that leaves a pair mid-stream
+  const int units = (kmax < 0 ? 0 : kmax) + 1;
+  L.slots = units + 1 > kMaxSplits ? kMaxSplits : units + 1;
   const size_t pairs = (size_t)s.B * s.Hkv;
   L.status = 0;
   L.ctr_score = kStatusBytes;
@@ -215,6 +218,30 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *why = "cuTensorMapEncodeTiled failed";
+    return false;
+  }
+  return true;
+}
+
+bool encode_draft_map(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d, int rows,
+                      const char** why) {
+  auto enc = get_encode();
+  if (!enc) {
+    *why = "cuTensorMapEncodeTiled unavailable";
+    return false;
+  }
+  // [B, T, Hkv, d] viewed as (d, Hkv, T, B): one box = `rows` draft rows of
+  // one kv head of one sequence, 64 dims wide; rows t >= T lie outside the
+  // tensor and arrive as zeros
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2, (cuuint64_t)T * Hkv * d * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dkv), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (draft) failed";
     return false;
   }
   return true;
@@ -248,7 +275,27 @@ struct AttendPlan {
   int cluster;   // > 0: in-cluster merge with this many CTAs per (b, h)
   int n_splits, bps, per_sm;
   int extra, slot_stride;  // non-uniform split map (tcgen05 path)
+  int streamk;             // tcgen05 path: n_splits CTAs share the flattened units
 };
+
+// Stream-K plan of the tcgen05 path: G CTAs, CTA c covering flattened units
+// [c*U/G, (c+1)*U/G) of U = pairs * W. Usable when every run is non-empty
+// and no longer than one pair (so a run touches at most two pairs). Returns
+// the largest number of partial slots a pair needs (its segments, plus one
+// when its last segment ends mid-run), or 0 when stream-K does not apply.
+static int streamk_slots(int pairs, int W, int G) {
+  const long long U = (long long)pairs * W;
+  if (G < 1 || U < G || (U + G - 1) / G > W) return 0;
+  auto cta_of = [&](long long f) { return (int)(((f + 1) * G - 1) / U); };
+  int most = 0;
+  for (int p = 0; p < pairs; ++p) {
+    const long long pend = (long long)(p + 1) * W;
+    const int first = cta_of(pend - W), last = cta_of(pend - 1);
+    const int mid = ((long long)(last + 1) * U / G > pend) ? 1 : 0;
+    most = std::max(most, last - first + 1 + mid);
+  }
+  return most;
+}
 
 static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int max_slots) {
   AttendPlan p{};
@@ -261,6 +308,14 @@ static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int 
     // some pairs getting one split more than others
     p.per_sm = attend_tc_ctas_per_sm(a);
     const int slots = sm_count() * (p.per_sm > 0 ? p.per_sm : 1);
+    const int sk = streamk_slots(pairs, n_units, slots);
+    if (sk > 0 && sk <= max_slots) {
+      p.streamk = 1;
+      p.n_splits = slots;
+      p.bps = (int)(((long long)pairs * n_units + slots - 1) / slots);
+      p.slot_stride = sk;
+      return p;
+    }
     int S = slots / pairs, extra = slots % pairs;
     if (S < 1) {
       S = 1;
@@ -308,6 +363,7 @@ static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, c
   a.bps = p.bps;
   a.split_extra = p.extra;
   a.slot_stride = p.slot_stride;
+  a.streamk = p.streamk;
   cudaError_t e;
   if (p.cluster > 0) {
     e = launch_attend_fast(a, p.cluster, st);
@@ -590,6 +646,7 @@ sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_p
   out->blocks_per_split = p.bps;
   out->ctas_per_sm = p.per_sm;
   out->split_extra = p.extra;
+  out->streamk = p.streamk;
   return SV_OK;
 }
 
@@ -670,6 +727,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   a.bps = p.bps;
   a.split_extra = p.extra;
   a.slot_stride = p.slot_stride;
+  a.streamk = p.streamk;
   cudaStream_t st = (cudaStream_t)stream;
   // the array keeps the previous call's contents: zero the status word and
   // the arrival counters (the partials are fully written before being read)

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version(L):
-    assert api.sv_abi_version() == 1
+    assert api.sv_abi_version() == api.ABI_VERSION == 2
 
 
 def test_budget_matches_oracle_golden(L):
@@ -80,16 +80,17 @@ def test_workspace_sizes(L):
     s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
     n = api.sv_workspace_bytes(s, 2048, 128)
     # status + two per-(b,h) counter arrays + scores + split partials o and
-    # (m, l); 129 work units (128 blocks + the draft tile) capped at 64 splits
+    # (m, l); 129 work units (128 blocks + the draft tile) capped at 64 slots
     pairs = 4 * 8
     ctrs = 2 * 256
     scores = pairs * 2048 * 4
     part = pairs * 64 * 32 * 128 * 4
     ml = pairs * 64 * 32 * 2 * 4
     assert n == 256 + ctrs + scores + part + ml
-    # 8 selected blocks + the draft tile = 9 split slots
+    # 8 selected blocks + the draft tile + one slot for a run that leaves a
+    # pair mid-stream = 10 partial slots
     n8 = api.sv_workspace_bytes(s, 2048, 8)
-    assert n8 == 256 + ctrs + scores + pairs * 9 * 32 * 128 * 4 + pairs * 9 * 32 * 2 * 4
+    assert n8 == 256 + ctrs + scores + pairs * 10 * 32 * 128 * 4 + pairs * 10 * 32 * 2 * 4
     bad = api.make_shape(4, 30, 8, 128, 64, 8, torch.bfloat16)  # Hq % Hkv != 0
     assert api.sv_workspace_bytes(bad, 2048, 128) == 0
     assert api.sv_workspace_bytes(api.make_shape(1, 4, 2, 12, 16, 4, 1), 64, 8) == 0  # d % 8

@@ -143,6 +143,14 @@ ATTEND_CASES = [
     ("tc_many_pairs_few_units", dict(B=8, Hq=32, Hkv=8, ctx=64 * 24), 2),
     ("tc_many_pairs_all_blocks", dict(B=8, Hq=32, Hkv=8, ctx=64 * 10), 10),
     ("tc_more_pairs_than_sms", dict(B=40, Hq=16, Hkv=4, ctx=64 * 6), 3),
+    # stream-K: every CTA takes an equal run of the flattened (pair, unit)
+    # sequence, crossing at most one pair boundary
+    ("tc_sk_32pairs_129units", dict(B=4, Hq=32, Hkv=8, ctx=64 * 200), 128),
+    ("tc_sk_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                               ctx=64 * 40), 29),
+    ("tc_sk_one_unit_per_cta", dict(B=4, Hq=8, Hkv=2, ctx=64 * 30), 18),
+    ("tc_sk_runs_cross_pairs", dict(B=19, Hq=4, Hkv=1, T=4, ctx=64 * 12), 8),
+    ("tc_sk_two_unit_pairs", dict(B=75, Hq=4, Hkv=2, T=2, ctx=64 * 4), 1),
     ("mma_R16_pad", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), 17),
     ("mma_R48_rows_pad", dict(Hq=8, Hkv=2, T=12, blk=32, ctx=32 * 45), 9),
     ("mma_d64_blk64", dict(d=64, ctx=64 * 30), 11),
@@ -171,6 +179,8 @@ def test_sparse_attend(name, over, n_sel):
     assert plan.path == want_path, (plan.path, want_path)
     if "cluster" in name and want_path == api.SV_PATH_MMA_SYNC:
         assert plan.cluster > 0
+    if "_sk_" in name:
+        assert plan.streamk == 1, (plan.n_splits, plan.blocks_per_split)
     out = torch.zeros_like(xd.q)
     api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, sel.shape[-1], xd.draft_k,
                          xd.draft_v, st.parents, out, st.ws)
@@ -202,7 +212,12 @@ def test_tc_late_rescale_divergent_rows():
     xd = x.to("cuda")
     st = api.LayerState(wl, xd, kmax=n_sel, build_reps=False)
     plan = api.sv_attend_plan(st.shape, st.kv, n_sel)
-    assert plan.path == api.SV_PATH_TCGEN05 and plan.n_splits == 1
+    assert plan.path == api.SV_PATH_TCGEN05
+    # one CTA walks a whole pair: a split map with one split, or (152 pairs on
+    # 152 SMs) stream-K runs of exactly one pair's 41 units
+    whole_pair = (plan.n_splits == 1 if not plan.streamk else
+                  wl.B * wl.Hkv * (n_sel + 1) == plan.n_splits * plan.blocks_per_split)
+    assert whole_pair, (plan.streamk, plan.n_splits, plan.blocks_per_split)
     out = torch.zeros_like(xd.q)
     api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, sel.shape[-1], xd.draft_k,
                          xd.draft_v, None, out, st.ws)
