@@ -391,28 +391,26 @@ def run_gpu(args, wl, rank, world, dist):
     tokens = sum_over_ranks(dist, wl.B * wl.T * args.steps)
     value = tokens / (ms_total / 1e3)
 
-    # roofline: the attention launches alone, replayed from one CUDA graph per
-    # input set (so host launch overhead cannot leak into the device time),
-    # rotating over the sets (cold L2), CUDA events on the launching stream
-    att_graphs = []
-    for ss in sets:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for st in ss.layers:
+    # roofline: the attention launches alone, back to back as in a layer
+    # stack: one CUDA graph of kRoofLaunches launches rotating over the input
+    # sets (cold L2), replayed; CUDA events on the launching stream
+    kRoofLaunches = 20
+    att_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(att_graph):
+        for i in range(kRoofLaunches):
+            for st in sets[i % n_sets].layers:
                 api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
                                      st.x.draft_v, st.parents, st.out, st.ws)
-        att_graphs.append(g)
-    n_rep = max(n_sets * 3, min(args.steps, 1000))
-    for i in range(n_sets):
-        att_graphs[i].replay()
+    n_rep = max(3, min(args.steps // kRoofLaunches, 100))
+    att_graph.replay()
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record()
     for i in range(n_rep):
-        att_graphs[i % n_sets].replay()
+        att_graph.replay()
     a1.record()
     torch.cuda.synchronize()
-    attend_ms = a0.elapsed_time(a1) / (n_rep * wl.layers)
+    attend_ms = a0.elapsed_time(a1) / (n_rep * kRoofLaunches * wl.layers)
     check_status(sets, "attention-only replays")
     log(f"attention launches: {attend_ms * 1e3:.1f} us")
     peak, peak_kind = read_peaks()
