@@ -220,6 +220,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp == PRODUCER) {
+    // warm L2 with this CTA's block-table rows while earlier kernels finish
+    // (a prefetch only: the lookups below still read after the wait)
+    for (int j = 0; j < sp.n; ++j) {
+      const int32_t* row = a.block_table + (size_t)(sp.pair[j] / a.Hkv) * a.nb_max;
+      for (int e = 32 * lane; e < a.nb; e += 32 * 32) prefetch_l2(row + e);
+    }
+  }
   pdl_wait();     // everything below may read what earlier kernels wrote
   pdl_trigger();  // let the next kernel launch and run its prologue
 
@@ -363,15 +371,11 @@ __global__ void __launch_bounds__(32 * 10, 1)
         mbar_wait_drain(smem_u32(&full[t % NS]), (t / NS) & 1);
     // The mid-stream segment's arrival, counted here while the CTA finishes
     // its last tiles: the softmax warps' mbarrier arrivals order their
-    // partial stores before this thread's device-scope fence.
+    // partial stores before this thread's device-scope release.
     if (lane == 0 && sp.n > 1) {
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      __threadfence();
-      if (atomicAdd(&a.counters[sp.pair[0]], 1u) == (unsigned)sp.nseg[0] - 1u) {
-        __threadfence();
-        merge_flag[0] = 1;
-      }
+      if (arrive_acq_rel(&a.counters[sp.pair[0]]) == (unsigned)sp.nseg[0] - 1u) merge_flag[0] = 1;
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -657,18 +661,13 @@ __global__ void __launch_bounds__(32 * 10, 1)
       }
       *reinterpret_cast<float4*>(a.part_o + (slot + rr) * TD + c4) = v;
     }
-    // CTA barrier, then one thread's device-scope fence publishes every
-    // thread's partial writes before the final segment's arrival (the
-    // barrier orders them before the fence); the last arrival for a pair
-    // fences again before the merge reads. (A mid-stream segment arrived
-    // from the producer warp.)
+    // CTA barrier, then one thread's acquire-release arrival publishes every
+    // thread's partial writes (the barrier orders them before it); the last
+    // arrival for a pair also acquires the others' partials for the merge.
+    // (A mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0) {
-      __threadfence();
-      if (atomicAdd(&a.counters[pair], 1u) == (unsigned)sp.nseg[jf] - 1u) {
-        __threadfence();
-        merge_flag[jf] = 1;
-      }
+      if (arrive_acq_rel(&a.counters[pair]) == (unsigned)sp.nseg[jf] - 1u) merge_flag[jf] = 1;
     }
   }
   __syncthreads();

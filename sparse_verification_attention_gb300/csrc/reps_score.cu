@@ -192,15 +192,13 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   }
 
   // Fused selection: the last CTA to finish scoring this (b, h) selects. The
-  // barrier orders every thread's score stores before thread 0's device-scope
-  // fence and arrival; the last arrival fences again before reading.
+  // barrier orders every thread's score stores before thread 0's
+  // acquire-release arrival; the last arrival thereby sees every score.
   __shared__ unsigned s_last;
   __shared__ TopkSmem<kScoreThreads> tsm;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const bool last = atomicAdd(&a.counters[pair], 1u) == gridDim.x - 1;
-    if (last) __threadfence();
+    const bool last = arrive_acq_rel(&a.counters[pair]) == gridDim.x - 1;
     s_last = last;
   }
   __syncthreads();
