@@ -34,11 +34,11 @@
 //     grows by more than 2^8, decided per warp so that the warp-collective
 //     TMEM loads/stores are taken by all lanes) and sum.
 //   * partials: a segment that ends mid-stream writes each set's unnormalised
-//     (o, m, l) rows from registers; the final segment folds the two sets in
-//     shared memory first. At the end of the CTA every segment counts one
-//     atomic arrival in the workspace; the CTA that arrives last for a pair
-//     merges all of its partials with log-sum-exp weights, writes the output
-//     and resets the count.
+//     (o, m, l) rows from registers (the producer warp counts its arrival);
+//     the final segment folds the two sets in shared memory first and counts
+//     its arrival at the end of the CTA. Each CTA then waits until its pairs'
+//     segments have all arrived and merges its share of their rows with
+//     log-sum-exp weights, writing the output.
 // Rows past R are padding: zero query rows whose outputs are never read.
 #include <atomic>
 
@@ -169,12 +169,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
   uint64_t* mma_done = o_done + 2; // drain: every issued MMA has completed
   uint64_t* q_ready = mma_done + 1; // Q landed (TMA) and padding rows zeroed
   uint64_t* q1_ready = q_ready + 1; // second segment's Q written into TMEM
-  uint64_t* mrg_bar = q1_ready + 1; // a merge's partials landed in the ring
-  uint64_t* mid_done = mrg_bar + 1; // the mid-stream segment's partials are written
+  uint64_t* mid_done = q1_ready + 1; // the mid-stream segment's partials are written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mid_done + 1);
   int* stage_info = reinterpret_cast<int*>(tmem_slot + 1);  // bit0 valid, bit1 draft tile
   volatile int* abort_flag = stage_info + NS;
-  volatile int* merge_flag = abort_flag + 1;  // [kMaxSeg]: this CTA merges that pair
   // ancestor masks of the drafts, copied out of the parameter space with
   // warp-uniform indices (per-lane indices into it would serialize)
   __shared__ unsigned long long s_anc[kMaxT];
@@ -198,10 +196,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
     mbar_init(smem_u32(mma_done), 1);
     mbar_init(smem_u32(q_ready), 5);  // producer's expect_tx + 4 zeroing warps
     mbar_init(smem_u32(q1_ready), 4);
-    mbar_init(smem_u32(mrg_bar), 1);
     mbar_init(smem_u32(mid_done), 2 * NSW);
     *abort_flag = 0;
-    for (int j = 0; j < kMaxSeg; ++j) merge_flag[j] = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -375,7 +371,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
     if (lane == 0 && sp.n > 1) {
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      if (arrive_acq_rel(&a.counters[sp.pair[0]]) == (unsigned)sp.nseg[0] - 1u) merge_flag[0] = 1;
+      arrive_release(&a.counters[sp.pair[0]], 1u);
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -661,95 +657,53 @@ __global__ void __launch_bounds__(32 * 10, 1)
       }
       *reinterpret_cast<float4*>(a.part_o + (slot + rr) * TD + c4) = v;
     }
-    // CTA barrier, then one thread's acquire-release arrival publishes every
-    // thread's partial writes (the barrier orders them before it); the last
-    // arrival for a pair also acquires the others' partials for the merge.
-    // (A mid-stream segment arrived from the producer warp.)
+    // CTA barrier, then one thread's release arrival publishes every
+    // thread's partial writes (the barrier orders them before it). (A
+    // mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0) {
-      if (arrive_acq_rel(&a.counters[pair]) == (unsigned)sp.nseg[jf] - 1u) merge_flag[jf] = 1;
+      arrive_release(&a.counters[pair], 1u);
     }
   }
   __syncthreads();
 
   // ------------------------------------------------------- merge of a pair
-  // The CTA that arrived last for a pair combines all of its partials:
+  // Every CTA merges its share of the rows of each pair it worked on, once
+  // all of the pair's segments have arrived:
   //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s.
-  // When they fit in the (now idle) ring, the partials arrive by bulk copies
-  // in one round trip and are combined from shared memory; otherwise each
-  // thread loads its items' partials from global memory, kMaxMergeSplits at
-  // a time.
-  int mrg_uses = 0;
+  // The pair's count word holds the arrivals (low 16 bits) and the finished
+  // row shares (high bits); whoever finishes the last share resets it. All
+  // of a CTA's arrivals come before any of its waits, and an arrival depends
+  // only on that CTA's own stream, so the waits end; they are bounded too.
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
   for (int j = 0; j < sp.n; ++j) {
-    if (!merge_flag[j]) continue;
     const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
-    const int ns = sp.nseg[j] + sp.mid[j];
+    const int nseg = sp.nseg[j];
+    const int ns = nseg + sp.mid[j];
+    const int share = ((a.R + nseg - 1) / nseg + 1) & ~1;
+    const int r0 = min(a.R, sp.slot[j] * share), r1 = min(a.R, r0 + share);
     const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    const int nitems = a.R * (TD / 4);
-    auto store = [&](int idx, float inv, float4 acc) {
-      const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-      const int t = rr / a.G, gq = rr % a.G;
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
-    };
-    const uint32_t ob = (uint32_t)a.rpad * TD * 4, mb = (uint32_t)a.rpad * 8;
-    // partials, their (m, l), then per-(partial, row) weights and per-row 1/L
-    const size_t need = (size_t)ns * (ob + mb) + ((size_t)ns + 1) * a.rpad * 4;
-    if (need <= (size_t)C::kRing) {
-      float* so = reinterpret_cast<float*>(ring);           // [ns][rpad][TD]
-      float* sml = so + (size_t)ns * a.rpad * TD;            // [ns][rpad][2]
-      float* sw = sml + (size_t)ns * a.rpad * 2;             // [ns][rpad]
-      float* sli = sw + (size_t)ns * a.rpad;                 // [rpad]
-      if (threadIdx.x == 0) {
-        fence_proxy_async_shared();  // earlier generic use of the ring
-        fence_proxy_async_global();  // the partial stores this CTA has acquired
-        const uint32_t bar = smem_u32(mrg_bar);
-        mbar_arrive_expect_tx(bar, (uint32_t)ns * (ob + mb));
-        for (int s = 0; s < ns; ++s) {
-          const size_t row = pbase + (size_t)s * a.rpad;
-          bulk_load(smem_u32(so + (size_t)s * a.rpad * TD), a.part_o + row * TD, ob, bar);
-          bulk_load(smem_u32(sml + (size_t)s * a.rpad * 2), a.part_ml + row * 2, mb, bar);
+    unsigned* ctr = &a.counters[pair];
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while ((load_acquire(ctr) & 0xFFFFu) < (unsigned)nseg) {
+        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+          atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+          break;
         }
+        __nanosleep(64);
       }
-      const bool got = mbar_wait_drain(smem_u32(mrg_bar), mrg_uses & 1);
-      ++mrg_uses;
-      if (got) {
-        // the weights depend on (partial, row) only: computed once per row
-        for (int rr = threadIdx.x; rr < a.R; rr += NT) {
-          float M = -INFINITY;
-          for (int s = 0; s < ns; ++s) M = fmaxf(M, sml[((size_t)s * a.rpad + rr) * 2]);
-          float Lsum = 0.f;
-          for (int s = 0; s < ns; ++s) {
-            const float2 ml = *reinterpret_cast<const float2*>(sml + ((size_t)s * a.rpad + rr) * 2);
-            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-            sw[(size_t)s * a.rpad + rr] = w;
-            Lsum += w * ml.y;
-          }
-          sli[rr] = 1.0f / Lsum;
-        }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < nitems; idx += NT) {
-          const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s = 0; s < ns; ++s) {
-            const float w = sw[(size_t)s * a.rpad + rr];
-            const float4 o = *reinterpret_cast<const float4*>(so + ((size_t)s * a.rpad + rr) * TD + c);
-            acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-          }
-          store(idx, sli[rr], acc);
-        }
-      } else if (threadIdx.x == 0) {
-        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      }
-      __syncthreads();  // the ring is read before a second merge refills it
-    } else {
-      auto load = [&](int idx, int s0, float2 (&ml)[kMaxMergeSplits], float4 (&o)[kMaxMergeSplits]) {
-        const int rr = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+    }
+    __syncthreads();  // thread 0's acquire covers the whole CTA's reads below
+    const int nitems = (r1 - r0) * (TD / 4);
+    for (int idx = threadIdx.x; idx < nitems; idx += NT) {
+      const int rr = r0 + idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+      float M = -INFINITY, Lsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
+        // kMaxMergeSplits partials' loads in flight together
+        float2 ml[kMaxMergeSplits];
+        float4 o[kMaxMergeSplits];
 #pragma unroll
         for (int q = 0; q < kMaxMergeSplits; ++q) {
           ml[q] = make_float2(-INFINITY, 0.f);
@@ -760,34 +714,36 @@ __global__ void __launch_bounds__(32 * 10, 1)
             o[q] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
           }
         }
-      };
-      for (int idx = threadIdx.x; idx < nitems; idx += NT) {
-        float M = -INFINITY, Lsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
-          float2 ml[kMaxMergeSplits];
-          float4 o[kMaxMergeSplits];
-          load(idx, s0, ml, o);
-          float Mc = M;
+        float Mc = M;
 #pragma unroll
-          for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
-          if (Mc > M) {
-            const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
-            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-            Lsum *= sc;
-            M = Mc;
-          }
-#pragma unroll
-          for (int q = 0; q < kMaxMergeSplits; ++q) {
-            const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
-            Lsum += w * ml[q].y;
-            acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
-          }
+        for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
+        if (Mc > M) {
+          const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
+          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+          Lsum *= sc;
+          M = Mc;
         }
-        store(idx, 1.0f / Lsum, acc);
+#pragma unroll
+        for (int q = 0; q < kMaxMergeSplits; ++q) {
+          const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
+          Lsum += w * ml[q].y;
+          acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
+        }
       }
+      const float inv = 1.0f / Lsum;
+      const int t = rr / a.G, gq = rr % a.G;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
     }
-    if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
+    if (threadIdx.x == 0) {
+      // every CTA of the pair has seen all arrivals before counting its
+      // share, so the last share may clear the word for the next call
+      if ((atomicAdd(ctr, 1u << 16) >> 16) == (unsigned)nseg - 1u) *ctr = 0u;
+    }
   }
 }
 

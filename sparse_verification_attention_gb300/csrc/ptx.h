@@ -98,24 +98,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// Untiled bulk copy global -> shared: both addresses 16-byte aligned, size a
-// multiple of 16; completion (bytes) on an mbarrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Order this thread's generic-proxy accesses before later async-proxy (bulk
-// copy) accesses of shared / global memory.
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Arrival count with acquire-release semantics at device scope: every store
 // that happens before it (including other threads' stores ordered by a CTA
 // barrier) is visible before the count moves, and the thread that sees the
@@ -124,6 +106,20 @@ __device__ __forceinline__ unsigned arrive_acq_rel(unsigned* ctr) {
   unsigned old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
   return old;
+}
+
+// Arrival count with release semantics at device scope: every store that
+// happens before it (including other threads' stores ordered by a CTA
+// barrier) is visible before the count moves.
+__device__ __forceinline__ void arrive_release(unsigned* ctr, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+// Load with acquire semantics at device scope.
+__device__ __forceinline__ unsigned load_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Hint: bring the 128-byte line holding p into L2.
