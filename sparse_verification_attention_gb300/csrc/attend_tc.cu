@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mid_done + 1);
   int* stage_info = reinterpret_cast<int*>(tmem_slot + 1);  // bit0 valid, bit1 draft tile
   volatile int* abort_flag = stage_info + NS;
+  volatile int* pair_done = abort_flag + 1;  // [kMaxSeg]: this CTA saw the pair complete
   // ancestor masks of the drafts, copied out of the parameter space with
   // warp-uniform indices (per-lane indices into it would serialize)
   __shared__ unsigned long long s_anc[kMaxT];
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
     mbar_init(smem_u32(q1_ready), 4);
     mbar_init(smem_u32(mid_done), 2 * NSW);
     *abort_flag = 0;
+    for (int j = 0; j < kMaxSeg; ++j) pair_done[j] = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -371,7 +373,9 @@ __global__ void __launch_bounds__(32 * 10, 1)
     if (lane == 0 && sp.n > 1) {
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      arrive_release(&a.counters[sp.pair[0]], 1u);
+      // the last arrival sees the pair complete (and acquires its partials)
+      if ((arrive_acq_rel(&a.counters[sp.pair[0]]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0])
+        pair_done[0] = 1;
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -657,12 +661,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
       }
       *reinterpret_cast<float4*>(a.part_o + (slot + rr) * TD + c4) = v;
     }
-    // CTA barrier, then one thread's release arrival publishes every
-    // thread's partial writes (the barrier orders them before it). (A
+    // CTA barrier, then one thread's acquire-release arrival publishes
+    // every thread's partial writes (the barrier orders them before it); the
+    // arrival that completes a pair also acquires the other partials. (A
     // mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0) {
-      arrive_release(&a.counters[pair], 1u);
+      if ((arrive_acq_rel(&a.counters[pair]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf])
+        pair_done[jf] = 1;
     }
   }
   __syncthreads();
@@ -676,73 +682,86 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // of a CTA's arrivals come before any of its waits, and an arrival depends
   // only on that CTA's own stream, so the waits end; they are bounded too.
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  for (int j = 0; j < sp.n; ++j) {
-    const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
-    const int nseg = sp.nseg[j];
-    const int ns = nseg + sp.mid[j];
-    const int share = ((a.R + nseg - 1) / nseg + 1) & ~1;
-    const int r0 = min(a.R, sp.slot[j] * share), r1 = min(a.R, r0 + share);
-    const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    unsigned* ctr = &a.counters[pair];
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while ((load_acquire(ctr) & 0xFFFFu) < (unsigned)nseg) {
+  // this CTA's slice [r0, r1) of the rows of each of its pairs
+  int r0[kMaxSeg], r1[kMaxSeg], nitem[kMaxSeg];
+  for (int j = 0; j < kMaxSeg; ++j) {
+    r0[j] = r1[j] = nitem[j] = 0;
+    if (j < sp.n) {
+      const int share = ((a.R + sp.nseg[j] - 1) / sp.nseg[j] + 1) & ~1;
+      r0[j] = min(a.R, sp.slot[j] * share);
+      r1[j] = min(a.R, r0[j] + share);
+      nitem[j] = (r1[j] - r0[j]) * (TD / 4);
+    }
+  }
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (int j = 0; j < sp.n; ++j) {
+      if (pair_done[j]) continue;  // this CTA's own arrival completed it
+      while ((load_acquire(&a.counters[sp.pair[j]]) & 0xFFFFu) < (unsigned)sp.nseg[j]) {
         if (globaltimer_ns() - t0 > kWaitBudgetNs) {
           atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
           break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
       }
     }
-    __syncthreads();  // thread 0's acquire covers the whole CTA's reads below
-    const int nitems = (r1 - r0) * (TD / 4);
-    for (int idx = threadIdx.x; idx < nitems; idx += NT) {
-      const int rr = r0 + idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-      float M = -INFINITY, Lsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
-        // kMaxMergeSplits partials' loads in flight together
-        float2 ml[kMaxMergeSplits];
-        float4 o[kMaxMergeSplits];
+  }
+  __syncthreads();  // thread 0's acquires cover the whole CTA's reads below
+  // the slices of both pairs in one pass, so all of their loads overlap
+  for (int idx = threadIdx.x; idx < nitem[0] + nitem[1]; idx += NT) {
+    const int j = idx < nitem[0] ? 0 : 1;
+    const int k = idx - (j ? nitem[0] : 0);
+    const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+    const int ns = sp.nseg[j] + sp.mid[j];
+    const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
+    const int rr = r0[j] + k / (TD / 4), c = (k % (TD / 4)) * 4;
+    float M = -INFINITY, Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
+      // kMaxMergeSplits partials' loads in flight together
+      float2 ml[kMaxMergeSplits];
+      float4 o[kMaxMergeSplits];
 #pragma unroll
-        for (int q = 0; q < kMaxMergeSplits; ++q) {
-          ml[q] = make_float2(-INFINITY, 0.f);
-          o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (s0 + q < ns) {
-            const size_t row = pbase + (size_t)(s0 + q) * a.rpad + rr;
-            ml[q] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
-            o[q] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
-          }
-        }
-        float Mc = M;
-#pragma unroll
-        for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
-        if (Mc > M) {
-          const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
-          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-          Lsum *= sc;
-          M = Mc;
-        }
-#pragma unroll
-        for (int q = 0; q < kMaxMergeSplits; ++q) {
-          const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
-          Lsum += w * ml[q].y;
-          acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
+      for (int q = 0; q < kMaxMergeSplits; ++q) {
+        ml[q] = make_float2(-INFINITY, 0.f);
+        o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + q < ns) {
+          const size_t row = pbase + (size_t)(s0 + q) * a.rpad + rr;
+          ml[q] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
+          o[q] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
         }
       }
-      const float inv = 1.0f / Lsum;
-      const int t = rr / a.G, gq = rr % a.G;
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
+      float Mc = M;
+#pragma unroll
+      for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
+      if (Mc > M) {
+        const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        Lsum *= sc;
+        M = Mc;
+      }
+#pragma unroll
+      for (int q = 0; q < kMaxMergeSplits; ++q) {
+        const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
+        Lsum += w * ml[q].y;
+        acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
+      }
     }
-    if (threadIdx.x == 0) {
-      // every CTA of the pair has seen all arrivals before counting its
-      // share, so the last share may clear the word for the next call
-      if ((atomicAdd(ctr, 1u << 16) >> 16) == (unsigned)nseg - 1u) *ctr = 0u;
+    const float inv = 1.0f / Lsum;
+    const int t = rr / a.G, gq = rr % a.G;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
+  }
+  if (threadIdx.x == 0) {
+    // every CTA of a pair has seen all arrivals before counting its slice,
+    // so the last slice may clear the word for the next call
+    for (int j = 0; j < sp.n; ++j) {
+      unsigned* ctr = &a.counters[sp.pair[j]];
+      if ((atomicAdd(ctr, 1u << 16) >> 16) == (unsigned)sp.nseg[j] - 1u) *ctr = 0u;
     }
   }
 }

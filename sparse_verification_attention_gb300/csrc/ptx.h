@@ -108,13 +108,6 @@ __device__ __forceinline__ unsigned arrive_acq_rel(unsigned* ctr) {
   return old;
 }
 
-// Arrival count with release semantics at device scope: every store that
-// happens before it (including other threads' stores ordered by a CTA
-// barrier) is visible before the count moves.
-__device__ __forceinline__ void arrive_release(unsigned* ctr, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
-}
-
 // Load with acquire semantics at device scope.
 __device__ __forceinline__ unsigned load_acquire(const unsigned* p) {
   unsigned v;
