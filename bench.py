@@ -61,13 +61,17 @@ def attend_bytes(wl: W.Workload, k: int) -> int:
 
 
 def layer_bytes(wl: W.Workload, k: int, computing: bool) -> int:
-    """Algorithmic bytes of one layer of the step: incremental rep build of
-    one block per sequence (read its keys, write its fp32 rep), the fp32
-    representative stream when the layer computes its selection, and the
-    attention launch."""
-    inc = wl.B * wl.Hkv * (wl.blk * wl.d * wl.elt + wl.d * 4)
+    """Algorithmic bytes of one layer of the step (one verification layer:
+    the fp32 representative stream when the layer computes its selection,
+    and the attention launch). Representatives are built at prefill and
+    updated when a block fills, outside the step (timed separately)."""
     reps = wl.B * wl.Hkv * wl.NB * wl.d * 4 if computing else 0
-    return inc + reps + attend_bytes(wl, k)
+    return reps + attend_bytes(wl, k)
+
+
+def rep_update_bytes(wl: W.Workload) -> int:
+    """One block's rep per (sequence, kv head): read its keys, write its rep."""
+    return wl.B * wl.Hkv * (wl.blk * wl.d * wl.elt + wl.d * 4)
 
 
 def step_bytes(wl: W.Workload, k: int) -> int:
@@ -314,13 +318,11 @@ class StepSet:
 
 
 def run_step(wl, ss: StepSet, ev=None):
-    """Launch one step on the current stream (graph-capturable)."""
+    """Launch one step on the current stream (graph-capturable): per layer,
+    score + select on computing layers, then the sparse attention."""
     from sparse_verification_attention_gb300 import api
-    nb = wl.NB
     for l, st in enumerate(ss.layers):
         computing = l % wl.compute_every == 0
-        if nb:
-            api.sv_build_reps(st.shape, st.kv, nb - 1, 1, st.reps)
         if computing:
             api.sv_score_select(st.shape, st.x.q, st.reps, st.kv, wl.budget, st.sel, st.kmax,
                                 st.ws)
@@ -437,6 +439,28 @@ def run_gpu(args, wl, rank, world, dist):
         dense = {"attend_ms": dms, "gbs": dbytes / (dms / 1e3) / 1e9,
                  "sparse_speedup": dms / attend_ms, "note": "same kernels, all blocks kept"}
 
+    # the incremental rep update (one newly filled block per (b, h)), outside
+    # the step: a block fills every blk / T steps
+    rep_update = None
+    if wl.NB:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(kRoofLaunches):
+                st = sets[i % n_sets].layers[0]
+                api.sv_build_reps(st.shape, st.kv, wl.NB - 1, 1, st.reps)
+        g.replay()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record()
+        for i in range(n_rep):
+            g.replay()
+        r1.record()
+        torch.cuda.synchronize()
+        rus = r0.elapsed_time(r1) / (n_rep * kRoofLaunches) * 1e3
+        rep_update = {"us_per_layer": rus, "bytes_per_layer": rep_update_bytes(wl),
+                      "every_steps": wl.blk / max(1, wl.T),
+                      "note": "sv_build_reps of one newly filled block per (b, h); not in the step"}
+
     # e2e: the public call with host buffers, copies inside the timed region
     e2e = run_e2e(args, wl, sets, dist)
     check_status(sets, "e2e")
@@ -451,13 +475,12 @@ def run_gpu(args, wl, rank, world, dist):
                "cores": torch.get_num_threads(), "kind": "oracle", "sample": o.describe(n, el)}
 
     traffic = traffic_from_profile(wl.name)
-    # kernels per layer: the incremental rep build, the fused score+select on
-    # computing layers, the attention (plus a merge kernel on paths that do
-    # not merge in-kernel)
+    # kernels per layer: the fused score+select on computing layers, the
+    # attention (plus a merge kernel on paths that do not merge in-kernel)
     plan = api.sv_attend_plan(st0.shape, st0.kv, k)
     att_launches = 1 if (plan.path == api.SV_PATH_TCGEN05 or plan.cluster > 0) else 2
-    launches_per_step = sum((1 if wl.NB else 0) + (1 if l % wl.compute_every == 0 else 0)
-                            + att_launches for l in range(wl.layers))
+    launches_per_step = sum((1 if l % wl.compute_every == 0 else 0) + att_launches
+                            for l in range(wl.layers))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -478,6 +501,7 @@ def run_gpu(args, wl, rank, world, dist):
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
                      "frac_of_nominal_8tbs": achieved / 8000.0},
         "dense": dense,
+        "rep_update": rep_update,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": launches_per_step * args.steps,
@@ -488,7 +512,7 @@ def run_gpu(args, wl, rank, world, dist):
 
 
 def run_e2e(args, wl, sets, dist):
-    """sv_build_reps + sv_verify_layer per layer through the public call, with
+    """sv_verify_layer per layer through the public call, with
     each step's per-token inputs (Q, draft K, draft V) copied in from pinned
     host memory and the output copied back, inside the timed region. Steps
     rotate over the same input sets as the device-timed loop."""
@@ -510,8 +534,6 @@ def run_e2e(args, wl, sets, dist):
             st.x.q.copy_(hq, non_blocking=True)
             st.x.draft_k.copy_(hk, non_blocking=True)
             st.x.draft_v.copy_(hv, non_blocking=True)
-            if nb:
-                api.sv_build_reps(st.shape, st.kv, nb - 1, 1, st.reps)
             reuse = int(l % wl.compute_every != 0)
             api.sv_verify_layer(st.shape, st.x.q, st.kv, st.reps, wl.budget, st.x.draft_k,
                                 st.x.draft_v, st.parents, reuse, st.sel, st.kmax, st.out, st.ws)
@@ -532,7 +554,7 @@ def run_e2e(args, wl, sets, dist):
     tokens = sum_over_ranks(dist, wl.B * wl.T * steps)
     return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
-            "note": "eager public calls (sv_build_reps + sv_verify_layer), rotating input sets"}
+            "note": "eager public calls (sv_verify_layer per layer), rotating input sets"}
 
 
 def main():
