@@ -33,6 +33,10 @@ Readings where the pages are silent (every one is listed in the design doc):
   R6 softmax scale 1/sqrt(d); Q and K are post-positional-encoding inputs.
   R7 reuse: a reuse layer takes the selection of the previous computing layer
      unchanged and does no scoring or selection of its own.
+  R8 a context that ends in a partial block: only the ctx // blk full blocks
+     get representatives and compete for the budget; the partial block's
+     ctx % blk tokens are always attended, outside the budget. Accepted drafts
+     are appended at positions ctx, ctx+1, ... in the order accepted.
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
 against closed forms, brute force, invariants or torch SDPA, except R1's
@@ -172,13 +176,17 @@ def _softmax_weighted_sum(scores: torch.Tensor, values: torch.Tensor) -> torch.T
 
 
 def sparse_attend(q, k_pool, v_pool, block_table, sel, draft_k, draft_v,
-                  parents: Sequence[int]) -> torch.Tensor:
+                  parents: Sequence[int], tail_block: int = 0,
+                  tail_len: int = 0) -> torch.Tensor:
     """Attention of every draft row over the ONE shared block set plus the
     drafts it may see.
 
     q [B,T,Hq,d]; pools [P,Hkv,blk,d]; block_table [B,>=NB]; sel [B,Hkv,k]
     (logical block indices; the same set for all T drafts and all G query
-    heads of a KV head); draft_k/v [B,T,Hkv,d]. Returns fp64 [B,T,Hq,d].
+    heads of a KV head); draft_k/v [B,T,Hkv,d]. With tail_len > 0 the first
+    tail_len tokens of logical block tail_block (the partial last block of
+    the context) are attended as well, outside the selection (reading R8).
+    Returns fp64 [B,T,Hq,d].
     """
     B, T, Hq, d = q.shape
     Hkv = k_pool.shape[1]
@@ -188,12 +196,14 @@ def sparse_attend(q, k_pool, v_pool, block_table, sel, draft_k, draft_v,
     for b in range(B):
         for h in range(Hkv):
             pages = [int(block_table[b, int(j)]) for j in sel[b, h].tolist()]
-            if pages:
-                Kp = torch.cat([k_pool[p, h].to(F64) for p in pages])   # [k*blk, d]
-                Vp = torch.cat([v_pool[p, h].to(F64) for p in pages])
-            else:
-                Kp = torch.zeros(0, d, dtype=F64)
-                Vp = torch.zeros(0, d, dtype=F64)
+            Ks = [k_pool[p, h].to(F64) for p in pages]
+            Vs = [v_pool[p, h].to(F64) for p in pages]
+            if tail_len > 0:
+                tp = int(block_table[b, tail_block])
+                Ks.append(k_pool[tp, h, :tail_len].to(F64))
+                Vs.append(v_pool[tp, h, :tail_len].to(F64))
+            Kp = torch.cat(Ks) if Ks else torch.zeros(0, d, dtype=F64)   # [k*blk (+tail), d]
+            Vp = torch.cat(Vs) if Vs else torch.zeros(0, d, dtype=F64)
             for t in range(T):
                 vis = ancestors(parents, t)
                 Kt = torch.cat([Kp, draft_k[b, vis, h].to(F64)])
@@ -237,6 +247,14 @@ def dense_verify_attention(q, k_ctx, v_ctx, draft_k, draft_v,
     return out
 
 
+def logical_kv_tokens(pool: torch.Tensor, block_table: torch.Tensor, ctx: int) -> torch.Tensor:
+    """The first ctx tokens of every sequence in logical order [B, ctx, Hkv, d]
+    (the last block may be partial)."""
+    blk = pool.shape[2]
+    nblk = (ctx + blk - 1) // blk
+    return logical_kv(pool, block_table, nblk)[:, :ctx]
+
+
 def logical_kv(pool: torch.Tensor, block_table: torch.Tensor, n_blocks: int) -> torch.Tensor:
     """Gather a paged pool [P,Hkv,blk,d] into logical order [B, n_blocks*blk, Hkv, d]."""
     B = block_table.shape[0]
@@ -260,7 +278,8 @@ def verify_layer(q, k_pool, v_pool, block_table, draft_k, draft_v, parents,
     or selection (inter-layer retrieval reuse). Returns (out, sel, scores);
     scores is None on a reuse layer.
     """
-    NB = ctx // blk
+    NB = ctx // blk              # full blocks: the candidates for selection
+    tail = ctx - NB * blk        # tokens of a partial last block, always attended
     G = q.shape[2] // k_pool.shape[1]
     if reuse_sel is not None:
         sel, scores = reuse_sel, None
@@ -270,7 +289,8 @@ def verify_layer(q, k_pool, v_pool, block_table, draft_k, draft_v, parents,
         scores = block_scores(q, reps, G)
         k = budget_from(budget, ctx, NB)
         sel = select_all(scores, k)
-    out = sparse_attend(q, k_pool, v_pool, block_table, sel, draft_k, draft_v, parents)
+    out = sparse_attend(q, k_pool, v_pool, block_table, sel, draft_k, draft_v, parents,
+                        tail_block=NB, tail_len=tail)
     return out, sel, scores
 
 
@@ -287,3 +307,30 @@ def verify_stack(layers, parents, ctx: int, blk: int, budget, compute_every: int
         outs.append(out)
         sels.append(sel)
     return outs, sels
+
+
+# --------------------------------------------------------------------------
+# Acceptance write-back: the step after verification (not on the pages)
+# --------------------------------------------------------------------------
+def append_accepted(k_pool, v_pool, block_table, ctx: Sequence[int], n_accept: Sequence[int],
+                    accept_idx, draft_k, draft_v):
+    """Append the accepted drafts' K/V to each sequence's paged cache.
+
+    Sequence b accepted the drafts accept_idx[b][0:n_accept[b]] (draft indices
+    along the accepted path, in order); their K/V rows go to logical positions
+    ctx[b], ctx[b]+1, ... (page block_table[b, pos // blk], slot pos % blk).
+    Returns updated copies of the pools and, per sequence, the logical blocks
+    that became full (reps to rebuild).
+    """
+    k_new, v_new = k_pool.clone(), v_pool.clone()
+    blk = k_pool.shape[2]
+    filled = []
+    for b in range(len(ctx)):
+        for i in range(n_accept[b]):
+            pos = ctx[b] + i
+            page = int(block_table[b, pos // blk])
+            k_new[page, :, pos % blk] = draft_k[b, int(accept_idx[b][i])]
+            v_new[page, :, pos % blk] = draft_v[b, int(accept_idx[b][i])]
+        first, last = ctx[b] // blk, (ctx[b] + n_accept[b]) // blk
+        filled.append(list(range(first, last)))
+    return k_new, v_new, filled

@@ -335,4 +335,81 @@ def pin_reuse(O):
     assert torch.equal(outs[1], ref1)
 
 
+# ------------------------------------------------- partial tail block (R8)
+def _fixed(nblocks):
+    from types import SimpleNamespace
+    return SimpleNamespace(mode=O_FIXED, fixed_blocks=nblocks, short_ctx=0, floor_blocks=0,
+                           frac_mid=0.0, long_ctx=0, frac_long=0.0)
+
+
+O_FIXED = 0
+
+
+def pin_tail_full_budget_equals_dense(O):
+    """A context ending in a partial block: keeping every full block and
+    always attending the partial one is full verification over exactly ctx
+    tokens (dense attention, which knows nothing of blocks)."""
+    for ctx, parents, T in ((4 * 5 + 3, [-1, 0, 1, 2], 4), (4 * 2 + 1, [-1, 0, 0, 1, 1], 5),
+                            (3, [-1, 0], 2)):
+        q, kp, vp, bt, dk, dv, par = small_inputs(T=T, parents=parents, NB=6)
+        blk = kp.shape[2]
+        nfull = ctx // blk
+        out, sel, _ = O.verify_layer(q, kp, vp, bt, dk, dv, parents, ctx, blk, _fixed(nfull))
+        dn = O.dense_verify_attention(q, O.logical_kv_tokens(kp, bt, ctx),
+                                      O.logical_kv_tokens(vp, bt, ctx), dk, dv, parents)
+        assert sel.shape[-1] == nfull
+        assert torch.allclose(out, dn, atol=1e-12), (ctx, (out - dn).abs().max())
+
+
+def pin_tail_outside_budget(O):
+    """The partial block is attended even with a budget of zero blocks:
+    then each row attends to the tail tokens and its visible drafts only."""
+    q, kp, vp, bt, dk, dv, par = small_inputs(T=3, NB=6)
+    blk = kp.shape[2]
+    ctx = 4 * blk + 2
+    out, sel, _ = O.verify_layer(q, kp, vp, bt, dk, dv, par, ctx, blk, _fixed(0))
+    B, T, Hq, d = q.shape
+    Hkv = kp.shape[1]
+    G = Hq // Hkv
+    for b in range(B):
+        page = int(bt[b, 4])
+        for h in range(Hkv):
+            for t in range(T):
+                vis = O.ancestors(par, t)
+                K = torch.cat([kp[page, h, :2], dk[b, vis, h]])
+                V = torch.cat([vp[page, h, :2], dv[b, vis, h]])
+                for g in range(G):
+                    s = (K @ q[b, t, h * G + g]) / math.sqrt(d)
+                    want = torch.softmax(s, 0) @ V
+                    assert torch.allclose(out[b, t, h * G + g], want, atol=1e-12)
+
+
+def pin_append_accepted(O):
+    """Acceptance write-back: the accepted drafts' rows land at positions
+    ctx, ctx+1, ... of their sequence in the order accepted; every other
+    position is unchanged; the blocks reported full are exactly those that
+    the append completed."""
+    q, kp, vp, bt, dk, dv, par = small_inputs(T=5, NB=6)
+    blk = kp.shape[2]
+    ctx = [blk * 2 + 3, blk * 3]
+    n_acc = [3, 5]
+    acc = [[0, 1, 3, -1, -1], [0, 2, 4, 1, 3]]
+    kn, vn, filled = O.append_accepted(kp, vp, bt, ctx, n_acc, acc, dk, dv)
+    for b in range(2):
+        before_k = O.logical_kv_tokens(kp, bt, ctx[b] + n_acc[b])[b]
+        after_k = O.logical_kv_tokens(kn, bt, ctx[b] + n_acc[b])[b]
+        after_v = O.logical_kv_tokens(vn, bt, ctx[b] + n_acc[b])[b]
+        assert torch.equal(after_k[:ctx[b]], before_k[:ctx[b]])
+        for i in range(n_acc[b]):
+            assert torch.equal(after_k[ctx[b] + i], dk[b, acc[b][i]])
+            assert torch.equal(after_v[ctx[b] + i], dv[b, acc[b][i]])
+    # 11 + 3 = 14 tokens fill block 2 (tokens 8..11 and 12..13 do not fill 3)
+    assert filled == [[2], [3]]
+    # pages not touched by the append are bit-identical
+    touched = {int(bt[b, (ctx[b] + i) // blk]) for b in range(2) for i in range(n_acc[b])}
+    for p in range(kp.shape[0]):
+        if p not in touched:
+            assert torch.equal(kn[p], kp[p]) and torch.equal(vn[p], vp[p])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

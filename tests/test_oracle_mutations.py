@@ -75,13 +75,17 @@ def _reps_off_by_one(k_pool, block_table, n_blocks, blk):
     return _orig_reps(k_pool, block_table, n_blocks, blk) * blk / (blk + 1)
 
 
-def _sparse_heads_mod(q, k_pool, v_pool, bt, sel, dk, dv, parents):
+def _sparse_heads_mod(q, k_pool, v_pool, bt, sel, dk, dv, parents, **kw):
     B, T, Hq, d = q.shape
     Hkv = k_pool.shape[1]
     G = Hq // Hkv
     perm = [(qh % Hkv) * G + (qh // Hkv) for qh in range(Hq)]
     inv = [perm.index(i) for i in range(Hq)]
-    return _orig_sparse(q[:, :, inv], k_pool, v_pool, bt, sel, dk, dv, parents)[:, :, perm]
+    return _orig_sparse(q[:, :, inv], k_pool, v_pool, bt, sel, dk, dv, parents, **kw)[:, :, perm]
+
+
+def _sparse_tail_dropped(q, k_pool, v_pool, bt, sel, dk, dv, parents, tail_block=0, tail_len=0):
+    return _orig_sparse(q, k_pool, v_pool, bt, sel, dk, dv, parents)  # forgets the partial block
 
 
 MUTATIONS = {
@@ -97,6 +101,7 @@ MUTATIONS = {
     "budget_floor_division": ("budget_blocks", _budget_floor_division),
     "reps_wrong_divisor": ("block_representatives", _reps_off_by_one),
     "attend_head_mapping": ("sparse_attend", _sparse_heads_mod),
+    "attend_tail_dropped": ("sparse_attend", _sparse_tail_dropped),
 }
 
 
