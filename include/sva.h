@@ -35,7 +35,8 @@
  *   - Nothing throws across the ABI. sv_last_error() describes the last
  *     non-OK status of the calling thread.
  *   - Limits: 1 <= T <= 64; Hq % Hkv == 0; d % 8 == 0 and 8 <= d <= 256;
- *     ctx % blk == 0 (every prefix block is full); NB = ctx/blk <= 16384.
+ *     NB = ctx/blk full blocks <= 16384; a partial last block (ctx % blk
+ *     tokens) is allowed.
  */
 #ifndef SVA_H_
 #define SVA_H_
@@ -93,14 +94,18 @@ typedef struct {
 
 /* Paged KV cache, caller-owned device memory. Page p of head h holds blk
  * consecutive tokens: k_pool[p][h][0..blk)[0..d). Every sequence has ctx
- * prefix tokens in NB = ctx/blk full blocks; logical block j of sequence b
- * lives in page block_table[b * nb_max + j]. Pool base addresses must be
- * 16-byte aligned. */
+ * prefix tokens: NB = ctx/blk full blocks and, when ctx % blk != 0, a
+ * partial last block (logical block NB, its first ctx % blk tokens). Logical
+ * block j of sequence b lives in page block_table[b * nb_max + j]. Only full
+ * blocks have representatives and compete for the budget; a partial last
+ * block is always attended, outside the budget (this library's reading of
+ * the method for the step after drafts are accepted). Pool base addresses
+ * must be 16-byte aligned. */
 typedef struct {
   const void* k_pool;       /* [num_pages, Hkv, blk, d]                    */
   const void* v_pool;       /* [num_pages, Hkv, blk, d]                    */
   const int32_t* block_table; /* [B, nb_max]                              */
-  int nb_max;               /* row stride of block_table, >= NB            */
+  int nb_max;               /* row stride of block_table, >= ceil(ctx/blk) */
   int num_pages;
   int ctx;                  /* prefix tokens per sequence (same for all)   */
 } sv_kv;
@@ -182,6 +187,7 @@ sv_status sv_score_select(const sv_shape* shape, const void* q, const float* rep
  * 0 <= draft_parent[t] < t for t > 0 (a tree); NULL = linear chain.
  * sel == NULL selects all NB blocks in order: dense full verification
  * attention [SpecPV], the comparison baseline (n_sel is then ignored).
+ * A partial last block (ctx % blk tokens) is attended in every case.
  * sel: [B, Hkv, sel_stride] int32 with n_sel <= sel_stride.
  * q: [B, T, Hq, d]; draft_k, draft_v: [B, T, Hkv, d]; out: [B, T, Hq, d].
  * The workspace holds the split-KV partial results (its size from

@@ -263,11 +263,15 @@ class LayerState:
         self.k = sv_budget_blocks(wl.budget, wl.ctx, nb)
         self.kmax = self.k if kmax is None else kmax
         dev = x.q.device
-        self.reps = torch.zeros(wl.B, wl.Hkv, max(nb, 1), wl.d, dtype=torch.float32, device=dev)
+        # [B, Hkv, nb_max, d]: the calls index representatives with the block
+        # table's width as stride (a partial last block gets a row, unused)
+        nb_max = max(x.block_table.shape[1], 1)
+        self.reps = torch.zeros(wl.B, wl.Hkv, nb_max, wl.d, dtype=torch.float32, device=dev)
         self.sel = torch.full((wl.B, wl.Hkv, max(self.kmax, 1)), -1, dtype=torch.int32, device=dev)
         self.out = torch.empty_like(x.q)
         # sized for the budgeted selection and for a dense (all-block) pass
-        self.ws = alloc_workspace(self.shape, max(nb, 1), max(self.kmax, nb, 1), device=dev)
+        # sized for the block table's width (nb_max), as the calls check it
+        self.ws = alloc_workspace(self.shape, nb_max, max(self.kmax, nb, 1), device=dev)
         self.parents = None if wl.parents is None else list(wl.parents)
         if build_reps and nb:
             sv_build_reps(self.shape, self.kv, 0, nb, self.reps, stream)

@@ -73,8 +73,10 @@ struct Consumer {
   int r_lo, r_hi;
   unsigned long long vis_lo, vis_hi;  // visible drafts of rows r_lo, r_hi
 
+  // draft: mask columns by the rows' ancestor bits; limit: columns past it
+  // (a partial last block) are masked
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const AttendArgs& a,
-                                       bool masked, int lane) {
+                                       bool draft, int limit, int lane) {
     const int t4 = lane & 3;
     float s[BLK / 8][4];
 #pragma unroll
@@ -95,18 +97,21 @@ struct Consumer {
       }
     }
 
-    // Scale into the log2 domain, mask (draft tile only), online softmax.
+    // Scale into the log2 domain, mask (draft tile, partial block), online
+    // softmax.
     float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < BLK / 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float v = s[nt][e] * a.scale_log2;
-        if (masked) {
+        const int u = 8 * nt + 2 * t4 + (e & 1);
+        if (draft) {
           // bit u of the row's ancestor mask (zero for padding rows)
-          const int u = 8 * nt + 2 * t4 + (e & 1);
           const unsigned long long vis = (e < 2) ? vis_lo : vis_hi;
           if (!((vis >> u) & 1ull)) v = -INFINITY;
+        } else if (u >= limit) {
+          v = -INFINITY;
         }
         s[nt][e] = v;
       }
@@ -177,12 +182,16 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = b * a.Hkv + h;
-  // Work units of this (b, h): the n_sel selected blocks, then the draft tile.
+  // Work units of this (b, h): the n_sel selected blocks, the partial last
+  // block (unit n_sel, if any), then the draft tile.
+  const int ntail = a.tail > 0 ? 1 : 0;
   const int u0 = split * a.bps;
-  const int u1 = min(a.n_sel + 1, u0 + a.bps);
+  const int u1 = min(a.n_sel + ntail + 1, u0 + a.bps);
   const int j0 = u0;
   const int nblk = max(0, min(u1, a.n_sel) - u0);
-  const bool has_draft = (u0 <= a.n_sel && a.n_sel < u1);
+  const bool has_tail = ntail && u0 <= a.n_sel && a.n_sel < u1;
+  const bool has_draft = (u0 <= a.n_sel + ntail && a.n_sel + ntail < u1);
+  const int nring = nblk + (has_tail ? 1 : 0);  // tiles through the ring
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -207,12 +216,15 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
     const int oob_row = a.num_pages * a.Hkv * BLK;  // past the end: TMA zero-fills
     int issued = 0;
     bool stop = false;
-    for (int base = 0; base < nblk && !stop; base += 32) {
+    for (int base = 0; base < nring && !stop; base += 32) {
       int row = oob_row, ok = 0;
-      if (base + lane < nblk) {
-        const int j = a.sel ? a.sel[(size_t)pair * a.sel_stride + j0 + base + lane]
-                            : j0 + base + lane;
-        if (j < 0 || j >= a.nb) {
+      if (base + lane < nring) {
+        // the partial last block rides after the selected ones (stage_ok 2)
+        const bool tailu = base + lane == nblk;
+        const int j = tailu ? a.nb
+                            : a.sel ? a.sel[(size_t)pair * a.sel_stride + j0 + base + lane]
+                                    : j0 + base + lane;
+        if (!tailu && (j < 0 || j >= a.nb)) {
           atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
         } else {
           const int page = a.block_table[(size_t)b * a.nb_max + j];
@@ -220,11 +232,11 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
             atomicOr(a.status, SV_FLAG_BAD_PAGE);
           } else {
             row = (page * a.Hkv + h) * BLK;
-            ok = 1;
+            ok = tailu ? 2 : 1;
           }
         }
       }
-      const int cnt = min(32, nblk - base);
+      const int cnt = min(32, nring - base);
       for (int qq = 0; qq < cnt; ++qq) {
         const int i = base + qq;
         const int rq = __shfl_sync(0xffffffffu, row, qq);
@@ -293,7 +305,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
     cs.l_lo = cs.l_hi = 0.f;
 
     const uint32_t sbase = smem_u32(smem);
-    for (int i = 0; i < nblk; ++i) {
+    for (int i = 0; i < nring; ++i) {
       const int s = i % NS;
       // warp-uniform outcome: ldmatrix/mma.sync below need all 32 lanes
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), (i / NS) & 1, kSpinLimit))) {
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
       }
       if (stage_ok[s]) {
         const uint32_t kb = sbase + s * C::kStageBytes;
-        cs.tile(kb, kb + C::kTileBytes, a, false, lane);
+        cs.tile(kb, kb + C::kTileBytes, a, false, stage_ok[s] == 2 ? a.tail : BLK, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
         *reinterpret_cast<uint4*>(smem + C::kTileBytes + o) = vv;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(NWC * 32) : "memory");
-      cs.tile(sbase, sbase + C::kTileBytes, a, true, lane);
+      cs.tile(sbase, sbase + C::kTileBytes, a, true, BLK, lane);
     }
     cs.l_lo += __shfl_xor_sync(0xffffffffu, cs.l_lo, 1);
     cs.l_lo += __shfl_xor_sync(0xffffffffu, cs.l_lo, 2);

@@ -62,11 +62,14 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int pair = b * a.Hkv + h;
-  // work units: the n_sel selected blocks, then the draft tile (unit n_sel)
+  // work units: the n_sel selected blocks, the partial last block (unit
+  // n_sel, if any), then the draft tile
+  const int ntail = a.tail > 0 ? 1 : 0;
   const int u0 = split * a.bps;
-  const int u1 = min(a.n_sel + 1, u0 + a.bps);
+  const int u1 = min(a.n_sel + ntail + 1, u0 + a.bps);
   const int j0 = u0, j1 = min(u1, a.n_sel);
-  const bool has_draft = (u0 <= a.n_sel && a.n_sel < u1);
+  const bool has_tail = ntail && u0 <= a.n_sel && a.n_sel < u1;
+  const bool has_draft = (u0 <= a.n_sel + ntail && a.n_sel + ntail < u1);
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
   const T* q = static_cast<const T*>(a.q);
@@ -103,6 +106,17 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
       for (int x = 0; x < a.blk; ++x)
         absorb<T>(st, kp + base + (size_t)x * a.d, vp + base + (size_t)x * a.d, a.d,
                   a.scale_log2, lane);
+    }
+    if (has_tail) {
+      const int page = a.block_table[(size_t)b * a.nb_max + a.nb];
+      if (page < 0 || page >= a.num_pages) {
+        if (lane == 0) atomicOr(a.status, SV_FLAG_BAD_PAGE);
+      } else {
+        const size_t base = ((size_t)page * a.Hkv + h) * a.blk * a.d;
+        for (int x = 0; x < a.tail; ++x)
+          absorb<T>(st, kp + base + (size_t)x * a.d, vp + base + (size_t)x * a.d, a.d,
+                    a.scale_log2, lane);
+      }
     }
     if (has_draft) {
       const unsigned long long vis = a.anc[t];

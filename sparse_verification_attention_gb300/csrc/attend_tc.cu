@@ -94,7 +94,8 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
 
 // The work of one CTA: up to kMaxSeg segments, each a run of consecutive work
 // units [u0, u1) of one (b, h) pair (units 0..n_sel-1 are the selected
-// blocks, unit n_sel the draft tile).
+// blocks, then the partial last block if the context has one, then the draft
+// tile).
 struct SegPlan {
   int n;
   int pair[kMaxSeg], u0[kMaxSeg], u1[kMaxSeg];
@@ -109,7 +110,7 @@ struct SegPlan {
 // arrival at the end of its CTA.
 __device__ SegPlan plan_segments(const AttendArgs& a) {
   SegPlan sp{};
-  const int W = a.n_sel + 1;
+  const int W = a.n_sel + (a.tail > 0 ? 1 : 0) + 1;
   const int c = blockIdx.x;
   if (a.streamk) {
     // stream-K: the flattened (pair, unit) sequence cut into gridDim.x equal
@@ -336,7 +337,43 @@ __global__ void __launch_bounds__(32 * 10, 1)
           }
         }
       }
-      if (sp.u0[j] <= a.n_sel && a.n_sel < sp.u1[j] && !stop) {
+      if (a.tail > 0 && sp.u0[j] <= a.n_sel && a.n_sel < sp.u1[j] && !stop) {
+        // the partial last block: a full page copy, of which the softmax keeps
+        // the first `tail` columns (stage_info bits 8..15)
+        int rq = oob_row, okq = 0;
+        if (lane == 0) {
+          const int page = a.block_table[(size_t)b * a.nb_max + a.nb];
+          if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.status, SV_FLAG_BAD_PAGE);
+          } else {
+            rq = (page * a.Hkv + h) * TBLK;
+            okq = 1 | (a.tail << 8);
+          }
+        }
+        int fail = 0;
+        if (lane == 0) {
+          const int s = i % NS;
+          if (i >= NS &&
+              !mbar_wait_abortable(smem_u32(&empty[s]), ((i / NS) & 1) ^ 1, abort_flag, a.status, 13u)) {
+            fail = 1;
+          } else {
+            stage_info[s] = okq;
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t kdst = smem_u32(ring + s * kStageBytes);
+            const uint32_t vdst = kdst + kTileBytes;
+            tma_load_2d(kdst, &tmK, 0, rq, fb);
+            tma_load_2d(kdst + kBoxBytes, &tmK, 64, rq, fb);
+            tma_load_2d(vdst, &tmV, 0, rq, fb);
+            tma_load_2d(vdst + kBoxBytes, &tmV, 64, rq, fb);
+            issued = i + 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, fail, 0)) stop = true;
+        ++i;
+      }
+      const int ud = a.n_sel + (a.tail > 0 ? 1 : 0);  // the draft tile's unit
+      if (sp.u0[j] <= ud && ud < sp.u1[j] && !stop) {
         // draft tile: this pair's draft rows t < T by TMA like any page; rows
         // T..63 lie outside the draft tensor and arrive as zeros (the softmax
         // masks them as well)
@@ -497,9 +534,12 @@ __global__ void __launch_bounds__(32 * 10, 1)
         }
         const int info = stage_info[s];
         if (info != 1) {
-          // invalid tile: nothing kept; draft tile: the row's visible drafts
-          // (branch-free: one 64-bit keep mask, one select per column)
-          const unsigned long long keepb = (info & 1) ? ((info & 2) ? vis : ~0ull) : 0ull;
+          // invalid tile: nothing kept; draft tile: the row's visible drafts;
+          // partial block: its first info >> 8 columns (branch-free: one
+          // 64-bit keep mask, one select per column)
+          const int lim = info >> 8;
+          const unsigned long long keepb =
+              (info & 1) ? ((info & 2) ? vis : (lim ? (1ull << lim) - 1ull : ~0ull)) : 0ull;
           const uint32_t klo = (uint32_t)keepb, khi = (uint32_t)(keepb >> 32);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {

@@ -101,6 +101,9 @@ struct AttendArgs {
   unsigned* status;
   int B, T, Hq, Hkv, G, d, blk, R, rpad;
   int nb, nb_max, num_pages, n_sel, sel_stride;
+  // tokens of a partial last block (logical block nb), 0 if none: always
+  // attended, as work unit n_sel (the draft tile follows it)
+  int tail;
   // Work units of a (b, h): the n_sel selected blocks, then the draft tile
   // (unit n_sel). Split s covers units [s*bps, min(n_sel+1, (s+1)*bps)).
   int n_splits, bps;

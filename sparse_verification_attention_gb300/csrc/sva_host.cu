@@ -68,12 +68,13 @@ sv_status check_shape(const sv_shape* s) {
 sv_status check_kv(const sv_shape* s, const sv_kv* kv, bool need_v) {
   if (!kv) return fail(SV_ERR_INVALID_ARG, "kv is NULL");
   if (kv->ctx < 0) return fail(SV_ERR_INVALID_ARG, "ctx=%d is negative", kv->ctx);
-  if (kv->ctx % s->blk)
-    return fail(SV_ERR_UNSUPPORTED, "ctx=%d is not a multiple of blk=%d", kv->ctx, s->blk);
-  const int nb = kv->ctx / s->blk;
+  const int nb = kv->ctx / s->blk;                       // full blocks
+  const int nblocks = (kv->ctx + s->blk - 1) / s->blk;   // with a partial last one
   if (nb > kMaxNB) return fail(SV_ERR_UNSUPPORTED, "NB=%d blocks exceeds %d", nb, kMaxNB);
-  if (kv->nb_max < nb) return fail(SV_ERR_INVALID_ARG, "nb_max=%d < NB=%d", kv->nb_max, nb);
-  if (nb > 0) {
+  if (kv->nb_max < nblocks)
+    return fail(SV_ERR_INVALID_ARG, "nb_max=%d < %d blocks holding ctx=%d", kv->nb_max, nblocks,
+                kv->ctx);
+  if (nblocks > 0) {
     if (!kv->k_pool || (need_v && !kv->v_pool) || !kv->block_table)
       return fail(SV_ERR_INVALID_ARG, "k_pool/v_pool/block_table is NULL");
     if (kv->num_pages < 1) return fail(SV_ERR_INVALID_ARG, "num_pages=%d", kv->num_pages);
@@ -187,9 +188,10 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   WsLayout L;
   const int G = s.Hq / s.Hkv;
   L.rpad = round_up(s.T * G, 16);
-  // one partial slot per work unit (selected blocks + the draft tile), plus
-  // one for a stream-K run that leaves a pair mid-stream
-  const int units = (kmax < 0 ? 0 : kmax) + 1;
+  // one partial slot per work unit (selected blocks, a partial last block,
+  // the draft tile), plus one for a stream-K run that leaves a pair
+  // mid-stream
+  const int units = (kmax < 0 ? 0 : kmax) + 2;
   L.slots = units + 1 > kMaxSplits ? kMaxSplits : units + 1;
   const size_t pairs = (size_t)s.B * s.Hkv;
   L.status = 0;
@@ -299,7 +301,7 @@ static int streamk_slots(int pairs, int W, int G) {
 
 static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int max_slots) {
   AttendPlan p{};
-  const int n_units = n_sel + 1;
+  const int n_units = n_sel + (a.tail > 0 ? 1 : 0) + 1;  // blocks, partial block, drafts
   const bool tcp = attend_tc_applies(a, dtype);
   const bool fast = !tcp && attend_fast_applies(a, dtype);
   p.path = tcp ? SV_PATH_TCGEN05 : fast ? SV_PATH_MMA_SYNC : SV_PATH_CUDA_CORES;
@@ -407,6 +409,7 @@ static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_
   a.R = s->T * a.G;
   a.rpad = L.rpad;
   a.nb = kv->ctx / s->blk;
+  a.tail = kv->ctx % s->blk;
   a.nb_max = kv->nb_max;
   a.num_pages = kv->num_pages;
   a.n_sel = n_sel;

@@ -78,7 +78,13 @@ class Workload:
 
     @property
     def NB(self) -> int:
+        """Full blocks of the context (the candidates for selection)."""
         return self.ctx // self.blk
+
+    @property
+    def NBT(self) -> int:
+        """Blocks holding the context, a partial last block included."""
+        return (self.ctx + self.blk - 1) // self.blk
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -191,7 +197,8 @@ def make_layer(wl: Workload, layer: int = 0, device="cpu",
     if planted is None:
         planted = planted_sets(wl)[layer] if wl.layers > 1 else planted_sets(wl)[0]
     dt = wl.torch_dtype
-    NB, P = wl.NB, wl.B * wl.NB
+    NB, NBT = wl.NB, wl.NBT
+    P = wl.B * NBT
     g = torch.Generator(device=device).manual_seed(wl.seed + layer)
     q = torch.randn(wl.B, wl.T, wl.Hq, wl.d, generator=g, device=device, dtype=dt)
     k_pool = torch.randn(P, wl.Hkv, wl.blk, wl.d, generator=g, device=device, dtype=dt)
@@ -202,7 +209,7 @@ def make_layer(wl: Workload, layer: int = 0, device="cpu",
         perm = torch.randperm(P, generator=g, device=device)
     else:
         perm = torch.arange(P, device=device)
-    block_table = perm.view(wl.B, NB).to(torch.int32).contiguous()
+    block_table = perm.view(wl.B, NBT).to(torch.int32).contiguous()
 
     if NB > 0:
         qbar0 = q[:, 0].float().view(wl.B, wl.Hkv, wl.G, wl.d).mean(dim=2)  # [B,Hkv,d]

@@ -80,17 +80,18 @@ def test_workspace_sizes(L):
     s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
     n = api.sv_workspace_bytes(s, 2048, 128)
     # status + two per-(b,h) counter arrays + scores + split partials o and
-    # (m, l); 129 work units (128 blocks + the draft tile) capped at 64 slots
+    # (m, l); 130 work units (128 blocks, a partial block, the draft tile)
+    # capped at 64 slots
     pairs = 4 * 8
     ctrs = 2 * 256
     scores = pairs * 2048 * 4
     part = pairs * 64 * 32 * 128 * 4
     ml = pairs * 64 * 32 * 2 * 4
     assert n == 256 + ctrs + scores + part + ml
-    # 8 selected blocks + the draft tile + one slot for a run that leaves a
-    # pair mid-stream = 10 partial slots
+    # 8 selected blocks + a partial last block + the draft tile + one slot
+    # for a run that leaves a pair mid-stream = 11 partial slots
     n8 = api.sv_workspace_bytes(s, 2048, 8)
-    assert n8 == 256 + ctrs + scores + pairs * 10 * 32 * 128 * 4 + pairs * 10 * 32 * 2 * 4
+    assert n8 == 256 + ctrs + scores + pairs * 11 * 32 * 128 * 4 + pairs * 11 * 32 * 2 * 4
     bad = api.make_shape(4, 30, 8, 128, 64, 8, torch.bfloat16)  # Hq % Hkv != 0
     assert api.sv_workspace_bytes(bad, 2048, 128) == 0
     assert api.sv_workspace_bytes(api.make_shape(1, 4, 2, 12, 16, 4, 1), 64, 8) == 0  # d % 8
@@ -112,9 +113,14 @@ def test_invalid_arguments_rejected_before_launch(L):
     st, msg = _status(L, L.sv_sparse_attend, C.byref(s), None, C.byref(kv), None, 0, 0, None, None,
                       None, None, None, 0, None)
     assert st == api.SV_ERR_INVALID_ARG and "NULL" in msg
-    bad_kv = api.KV(fake, fake, fake, 64, 64, 1000)  # ctx % blk != 0
-    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(bad_kv), 0, 1, fake, None)
-    assert st == api.SV_ERR_UNSUPPORTED, msg
+    # a partial last block (1000 = 62 * 16 + 8) needs its own block-table column
+    tail_kv = api.KV(fake, fake, fake, 62, 64, 1000)
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(tail_kv), 0, 1, fake, None)
+    assert st == api.SV_ERR_INVALID_ARG and "nb_max" in msg
+    # ... and gets no representative: only the 62 full blocks do
+    tail_kv = api.KV(fake, fake, fake, 63, 64, 1000)
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(tail_kv), 62, 1, fake, None)
+    assert st == api.SV_ERR_INVALID_ARG, msg
     st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(kv), 60, 10, fake, None)
     assert st == api.SV_ERR_INVALID_ARG, msg
     small = api.KV(fake, fake, fake, 10, 64, 1024)  # nb_max < NB

@@ -151,6 +151,12 @@ ATTEND_CASES = [
     ("tc_sk_one_unit_per_cta", dict(B=4, Hq=8, Hkv=2, ctx=64 * 30), 18),
     ("tc_sk_runs_cross_pairs", dict(B=19, Hq=4, Hkv=1, T=4, ctx=64 * 12), 8),
     ("tc_sk_two_unit_pairs", dict(B=75, Hq=4, Hkv=2, T=2, ctx=64 * 4), 1),
+    # contexts ending in a partial block: its tokens are always attended
+    ("tc_tail_split", dict(ctx=64 * 20 + 17), 7),
+    ("tc_sk_tail", dict(B=4, Hq=32, Hkv=8, ctx=64 * 100 + 40), 50),
+    ("tc_tail_only", dict(ctx=37), 0),
+    ("tc_sk_tail_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                                    ctx=64 * 30 + 63), 20),
     ("mma_R16_pad", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), 17),
     ("mma_R48_rows_pad", dict(Hq=8, Hkv=2, T=12, blk=32, ctx=32 * 45), 9),
     ("mma_d64_blk64", dict(d=64, ctx=64 * 30), 11),
@@ -161,6 +167,10 @@ ATTEND_CASES = [
     ("generic_T_gt_blk", dict(T=40, Hq=2, Hkv=1, blk=32, ctx=32 * 30), 7),
     ("generic_R256", dict(T=32, Hq=16, Hkv=2, ctx=64 * 20), 6),
     ("generic_blk16_bf16", dict(blk=16, ctx=16 * 90), 19),
+    ("mma_tail", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50 + 5), 17),
+    ("mma_many_tail", dict(B=8, Hq=32, Hkv=8, blk=32, ctx=32 * 40 + 31), 9),
+    ("generic_tail_f32", dict(dtype="f32", d=64, blk=16, ctx=16 * 64 + 9, Hq=4, Hkv=2, T=4), 8),
+    ("generic_tail_R256", dict(T=32, Hq=16, Hkv=2, ctx=64 * 20 + 63), 6),
 ]
 
 
@@ -188,7 +198,8 @@ def test_sparse_attend(name, over, n_sel):
     words = st.ws[:8].view(torch.int32).tolist()
     assert api.sv_read_status(st.ws) == 0, f"status words {words} plan {plan.cluster} {plan.n_splits}"
     ref = O.sparse_attend(x.q, x.k_pool, x.v_pool, x.block_table, sel[:, :, :n_sel].long(),
-                          x.draft_k, x.draft_v, wl.parent_list())
+                          x.draft_k, x.draft_v, wl.parent_list(), tail_block=wl.NB,
+                          tail_len=wl.ctx % wl.blk)
     U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
 
 
@@ -228,12 +239,16 @@ def test_tc_late_rescale_divergent_rows():
     U.compare_out(out, ref, U.BF16_ATOL)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32", "bf16_many_pairs"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "bf16_many_pairs", "bf16_tail", "f32_tail"])
 def test_dense_attend(dtype):
     if dtype == "bf16":
         over = dict(ctx=64 * 33)
     elif dtype == "bf16_many_pairs":
         dtype, over = "bf16", dict(B=8, Hq=32, Hkv=8, ctx=64 * 21)
+    elif dtype == "bf16_tail":
+        dtype, over = "bf16", dict(B=4, Hq=32, Hkv=8, ctx=64 * 21 + 50)
+    elif dtype == "f32_tail":
+        dtype, over = "f32", dict(d=64, blk=16, ctx=16 * 70 + 3, T=5, parents=(-1, 0, 0, 1, 2))
     else:
         over = dict(d=64, blk=16, ctx=16 * 70, T=5, parents=(-1, 0, 0, 1, 2))
     wl = small_wl(dtype, **over)
@@ -244,8 +259,8 @@ def test_dense_attend(dtype):
     api.sv_sparse_attend(st.shape, xd.q, st.kv, None, 0, 0, xd.draft_k, xd.draft_v, st.parents,
                          out, st.ws)
     torch.cuda.synchronize()
-    ref = O.dense_verify_attention(x.q, O.logical_kv(x.k_pool, x.block_table, wl.NB),
-                                   O.logical_kv(x.v_pool, x.block_table, wl.NB), x.draft_k,
+    ref = O.dense_verify_attention(x.q, O.logical_kv_tokens(x.k_pool, x.block_table, wl.ctx),
+                                   O.logical_kv_tokens(x.v_pool, x.block_table, wl.ctx), x.draft_k,
                                    x.draft_v, wl.parent_list())
     U.compare_out(out, ref, U.out_atol(wl.torch_dtype))
 
@@ -288,7 +303,8 @@ def _verify_vs_oracle(wl, x, xd, pairs=None):
         differ = U.compare_selection(gsel[b:b + 1, hs], sub_scores, k)
         sel = O.select_all(scores, k)
         ref = O.sparse_attend(qb, x.k_pool, x.v_pool, btb, sel, x.draft_k[b:b + 1],
-                              x.draft_v[b:b + 1], wl.parent_list())
+                              x.draft_v[b:b + 1], wl.parent_list(), tail_block=wl.NB,
+                              tail_len=wl.ctx % wl.blk)
         for i, h in enumerate(hs):
             if (0, i) in differ:
                 continue
@@ -327,6 +343,15 @@ def test_verify_tiny_f32():
 
 def test_verify_llama8b_32k_full():
     wl = W.WORKLOADS["llama8b_32k"]
+    x = W.make_layer(wl)
+    _verify_vs_oracle(wl, x, x.to("cuda"))
+
+
+def test_verify_llama8b_32k_partial_last_block():
+    """A 32K context plus 40 tokens: 512 full blocks compete for the budget,
+    the 40-token block is always attended."""
+    from dataclasses import replace
+    wl = replace(W.WORKLOADS["llama8b_32k"], ctx=32768 + 40)
     x = W.make_layer(wl)
     _verify_vs_oracle(wl, x, x.to("cuda"))
 

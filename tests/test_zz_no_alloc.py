@@ -48,6 +48,7 @@ def _sel(B, H, NB, k, seed):
 CASES = [
     # name (expected path), workload overrides, selection sizes of the two calls
     ("tc", dict(), (13, 29)),
+    ("tc_partial_last_block", dict(ctx=64 * 40 + 13), (13, 29)),
     ("tc_many_pairs_tree16", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
                                   ctx=64 * 20), (11, 3)),
     ("mma", dict(Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), (17, 40)),
