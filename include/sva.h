@@ -240,6 +240,29 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           int kmax, int* k_out, void* out, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* Acceptance write-back: the step after verification. The pages have no
+ * formula for it; it closes the loop that [SV-Fig1] verifies one step of:
+ * the accepted drafts become context for the next step. Sequence b (ctx_b =
+ * seq_ctx[b] tokens before the call) appends the K/V rows of drafts
+ * accept_idx[b][0 .. n) in that order, n = n_accept[b] clamped to [0, T], at
+ * token positions ctx_b, ctx_b + 1, ... (page block_table[b][pos / blk],
+ * slot pos % blk), for every KV head. When reps is not NULL, every block the
+ * append makes full (blocks ctx_b / blk .. (ctx_b + n) / blk - 1) gets its
+ * representative rebuilt as in sv_build_reps.
+ * k_pool, v_pool: [num_pages, Hkv, blk, d], written; block_table: [B, nb_max]
+ * with the pages for the new positions already assigned; seq_ctx, n_accept:
+ * DEVICE int32 [B]; accept_idx: DEVICE int32 [B, T]; draft_k, draft_v:
+ * [B, T, Hkv, d]; reps: [B, Hkv, nb_max, d] fp32 or NULL; workspace (may be
+ * NULL): a workspace whose status word receives SV_FLAG_BAD_BLOCK_INDEX for
+ * a draft index outside [0, T) and SV_FLAG_BAD_PAGE for a position without a
+ * valid page (those rows are skipped). Rows of different sequences must not
+ * share pages. Asynchronous on stream. */
+sv_status sv_append_kv(const sv_shape* shape, void* k_pool, void* v_pool,
+                       const int32_t* block_table, int nb_max, int num_pages,
+                       const int32_t* seq_ctx, const int32_t* n_accept,
+                       const int32_t* accept_idx, const void* draft_k, const void* draft_v,
+                       float* reps, void* workspace, void* stream);
+
 /* sv_sparse_attend without a workspace. The paper has no counterpart: this
  * entry exists for callers that cannot allocate device memory, such as an
  * operation hosted by another runtime (a plugin or callback handed only its

@@ -30,7 +30,7 @@ ABI_VERSION = 2  # SV_ABI_VERSION the structures below match
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
             "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
-            "sv_verify_layer", "sv_sparse_attend_noalloc")
+            "sv_verify_layer", "sv_sparse_attend_noalloc", "sv_append_kv")
 
 
 class SvError(RuntimeError):
@@ -93,6 +93,8 @@ def lib() -> C.CDLL:
                                     vp, vp, sz, vp]),
             "sv_sparse_attend_noalloc": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, i, i, vp,
                                              vp, C.POINTER(C.c_int32), vp, vp, vp]),
+            "sv_append_kv": (i, [C.POINTER(Shape), vp, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp,
+                                 vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -226,6 +228,17 @@ def sv_sparse_attend_noalloc(shape: Shape, q, kv: KV, sel, n_sel: int, sel_strid
                                           sel_stride, _ptr(draft_k), _ptr(draft_v),
                                           _parents(parents), _ptr(out), _ptr(flags_out),
                                           _stream(stream)))
+
+
+def sv_append_kv(shape: Shape, k_pool, v_pool, block_table, seq_ctx, n_accept, accept_idx,
+                 draft_k, draft_v, reps=None, ws=None, stream=None):
+    """Append each sequence's accepted drafts to its paged cache (and rebuild
+    the representatives of blocks that fill). seq_ctx, n_accept: device int32
+    [B]; accept_idx: device int32 [B, T]."""
+    _check(lib().sv_append_kv(C.byref(shape), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                              block_table.shape[1], k_pool.shape[0], _ptr(seq_ctx),
+                              _ptr(n_accept), _ptr(accept_idx), _ptr(draft_k), _ptr(draft_v),
+                              _ptr(reps), _ptr(ws), _stream(stream)))
 
 
 def sv_attend_plan(shape: Shape, kv: KV, n_sel: int) -> Plan:

@@ -62,6 +62,25 @@ struct RepsArgs {
 };
 cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st);
 
+// Acceptance write-back: sequence b appends the drafts accept_idx[b][0, n)
+// (n = n_accept[b], clamped to [0, T]) at positions seq_ctx[b], ... of its
+// paged cache.
+struct AppendArgs {
+  void* k_pool;
+  void* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_ctx;     // [B] device
+  const int32_t* n_accept;    // [B] device
+  const int32_t* accept_idx;  // [B, T] device
+  const void* draft_k;        // [B, T, Hkv, d]
+  const void* draft_v;
+  unsigned* status;           // may be null
+  int B, T, Hkv, d, blk, nb_max, num_pages;
+};
+cudaError_t launch_append_kv(const AppendArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_append_reps(const RepsArgs& a, const AppendArgs& ap, int dtype,
+                               cudaStream_t st);
+
 struct ScoreArgs {
   const void* q;
   const float* reps;

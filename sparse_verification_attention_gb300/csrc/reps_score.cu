@@ -39,18 +39,15 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 constexpr int kRepThreads = 128;
 constexpr int kRepBatch = 8;  // token loads in flight per thread
 
+// Representative of logical block j of (sequence b, kv head h); all
+// kRepThreads threads of the CTA call it (part: kRepThreads * VEC floats of
+// shared memory).
 template <typename T>
-__global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
+__device__ void block_rep(const RepsArgs& a, int b, int h, int j, float* part) {
   constexpr int VEC = 16 / sizeof(T);  // elements per 16-byte chunk
-  __shared__ float part[kRepThreads * VEC];
-  const int j = a.first_block + blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
   const int chunks = a.d / VEC;
   const int groups = kRepThreads / chunks;  // >= 1 since d <= 256
   const int c = threadIdx.x % chunks, g = threadIdx.x / chunks;
-  pdl_wait();
-  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   const int page = a.block_table[(size_t)b * a.nb_max + j];
   float* dst = a.reps + (((size_t)b * a.Hkv + h) * a.nb_max + j) * a.d;
   if (page < 0 || page >= a.num_pages) {
@@ -95,6 +92,32 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
     for (int gg = 0; gg < groups; ++gg) sum += part[(gg * chunks + ci) * VEC + ei];
     dst[i] = sum * inv;
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
+  __shared__ float part[kRepThreads * (16 / sizeof(T))];
+  pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
+  block_rep<T>(a, blockIdx.z, blockIdx.y, a.first_block + blockIdx.x, part);
+}
+
+// After an append: grid (B, most blocks one append can complete, Hkv); CTA
+// (b, f, h) rebuilds block ctx_b / blk + f of sequence b if the append made
+// it full.
+template <typename T>
+__global__ void __launch_bounds__(kRepThreads) append_reps_kernel(RepsArgs a, AppendArgs ap) {
+  __shared__ float part[kRepThreads * (16 / sizeof(T))];
+  pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
+  const int b = blockIdx.x, h = blockIdx.z;
+  const int ctx = ap.seq_ctx[b];
+  const int n = min(max(ap.n_accept[b], 0), ap.T);
+  if (ctx < 0) return;  // flagged by the copy kernel
+  const int j = ctx / a.blk + blockIdx.y;
+  if (j >= (ctx + n) / a.blk) return;
+  if (j >= a.nb_max) return;  // flagged by the copy kernel
+  block_rep<T>(a, b, h, j, part);
 }
 
 // ------------------------------------------------------------------ scores
@@ -209,6 +232,17 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
 }
 
 }  // namespace
+
+cudaError_t launch_append_reps(const RepsArgs& a, const AppendArgs& ap, int dtype,
+                               cudaStream_t st) {
+  // appending at most T tokens completes at most (blk - 1 + T) / blk blocks
+  const int most = (a.blk - 1 + ap.T) / a.blk;
+  if (a.B == 0 || most == 0) return cudaSuccess;
+  dim3 grid(a.B, most, a.Hkv);
+  if (dtype == SV_BF16)
+    return launch_pdl(append_reps_kernel<__nv_bfloat16>, grid, dim3(kRepThreads), 0, st, a, ap);
+  return launch_pdl(append_reps_kernel<float>, grid, dim3(kRepThreads), 0, st, a, ap);
+}
 
 cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st) {
   if (a.n_blocks == 0) return cudaSuccess;

@@ -558,6 +558,37 @@ sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block,
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "build_reps launch");
 }
 
+sv_status sv_append_kv(const sv_shape* shape, void* k_pool, void* v_pool, const int32_t* block_table,
+                       int nb_max, int num_pages, const int32_t* seq_ctx, const int32_t* n_accept,
+                       const int32_t* accept_idx, const void* draft_k, const void* draft_v,
+                       float* reps, void* workspace, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if (!k_pool || !v_pool || !block_table || !seq_ctx || !n_accept || !accept_idx || !draft_k ||
+      !draft_v)
+    return fail(SV_ERR_INVALID_ARG, "a pool, table, index array or draft tensor is NULL");
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16))
+    return fail(SV_ERR_INVALID_ARG, "pools and draft tensors must be 16-byte aligned");
+  if (nb_max < 1 || num_pages < 1)
+    return fail(SV_ERR_INVALID_ARG, "nb_max=%d / num_pages=%d", nb_max, num_pages);
+  if (reps && !aligned(reps, 16)) return fail(SV_ERR_INVALID_ARG, "reps must be 16-byte aligned");
+  if (workspace && !aligned(workspace, 256))
+    return fail(SV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  unsigned* status = static_cast<unsigned*>(workspace);
+  const AppendArgs ap{k_pool, v_pool, block_table, seq_ctx, n_accept, accept_idx, draft_k, draft_v,
+                      status, shape->B, shape->T, shape->Hkv, shape->d, shape->blk, nb_max, num_pages};
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_append_kv(ap, shape->dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  if (reps) {
+    const RepsArgs ra{k_pool, block_table, reps, shape->B, shape->Hkv, shape->d, shape->blk, nb_max,
+                      num_pages, 0, 0, status};
+    e = launch_append_reps(ra, ap, shape->dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "append reps launch");
+  }
+  return SV_OK;
+}
+
 sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* reps, const sv_kv* kv,
                           float* scores, void* stream) {
   sv_status r = check_shape(shape);

@@ -146,3 +146,10 @@ def test_invalid_arguments_rejected_before_launch(L):
     assert st == api.SV_ERR_UNSUPPORTED, msg
     st, msg = _status(L, L.sv_clear_status, None, None)
     assert st == api.SV_ERR_INVALID_ARG
+    # acceptance write-back: NULL index arrays, misaligned pools
+    st, msg = _status(L, L.sv_append_kv, C.byref(s), fake, fake, fake, 64, 64, None, fake, fake,
+                      fake, fake, None, None, None)
+    assert st == api.SV_ERR_INVALID_ARG and "NULL" in msg
+    st, msg = _status(L, L.sv_append_kv, C.byref(s), fake + 4, fake, fake, 64, 64, fake, fake, fake,
+                      fake, fake, None, None, None)
+    assert st == api.SV_ERR_INVALID_ARG and "aligned" in msg

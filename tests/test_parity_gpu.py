@@ -462,3 +462,117 @@ def test_bad_indices_flagged_not_faulting():
     torch.cuda.synchronize()
     assert api.sv_read_status(st.ws) & api.SV_FLAG_BAD_PAGE
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------------ acceptance write-back
+def _append_case(dtype, blk, ctx, n_acc, acc, T=6, Hkv=2, d=128, seed=3):
+    B = len(ctx)
+    nbt = max((c + T + blk - 1) // blk for c in ctx)  # room for every appended token
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    P = B * nbt
+    kp = torch.randn(P, Hkv, blk, d, generator=g).to(dt)
+    vp = torch.randn(P, Hkv, blk, d, generator=g).to(dt)
+    dk = torch.randn(B, T, Hkv, d, generator=g).to(dt)
+    dv = torch.randn(B, T, Hkv, d, generator=g).to(dt)
+    bt = torch.randperm(P, generator=g).view(B, nbt).to(torch.int32)
+    accept = torch.full((B, T), -1, dtype=torch.int32)
+    for b in range(B):
+        accept[b, :len(acc[b])] = torch.tensor(acc[b], dtype=torch.int32)
+    return kp, vp, dk, dv, bt, accept
+
+
+@pytest.mark.parametrize("dtype,blk", [("bf16", 64), ("bf16", 16), ("f32", 16)])
+def test_append_kv_vs_oracle(dtype, blk):
+    ctx = [blk * 3 + 5, blk * 2, blk * 4 + blk - 1]
+    n_acc = [3, 6, 2]
+    acc = [[0, 1, 3], [0, 2, 4, 5, 1, 3], [0, 5]]
+    T, Hkv, d = 6, 2, 128
+    kp, vp, dk, dv, bt, accept = _append_case(dtype, blk, ctx, n_acc, acc, T=T, Hkv=Hkv, d=d)
+    B, nbt = bt.shape
+    shape = api.make_shape(B, 4, Hkv, d, blk, T, kp.dtype)
+    reps_before = torch.randn(B, Hkv, nbt, d)  # stand-ins: only filled blocks may change
+    kpd, vpd, reps = kp.cuda(), vp.cuda(), reps_before.clone().cuda()
+    ws = api.alloc_workspace(shape, nbt, 4)
+    api.sv_append_kv(shape, kpd, vpd, bt.cuda(), torch.tensor(ctx, dtype=torch.int32).cuda(),
+                     torch.tensor(n_acc, dtype=torch.int32).cuda(), accept.cuda(), dk.cuda(),
+                     dv.cuda(), reps, ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(ws) == 0
+    kn, vn, filled = O.append_accepted(kp, vp, bt, ctx, n_acc, accept.tolist(), dk, dv)
+    assert torch.equal(kpd.cpu(), kn) and torch.equal(vpd.cpu(), vn)  # a copy: bit-exact
+    new_reps = O.block_representatives(kn, bt, nbt, blk)
+    got = reps.cpu()
+    for b in range(B):
+        for j in range(nbt):
+            if j in filled[b]:
+                assert torch.allclose(got[b, :, j].double(), new_reps[b, :, j], atol=1e-5), (b, j)
+            else:
+                assert torch.equal(got[b, :, j], reps_before[b, :, j]), (b, j)
+    assert any(filled)  # the case completes blocks
+
+
+def test_append_kv_bad_index_skipped_and_flagged():
+    ctx, n_acc, acc = [64 + 3, 64], [2, 2], [[0, 7], [1, 0]]  # draft 7 does not exist (T = 6)
+    kp, vp, dk, dv, bt, accept = _append_case("bf16", 64, ctx, n_acc, acc)
+    B, nbt = bt.shape
+    shape = api.make_shape(B, 4, 2, 128, 64, 6, kp.dtype)
+    kpd, vpd = kp.cuda(), vp.cuda()
+    ws = api.alloc_workspace(shape, nbt, 4)
+    api.sv_append_kv(shape, kpd, vpd, bt.cuda(), torch.tensor(ctx, dtype=torch.int32).cuda(),
+                     torch.tensor(n_acc, dtype=torch.int32).cuda(), accept.cuda(), dk.cuda(),
+                     dv.cuda(), None, ws)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(ws) & api.SV_FLAG_BAD_BLOCK_INDEX
+    # the bad row is skipped, the others land
+    good = [[0], [1, 0]]
+    kn, vn, _ = O.append_accepted(kp, vp, bt, ctx, [1, 2], good, dk, dv)
+    assert torch.equal(kpd.cpu(), kn) and torch.equal(vpd.cpu(), vn)
+
+
+def test_verify_append_verify_loop():
+    """Two steps of the speculative loop on the device against the oracle:
+    verify at ctx, append n accepted drafts (the same n for every sequence),
+    then verify the next step's drafts at ctx + n, whose last block is
+    partial."""
+    from dataclasses import replace
+    wl = replace(small_wl(B=3, Hq=8, Hkv=2, ctx=64 * 24, T=8), ctx=64 * 24)
+    n = 5
+    x = W.make_layer(replace(wl, ctx=wl.ctx + 64))  # pages for the appended tokens
+    x0 = W.LayerInputs(x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k, x.draft_v, x.planted,
+                       parents=x.parents)
+    xd = x0.to("cuda")
+    st = api.LayerState(wl, xd)
+    out1 = st.verify()
+    torch.cuda.synchronize()
+    # accept the first n drafts of the chain
+    accept = torch.tensor([list(range(n)) + [-1] * (wl.T - n)] * wl.B, dtype=torch.int32)
+    ctx_t = torch.full((wl.B,), wl.ctx, dtype=torch.int32)
+    nacc_t = torch.full((wl.B,), n, dtype=torch.int32)
+    api.sv_append_kv(st.shape, xd.k_pool, xd.v_pool, xd.block_table, ctx_t.cuda(), nacc_t.cuda(),
+                     accept.cuda(), xd.draft_k, xd.draft_v, st.reps, st.ws)
+    # next step: new drafts and queries over the longer context
+    wl2 = replace(wl, ctx=wl.ctx + n)
+    g = torch.Generator().manual_seed(77)
+    q2 = torch.randn(x.q.shape, generator=g).to(x.q.dtype)
+    dk2 = torch.randn(x.draft_k.shape, generator=g).to(x.q.dtype)
+    dv2 = torch.randn(x.draft_v.shape, generator=g).to(x.q.dtype)
+    st2 = api.LayerState(wl2, W.LayerInputs(q2.cuda(), xd.k_pool, xd.v_pool, xd.block_table,
+                                            dk2.cuda(), dv2.cuda(), x.planted, parents=x.parents),
+                         build_reps=False)
+    st2.reps.copy_(st.reps)  # the running representatives, updated by the append
+    out2 = st2.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0 and api.sv_read_status(st2.ws) == 0
+    # the same two steps on the oracle
+    ref1, _, _ = O.verify_layer(x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k, x.draft_v,
+                                wl.parent_list(), wl.ctx, wl.blk, wl.budget)
+    U.compare_out(out1, ref1, U.BF16_ATOL)
+    kn, vn, _ = O.append_accepted(x.k_pool, x.v_pool, x.block_table, [wl.ctx] * wl.B, [n] * wl.B,
+                                  accept.tolist(), x.draft_k, x.draft_v)
+    assert torch.equal(xd.k_pool.cpu(), kn) and torch.equal(xd.v_pool.cpu(), vn)
+    ref2, sel2, scores2 = O.verify_layer(q2, kn, vn, x.block_table, dk2, dv2, wl.parent_list(),
+                                         wl2.ctx, wl.blk, wl.budget)
+    differ = U.compare_selection(st2.sel.cpu(), scores2, st2.k)
+    assert not differ
+    U.compare_out(out2, ref2, U.BF16_ATOL)
