@@ -310,6 +310,27 @@ def verify_stack(layers, parents, ctx: int, blk: int, budget, compute_every: int
 
 
 # --------------------------------------------------------------------------
+# The shared-set diagnostic  [SV-Fig1]: how much each draft's own block set
+# overlaps the first draft's (the set every draft actually uses)
+# --------------------------------------------------------------------------
+def draft_selection_overlap(q: torch.Tensor, reps: torch.Tensor, G: int, k: int) -> torch.Tensor:
+    """overlap[b, h, t] = |S_t ∩ S_0| / k, where S_t is the top-k block set
+    that draft t's own query would select (same scoring and tie rule as
+    draft 0's). q [B,T,Hq,d]; reps [B,Hkv,NB,d]. Returns fp64 [B,Hkv,T]."""
+    B, T = q.shape[0], q.shape[1]
+    Hkv, NB = reps.shape[1], reps.shape[2]
+    kk = min(k, NB)
+    sets = [select_all(block_scores(q[:, t:t + 1], reps, G), kk) for t in range(T)]
+    out = torch.zeros(B, Hkv, T, dtype=F64)
+    for b in range(B):
+        for h in range(Hkv):
+            s0 = set(sets[0][b, h].tolist())
+            for t in range(T):
+                out[b, h, t] = len(s0 & set(sets[t][b, h].tolist())) / kk if kk else 1.0
+    return out
+
+
+# --------------------------------------------------------------------------
 # Acceptance write-back: the step after verification (not on the pages)
 # --------------------------------------------------------------------------
 def append_accepted(k_pool, v_pool, block_table, ctx: Sequence[int], n_accept: Sequence[int],

@@ -412,4 +412,23 @@ def pin_append_accepted(O):
             assert torch.equal(kn[p], kp[p]) and torch.equal(vn[p], vp[p])
 
 
+# ------------------------------------------------- shared-set diagnostic
+def pin_draft_overlap_closed_form(O):
+    """One-hot representatives: block j's rep is e_(j mod d) scaled by
+    (j + 1), so a query equal to e_i scores block j by (j + 1) [j = i mod d].
+    Draft t's query e_(t) with d = 4, NB = 8, k = 2 picks blocks {t, t + 4};
+    the overlap with draft 0's {0, 4} is 1 for t = 0 and 0 otherwise; a draft
+    that repeats draft 0's query overlaps fully."""
+    B, T, Hkv, G, d, NB = 1, 5, 1, 1, 4, 8
+    reps = torch.zeros(B, Hkv, NB, d, dtype=F64)
+    for j in range(NB):
+        reps[0, 0, j, j % d] = j + 1.0
+    q = torch.zeros(B, T, Hkv * G, d, dtype=F64)
+    for t in range(4):
+        q[0, t, 0, t] = 1.0
+    q[0, 4, 0, 0] = 3.0  # same direction as draft 0
+    ov = O.draft_selection_overlap(q, reps, G, 2)
+    assert ov[0, 0].tolist() == [1.0, 0.0, 0.0, 0.0, 1.0]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -576,3 +576,60 @@ def test_verify_append_verify_loop():
     differ = U.compare_selection(st2.sel.cpu(), scores2, st2.k)
     assert not differ
     U.compare_out(out2, ref2, U.BF16_ATOL)
+
+
+# ------------------------------------------------------------------ reuse schedules, diagnostic
+@pytest.mark.parametrize("every", [3, 4])
+def test_stack_reuse_schedules(every):
+    """Layers recompute the selection every `every`-th layer and reuse it in
+    between (any schedule goes through the reuse flag); every layer against
+    the oracle stack, with a partial last block."""
+    from dataclasses import replace
+    wl = replace(small_wl(ctx=64 * 30 + 20), name="stack", layers=6, compute_every=every, drift=2,
+                 budget=W.Budget(W.BUDGET_FIXED, 9, 0, 0, 0, 0, 0))
+    ps = W.planted_sets(wl)
+    prev, sels, outs, cpu_layers = None, [], [], []
+    for l in range(wl.layers):
+        xd = W.make_layer(wl, l, device="cuda", planted=ps[l])
+        st = api.LayerState(wl, xd)
+        reuse = l % every != 0
+        if reuse:
+            st.sel = prev.sel.clone()
+        st.verify(reuse=int(reuse))
+        torch.cuda.synchronize()
+        assert api.sv_read_status(st.ws) == 0
+        sels.append(st.sel.cpu())
+        outs.append(st.out.cpu())
+        x = xd.to("cpu")
+        cpu_layers.append((x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k, x.draft_v))
+        prev = st
+    ref_outs, ref_sels = O.verify_stack(cpu_layers, wl.parent_list(), wl.ctx, wl.blk, wl.budget,
+                                        every)
+    for l in range(wl.layers):
+        if l % every:
+            assert torch.equal(sels[l], sels[l - l % every])
+        else:
+            reps = O.block_representatives(cpu_layers[l][1], cpu_layers[l][3], wl.NB, wl.blk)
+            scores = O.block_scores(cpu_layers[l][0], reps, wl.G)
+            assert not U.compare_selection(sels[l], scores, ref_sels[l].shape[-1])
+        U.compare_out(outs[l], ref_outs[l], U.BF16_ATOL)
+
+
+def test_draft_selection_overlap_vs_oracle():
+    """The shared-set diagnostic on the device (the library's score and
+    select per draft) equals the oracle's overlaps."""
+    from sparse_verification_attention_gb300 import diagnostics
+    wl = small_wl(B=2, ctx=64 * 40, T=8)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    k = 10
+    got = diagnostics.draft_selection_overlap(st.shape, xd.q, st.reps, st.kv, k)
+    reps = O.block_representatives(x.k_pool, x.block_table, wl.NB, wl.blk)
+    want = O.draft_selection_overlap(x.q, reps, wl.G, k)
+    assert got.shape == want.shape
+    assert torch.all(got[:, :, 0] == 1.0)
+    # selections match bit-exactly away from near-ties, so the overlaps agree
+    # to within one block
+    assert (got - want).abs().max().item() <= 1.0 / k + 1e-12
+    assert (got - want).abs().mean().item() < 0.02
