@@ -231,7 +231,12 @@ sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_p
  *               selection already in sel_cache (written by an earlier
  *               reuse == 0 call with the same shape, kv->ctx and budget) is
  *               attended to as is.
- * reps may be NULL when reuse == 1. sel_cache: [B, Hkv, kmax] int32, in/out.
+ *   reuse == 2: full verification [SpecPV] -- every block of the context is
+ *               attended (as sv_sparse_attend with sel == NULL), for the
+ *               periodic full-verification steps that partial verification
+ *               interleaves; reps, budget and sel_cache are not used (may be
+ *               NULL) and sel_cache keeps its contents.
+ * reps may be NULL when reuse != 0. sel_cache: [B, Hkv, kmax] int32, in/out.
  * *k_out (host, may be NULL) receives the number of blocks attended. */
 sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           const float* reps, const sv_budget* budget,

@@ -259,6 +259,26 @@ def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: W.Budget, draft_k, dr
 
 
 # ------------------------------------------------------------ convenience
+VERIFY_COMPUTE, VERIFY_REUSE, VERIFY_FULL = 0, 1, 2  # sv_verify_layer's reuse values
+
+
+class VerifySchedule:
+    """Which sv_verify_layer mode a (step, layer) runs: every `full_period`-th
+    step is a full verification over every block (the periodic full steps that
+    partial verification interleaves; 0 = never); in the other steps layer l
+    recomputes its selection when l % compute_every == 0 and reuses the last
+    one otherwise."""
+
+    def __init__(self, full_period: int = 0, compute_every: int = 1):
+        if full_period < 0 or compute_every < 1:
+            raise ValueError("full_period >= 0 and compute_every >= 1")
+        self.full_period = full_period
+        self.compute_every = compute_every
+
+    def mode(self, step: int, layer: int = 0) -> int:
+        if self.full_period and step % self.full_period == self.full_period - 1:
+            return VERIFY_FULL
+        return VERIFY_COMPUTE if layer % self.compute_every == 0 else VERIFY_REUSE
 class LayerState:
     """Device-resident state of one verification layer: the paged KV cache,
     its block representatives, a selection cache slot and a workspace.

@@ -691,8 +691,22 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
-  if (reuse != 0 && reuse != 1) return fail(SV_ERR_INVALID_ARG, "reuse=%d must be 0 or 1", reuse);
+  if (reuse < 0 || reuse > 2)
+    return fail(SV_ERR_INVALID_ARG, "reuse=%d must be 0, 1 or 2", reuse);
   const int nb = kv->ctx / shape->blk;
+  if (reuse == 2) {
+    // full verification: every block, no scoring, selection or budget
+    if (!q || !draft_k || !draft_v || !out)
+      return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out is NULL");
+    if (!aligned(q, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16) || !aligned(out, 16))
+      return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out must be 16-byte aligned");
+    if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
+    WsLayout L;
+    if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+    if (k_out) *k_out = nb;
+    return run_attend(shape, q, kv, nullptr, nb, nb, draft_k, draft_v, draft_parent, out,
+                      workspace, L, (cudaStream_t)stream);
+  }
   const int k = budget_blocks(budget, kv->ctx, nb);
   if (k < 0) return fail(SV_ERR_INVALID_ARG, "invalid budget");
   if (k > kmax) return fail(SV_ERR_INVALID_ARG, "budget k=%d exceeds kmax=%d", k, kmax);

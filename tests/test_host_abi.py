@@ -138,7 +138,7 @@ def test_invalid_arguments_rejected_before_launch(L):
                       bad_par, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "draft_parent" in msg
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), fake, C.byref(b), fake,
-                      fake, None, 2, fake, 8, None, fake, fake, ws_n, None)
+                      fake, None, 3, fake, 8, None, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "reuse" in msg
     big_t = api.make_shape(1, 4, 2, 64, 16, 65, torch.float32)
     st, msg = _status(L, L.sv_sparse_attend, C.byref(big_t), fake, C.byref(kv), fake, 8, 8, fake,
@@ -153,3 +153,28 @@ def test_invalid_arguments_rejected_before_launch(L):
     st, msg = _status(L, L.sv_append_kv, C.byref(s), fake + 4, fake, fake, 64, 64, fake, fake, fake,
                       fake, fake, None, None, None)
     assert st == api.SV_ERR_INVALID_ARG and "aligned" in msg
+
+
+def test_verify_schedule():
+    s = api.VerifySchedule(full_period=4, compute_every=2)
+    modes = [[s.mode(step, layer) for layer in range(4)] for step in range(8)]
+    assert modes[3] == modes[7] == [api.VERIFY_FULL] * 4          # every 4th step is full
+    assert modes[0] == [api.VERIFY_COMPUTE, api.VERIFY_REUSE] * 2  # otherwise compute / reuse
+    assert api.VerifySchedule().mode(5, 3) == api.VERIFY_COMPUTE
+    with pytest.raises(ValueError):
+        api.VerifySchedule(compute_every=0)
+
+
+def test_verify_full_mode_needs_no_selection_buffers(L):
+    """reuse = 2 (full verification) validates without reps, budget or
+    sel_cache; reuse = 3 is rejected."""
+    s = api.make_shape(1, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20
+    kv = api.KV(fake, fake, fake, 64, 64, 1024)
+    ws_n = api.sv_workspace_bytes(s, 64, 8)
+    st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, None, fake,
+                      fake, None, 3, None, 0, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "reuse" in msg
+    st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, None, fake,
+                      fake, None, 2, None, 8, None, fake, fake, ws_n - 1, None)
+    assert st == api.SV_ERR_WORKSPACE, msg  # got past every selection check

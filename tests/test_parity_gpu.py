@@ -633,3 +633,21 @@ def test_draft_selection_overlap_vs_oracle():
     # to within one block
     assert (got - want).abs().max().item() <= 1.0 / k + 1e-12
     assert (got - want).abs().mean().item() < 0.02
+
+
+def test_verify_full_mode_equals_dense():
+    """sv_verify_layer(reuse = 2): full verification over every block and the
+    partial one, against the oracle's dense attention; sel_cache untouched."""
+    wl = small_wl(B=3, Hq=8, Hkv=2, ctx=64 * 22 + 30)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, kmax=wl.NB, build_reps=False)
+    st.sel.fill_(-7)
+    out = st.verify(reuse=api.VERIFY_FULL)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    assert int((st.sel != -7).sum()) == 0
+    ref = O.dense_verify_attention(x.q, O.logical_kv_tokens(x.k_pool, x.block_table, wl.ctx),
+                                   O.logical_kv_tokens(x.v_pool, x.block_table, wl.ctx), x.draft_k,
+                                   x.draft_v, wl.parent_list())
+    U.compare_out(out, ref, U.BF16_ATOL)
