@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 2
+#define SV_ABI_VERSION 3
 
 typedef enum {
   SV_OK = 0,
@@ -94,8 +94,9 @@ typedef struct {
 
 /* Paged KV cache, caller-owned device memory. Page p of head h holds blk
  * consecutive tokens: k_pool[p][h][0..blk)[0..d). Every sequence has ctx
- * prefix tokens: NB = ctx/blk full blocks and, when ctx % blk != 0, a
- * partial last block (logical block NB, its first ctx % blk tokens). Logical
+ * prefix tokens, or seq_ctx[b] when seq_ctx is given: NB = ctx/blk full
+ * blocks and, when ctx % blk != 0, a partial last block (logical block NB,
+ * its first ctx % blk tokens). Logical
  * block j of sequence b lives in page block_table[b * nb_max + j]. Only full
  * blocks have representatives and compete for the budget; a partial last
  * block is always attended, outside the budget (this library's reading of
@@ -108,6 +109,13 @@ typedef struct {
   int nb_max;               /* row stride of block_table, >= ceil(ctx/blk) */
   int num_pages;
   int ctx;                  /* prefix tokens per sequence (same for all)   */
+  /* Per-sequence prefix lengths, HOST memory, B entries (B <= 64), or NULL
+   * for the uniform ctx above (which is then ignored when non-NULL). Read
+   * during the call only; the caller keeps ownership. With per-sequence
+   * lengths every budget is taken per sequence (the piecewise rule of each
+   * sequence's own ctx), sel rows hold k_b valid entries followed by -1, and
+   * nb_max must cover the longest sequence. */
+  const int32_t* seq_ctx;
 } sv_kv;
 
 /* ABI version (SV_ABI_VERSION of the built library). Host only. */

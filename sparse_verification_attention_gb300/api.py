@@ -25,7 +25,7 @@ SV_BF16, SV_F32 = 0, 1
 SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
 
 SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
-ABI_VERSION = 2  # SV_ABI_VERSION the structures below match
+ABI_VERSION = 3  # SV_ABI_VERSION the structures below match
 
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
@@ -52,7 +52,8 @@ class BudgetC(C.Structure):
 
 class KV(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("block_table", C.c_void_p),
-                ("nb_max", C.c_int), ("num_pages", C.c_int), ("ctx", C.c_int)]
+                ("nb_max", C.c_int), ("num_pages", C.c_int), ("ctx", C.c_int),
+                ("seq_ctx", C.POINTER(C.c_int32))]
 
 
 class Plan(C.Structure):
@@ -140,9 +141,17 @@ def make_budget(b: W.Budget) -> BudgetC:
 
 
 def make_kv(k_pool: torch.Tensor, v_pool: Optional[torch.Tensor], block_table: torch.Tensor,
-            ctx: int) -> KV:
-    return KV(k_pool.data_ptr(), None if v_pool is None else v_pool.data_ptr(),
-              block_table.data_ptr(), block_table.shape[1], k_pool.shape[0], ctx)
+            ctx: int, seq_ctx: Optional[Sequence[int]] = None) -> KV:
+    """The cache descriptor. seq_ctx (one prefix length per sequence, kept on
+    the host) replaces the uniform ctx; the returned structure owns the
+    array it points to."""
+    kv = KV(k_pool.data_ptr(), None if v_pool is None else v_pool.data_ptr(),
+            block_table.data_ptr(), block_table.shape[1], k_pool.shape[0], ctx)
+    if seq_ctx is not None:
+        arr = (C.c_int32 * len(seq_ctx))(*[int(c) for c in seq_ctx])
+        kv._seq_ctx_keep = arr
+        kv.seq_ctx = C.cast(arr, C.POINTER(C.c_int32))
+    return kv
 
 
 def _parents(parents: Optional[Sequence[int]]):
@@ -288,12 +297,16 @@ class LayerState:
     """
 
     def __init__(self, wl: W.Workload, x: W.LayerInputs, kmax: Optional[int] = None,
-                 build_reps: bool = True, stream=None):
+                 build_reps: bool = True, stream=None, seq_ctx: Optional[Sequence[int]] = None):
+        """seq_ctx: one prefix length per sequence (each at most wl.ctx, the
+        length the block table is laid out for); wl.ctx for all when None."""
         self.wl, self.x = wl, x
         self.shape = make_shape(wl.B, wl.Hq, wl.Hkv, wl.d, wl.blk, wl.T, wl.torch_dtype)
-        self.kv = make_kv(x.k_pool, x.v_pool, x.block_table, wl.ctx)
+        self.kv = make_kv(x.k_pool, x.v_pool, x.block_table, wl.ctx, seq_ctx)
         nb = wl.NB
-        self.k = sv_budget_blocks(wl.budget, wl.ctx, nb)
+        ctxs = [wl.ctx] if seq_ctx is None else list(seq_ctx)
+        # the largest per-sequence budget: the selection rows' valid prefix
+        self.k = max(sv_budget_blocks(wl.budget, c, c // wl.blk) for c in ctxs) if ctxs else 0
         self.kmax = self.k if kmax is None else kmax
         dev = x.q.device
         # [B, Hkv, nb_max, d]: the calls index representatives with the block

@@ -184,13 +184,15 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
   const int pair = b * a.Hkv + h;
   // Work units of this (b, h): the n_sel selected blocks, the partial last
   // block (unit n_sel, if any), then the draft tile.
-  const int ntail = a.tail > 0 ? 1 : 0;
+  const int nsel = n_of(a.vl, b, a.n_sel), nbb = nb_of(a.vl, b, a.nb);
+  const int tail = tail_of(a.vl, b, a.tail);
+  const int ntail = tail > 0 ? 1 : 0;
   const int u0 = split * a.bps;
-  const int u1 = min(a.n_sel + ntail + 1, u0 + a.bps);
+  const int u1 = min(nsel + ntail + 1, u0 + a.bps);
   const int j0 = u0;
-  const int nblk = max(0, min(u1, a.n_sel) - u0);
-  const bool has_tail = ntail && u0 <= a.n_sel && a.n_sel < u1;
-  const bool has_draft = (u0 <= a.n_sel + ntail && a.n_sel + ntail < u1);
+  const int nblk = max(0, min(u1, nsel) - u0);
+  const bool has_tail = ntail && u0 <= nsel && nsel < u1;
+  const bool has_draft = (u0 <= nsel + ntail && nsel + ntail < u1);
   const int nring = nblk + (has_tail ? 1 : 0);  // tiles through the ring
 
   if (threadIdx.x == 0) {
@@ -221,10 +223,10 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
       if (base + lane < nring) {
         // the partial last block rides after the selected ones (stage_ok 2)
         const bool tailu = base + lane == nblk;
-        const int j = tailu ? a.nb
+        const int j = tailu ? nbb
                             : a.sel ? a.sel[(size_t)pair * a.sel_stride + j0 + base + lane]
                                     : j0 + base + lane;
-        if (!tailu && (j < 0 || j >= a.nb)) {
+        if (!tailu && (j < 0 || j >= nbb)) {
           atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
         } else {
           const int page = a.block_table[(size_t)b * a.nb_max + j];
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(32 * (NWC + 1))
       }
       if (stage_ok[s]) {
         const uint32_t kb = sbase + s * C::kStageBytes;
-        cs.tile(kb, kb + C::kTileBytes, a, false, stage_ok[s] == 2 ? a.tail : BLK, lane);
+        cs.tile(kb, kb + C::kTileBytes, a, false, stage_ok[s] == 2 ? tail : BLK, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));

@@ -64,12 +64,14 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
   const int pair = b * a.Hkv + h;
   // work units: the n_sel selected blocks, the partial last block (unit
   // n_sel, if any), then the draft tile
-  const int ntail = a.tail > 0 ? 1 : 0;
+  const int nsel = n_of(a.vl, b, a.n_sel), nbb = nb_of(a.vl, b, a.nb);
+  const int tail = tail_of(a.vl, b, a.tail);
+  const int ntail = tail > 0 ? 1 : 0;
   const int u0 = split * a.bps;
-  const int u1 = min(a.n_sel + ntail + 1, u0 + a.bps);
-  const int j0 = u0, j1 = min(u1, a.n_sel);
-  const bool has_tail = ntail && u0 <= a.n_sel && a.n_sel < u1;
-  const bool has_draft = (u0 <= a.n_sel + ntail && a.n_sel + ntail < u1);
+  const int u1 = min(nsel + ntail + 1, u0 + a.bps);
+  const int j0 = u0, j1 = min(u1, nsel);
+  const bool has_tail = ntail && u0 <= nsel && nsel < u1;
+  const bool has_draft = (u0 <= nsel + ntail && nsel + ntail < u1);
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
   const T* q = static_cast<const T*>(a.q);
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
     st.l = 0.f;
     for (int jj = j0; jj < j1; ++jj) {
       const int j = a.sel ? a.sel[(size_t)pair * a.sel_stride + jj] : jj;
-      if (j < 0 || j >= a.nb) {
+      if (j < 0 || j >= nbb) {
         if (lane == 0) atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
         continue;
       }
@@ -108,12 +110,12 @@ __global__ void __launch_bounds__(128) attend_generic_kernel(const __grid_consta
                   a.scale_log2, lane);
     }
     if (has_tail) {
-      const int page = a.block_table[(size_t)b * a.nb_max + a.nb];
+      const int page = a.block_table[(size_t)b * a.nb_max + nbb];
       if (page < 0 || page >= a.num_pages) {
         if (lane == 0) atomicOr(a.status, SV_FLAG_BAD_PAGE);
       } else {
         const size_t base = ((size_t)page * a.Hkv + h) * a.blk * a.d;
-        for (int x = 0; x < a.tail; ++x)
+        for (int x = 0; x < tail; ++x)
           absorb<T>(st, kp + base + (size_t)x * a.d, vp + base + (size_t)x * a.d, a.d,
                     a.scale_log2, lane);
       }

@@ -138,11 +138,14 @@ __device__ SegPlan plan_segments(const AttendArgs& a) {
   } else {
     int pair, split, nsp;
     split_of_cta(c, a.n_splits, a.split_extra, &pair, &split, &nsp);
-    const int bps = (W + nsp - 1) / nsp;
+    // this pair's units (sequences may differ in selected blocks and tail)
+    const int bq = pair / a.Hkv;
+    const int Wp = n_of(a.vl, bq, a.n_sel) + (tail_of(a.vl, bq, a.tail) > 0 ? 1 : 0) + 1;
+    const int bps = (Wp + nsp - 1) / nsp;
     sp.n = 1;
     sp.pair[0] = pair;
-    sp.u0[0] = min(W, split * bps);
-    sp.u1[0] = min(W, sp.u0[0] + bps);
+    sp.u0[0] = min(Wp, split * bps);
+    sp.u1[0] = min(Wp, sp.u0[0] + bps);
     sp.slot[0] = split;
     sp.nseg[0] = nsp;
     sp.mid[0] = 0;
@@ -290,13 +293,15 @@ __global__ void __launch_bounds__(32 * 10, 1)
     int i = 0;  // tile index over all segments
     for (int j = 0; j < sp.n && !stop; ++j) {
       const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+      const int nsel = n_of(a.vl, b, a.n_sel), nbb = nb_of(a.vl, b, a.nb);
+      const int tail = tail_of(a.vl, b, a.tail);
       const int ub = sp.u0[j];
-      const int nblk = max(0, min(sp.u1[j], a.n_sel) - ub);
+      const int nblk = max(0, min(sp.u1[j], nsel) - ub);
       for (int base = 0; base < nblk && !stop; base += 32) {
         int row = oob_row, ok = 0;
         if (base + lane < nblk) {
           const int jb = a.sel ? a.sel[(size_t)pair * a.sel_stride + ub + base + lane] : ub + base + lane;
-          if (jb < 0 || jb >= a.nb) {
+          if (jb < 0 || jb >= nbb) {
             atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
           } else {
             const int page = a.block_table[(size_t)b * a.nb_max + jb];
@@ -337,17 +342,17 @@ __global__ void __launch_bounds__(32 * 10, 1)
           }
         }
       }
-      if (a.tail > 0 && sp.u0[j] <= a.n_sel && a.n_sel < sp.u1[j] && !stop) {
+      if (tail > 0 && sp.u0[j] <= nsel && nsel < sp.u1[j] && !stop) {
         // the partial last block: a full page copy, of which the softmax keeps
         // the first `tail` columns (stage_info bits 8..15)
         int rq = oob_row, okq = 0;
         if (lane == 0) {
-          const int page = a.block_table[(size_t)b * a.nb_max + a.nb];
+          const int page = a.block_table[(size_t)b * a.nb_max + nbb];
           if (page < 0 || page >= a.num_pages) {
             atomicOr(a.status, SV_FLAG_BAD_PAGE);
           } else {
             rq = (page * a.Hkv + h) * TBLK;
-            okq = 1 | (a.tail << 8);
+            okq = 1 | (tail << 8);
           }
         }
         int fail = 0;
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         if (__shfl_sync(0xffffffffu, fail, 0)) stop = true;
         ++i;
       }
-      const int ud = a.n_sel + (a.tail > 0 ? 1 : 0);  // the draft tile's unit
+      const int ud = nsel + (tail > 0 ? 1 : 0);  // the draft tile's unit
       if (sp.u0[j] <= ud && ud < sp.u1[j] && !stop) {
         // draft tile: this pair's draft rows t < T by TMA like any page; rows
         // T..63 lie outside the draft tensor and arrive as zeros (the softmax

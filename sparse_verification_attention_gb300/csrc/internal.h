@@ -53,12 +53,23 @@ struct WsLayout {
 WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax);
 
 // ---------------------------------------------------------------- kernels
+// Per-sequence counts of a call whose sequences have different contexts
+// (on = 0: every sequence uses the call's uniform values).
+constexpr int kMaxVarB = 64;  // sequences of such a call
+struct VarLen {
+  int on;
+  int nb[kMaxVarB];    // full blocks of sequence b
+  int tail[kMaxVarB];  // tokens of its partial last block
+  int n[kMaxVarB];     // blocks it selects / attends
+};
+
 struct RepsArgs {
   const void* k_pool;
   const int32_t* block_table;
   float* reps;
   int B, Hkv, d, blk, nb_max, num_pages, first_block, n_blocks;
   unsigned* status;  // may be null (sv_build_reps has no workspace)
+  VarLen vl;         // per-sequence full blocks: blocks past them are skipped
 };
 cudaError_t launch_build_reps(const RepsArgs& a, int dtype, cudaStream_t st);
 
@@ -92,6 +103,7 @@ struct ScoreArgs {
   int32_t* sel;
   int k, kmax;
   unsigned* counters;  // [B*Hkv], zero between calls
+  VarLen vl;           // per-sequence nb (rows) and k; score rows keep stride nb
 };
 cudaError_t launch_score(ScoreArgs a, int dtype, cudaStream_t st);
 // Largest block count whose selection the score kernel fuses (its 256
@@ -102,6 +114,8 @@ struct SelectArgs {
   const float* scores;
   int32_t* sel;
   int pairs, nb, k, kmax;
+  int Hkv;             // pairs are (b, h) with b = pair / Hkv
+  VarLen vl;           // per-sequence nb and k; score rows keep stride nb
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
@@ -135,7 +149,27 @@ struct AttendArgs {
   int streamk;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
+  VarLen vl;  // per-sequence nb, tail and n_sel (on = 0: the uniform ones)
 };
+
+// The contexts of one call: uniform (var = false) or per sequence.
+struct Ctxs {
+  bool var;
+  int nb, nb_min;  // largest and smallest full-block counts over sequences
+  int tail;        // partial-block tokens (uniform contexts)
+  VarLen vl;       // per sequence: nb and tail (n left to the caller)
+};
+
+// The counts of sequence b under a VarLen block (uniform values when off).
+__host__ __device__ inline int nb_of(const VarLen& v, int b, int uniform) {
+  return v.on ? v.nb[b] : uniform;
+}
+__host__ __device__ inline int tail_of(const VarLen& v, int b, int uniform) {
+  return v.on ? v.tail[b] : uniform;
+}
+__host__ __device__ inline int n_of(const VarLen& v, int b, int uniform) {
+  return v.on ? v.n[b] : uniform;
+}
 
 // CTA c of a 1-D grid under the non-uniform split map -> (pair, split, splits
 // of that pair).

@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(kRepThreads) build_reps_kernel(RepsArgs a) {
   __shared__ float part[kRepThreads * (16 / sizeof(T))];
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
-  block_rep<T>(a, blockIdx.z, blockIdx.y, a.first_block + blockIdx.x, part);
+  const int b = blockIdx.z, j = a.first_block + blockIdx.x;
+  if (a.vl.on && j >= a.vl.nb[b]) return;  // past this sequence's full blocks
+  block_rep<T>(a, b, blockIdx.y, j, part);
 }
 
 // After an append: grid (B, most blocks one append can complete, Hkv); CTA
@@ -144,12 +146,20 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   const int b = pair / a.Hkv, h = pair % a.Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nchunk = a.d / 4;
+  const int nbb = nb_of(a.vl, b, a.nb);  // this sequence's blocks (rows keep stride nb)
   const int r0 = blockIdx.x * a.rows_per_cta;
-  const int r1 = min(a.nb, r0 + a.rows_per_cta);
+  const int r1 = min(nbb, r0 + a.rows_per_cta);
   const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
   float* srow = a.scores + (size_t)pair * a.nb;
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
+  if (r0 >= nbb) {
+    // past this sequence's blocks: no rows, no arrival; a sequence without
+    // full blocks gets an empty selection from its first CTA
+    if (nbb == 0 && blockIdx.x == 0 && a.sel && a.nb <= kFusedSelectMaxNB)
+      for (int i = threadIdx.x; i < a.kmax; i += kScoreThreads) a.sel[(size_t)pair * a.kmax + i] = -1;
+    return;
+  }
 
   float4 qh[CH];
   bool have_q = false;
@@ -221,12 +231,14 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   __shared__ TopkSmem<kScoreThreads> tsm;
   __syncthreads();
   if (threadIdx.x == 0) {
-    const bool last = arrive_acq_rel(&a.counters[pair]) == gridDim.x - 1;
+    const unsigned ctas = (unsigned)((nbb + a.rows_per_cta - 1) / a.rows_per_cta);
+    const bool last = arrive_acq_rel(&a.counters[pair]) == ctas - 1;
     s_last = last;
   }
   __syncthreads();
   if (s_last) {
-    cta_topk<kScoreThreads, kScoreKeys>(srow, a.nb, a.k, a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
+    cta_topk<kScoreThreads, kScoreKeys>(srow, nbb, n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax,
+                                        a.kmax, tsm);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
 }

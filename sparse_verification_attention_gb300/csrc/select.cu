@@ -25,9 +25,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const __grid_con
   __shared__ TopkSmem<kSelThreads> tsm;
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
-  const int pair = blockIdx.x;
-  cta_topk<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, a.nb, a.k,
-                                  a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
+  const int pair = blockIdx.x, b = pair / a.Hkv;
+  cta_topk<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, nb_of(a.vl, b, a.nb),
+                                  n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
 }
 
 }  // namespace

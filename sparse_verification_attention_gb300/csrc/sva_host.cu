@@ -67,13 +67,26 @@ sv_status check_shape(const sv_shape* s) {
 
 sv_status check_kv(const sv_shape* s, const sv_kv* kv, bool need_v) {
   if (!kv) return fail(SV_ERR_INVALID_ARG, "kv is NULL");
-  if (kv->ctx < 0) return fail(SV_ERR_INVALID_ARG, "ctx=%d is negative", kv->ctx);
-  const int nb = kv->ctx / s->blk;                       // full blocks
-  const int nblocks = (kv->ctx + s->blk - 1) / s->blk;   // with a partial last one
+  int nb = 0, nblocks = 0;  // the largest over the sequences
+  if (kv->seq_ctx) {
+    if (s->B > kMaxVarB)
+      return fail(SV_ERR_UNSUPPORTED, "B=%d sequences with per-sequence ctx exceeds %d", s->B,
+                  kMaxVarB);
+    for (int b = 0; b < s->B; ++b) {
+      const int c = kv->seq_ctx[b];
+      if (c < 0) return fail(SV_ERR_INVALID_ARG, "seq_ctx[%d]=%d is negative", b, c);
+      nb = std::max(nb, c / s->blk);
+      nblocks = std::max(nblocks, (c + s->blk - 1) / s->blk);
+    }
+  } else {
+    if (kv->ctx < 0) return fail(SV_ERR_INVALID_ARG, "ctx=%d is negative", kv->ctx);
+    nb = kv->ctx / s->blk;                        // full blocks
+    nblocks = (kv->ctx + s->blk - 1) / s->blk;    // with a partial last one
+  }
   if (nb > kMaxNB) return fail(SV_ERR_UNSUPPORTED, "NB=%d blocks exceeds %d", nb, kMaxNB);
   if (kv->nb_max < nblocks)
-    return fail(SV_ERR_INVALID_ARG, "nb_max=%d < %d blocks holding ctx=%d", kv->nb_max, nblocks,
-                kv->ctx);
+    return fail(SV_ERR_INVALID_ARG, "nb_max=%d < %d blocks holding the context", kv->nb_max,
+                nblocks);
   if (nblocks > 0) {
     if (!kv->k_pool || (need_v && !kv->v_pool) || !kv->block_table)
       return fail(SV_ERR_INVALID_ARG, "k_pool/v_pool/block_table is NULL");
@@ -84,6 +97,29 @@ sv_status check_kv(const sv_shape* s, const sv_kv* kv, bool need_v) {
       return fail(SV_ERR_UNSUPPORTED, "pool of %d pages is too large", kv->num_pages);
   }
   return SV_OK;
+}
+
+// Full blocks and partial-block tokens of every sequence of a (validated)
+// cache: uniform, or per sequence when kv->seq_ctx is given.
+Ctxs ctxs_of(const sv_shape* s, const sv_kv* kv) {
+  Ctxs c{};
+  c.var = kv->seq_ctx != nullptr;
+  c.vl.on = c.var ? 1 : 0;
+  if (!c.var) {
+    c.nb = c.nb_min = kv->ctx / s->blk;
+    c.tail = kv->ctx % s->blk;
+    return c;
+  }
+  c.nb_min = 1 << 30;
+  for (int b = 0; b < s->B; ++b) {
+    const int x = kv->seq_ctx[b];
+    c.vl.nb[b] = x / s->blk;
+    c.vl.tail[b] = x % s->blk;
+    c.nb = std::max(c.nb, c.vl.nb[b]);
+    c.nb_min = std::min(c.nb_min, c.vl.nb[b]);
+  }
+  if (s->B == 0) c.nb_min = 0;
+  return c;
 }
 
 int budget_blocks(const sv_budget* bd, int ctx, int nb) {
@@ -301,7 +337,13 @@ static int streamk_slots(int pairs, int W, int G) {
 
 static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int max_slots) {
   AttendPlan p{};
-  const int n_units = n_sel + (a.tail > 0 ? 1 : 0) + 1;  // blocks, partial block, drafts
+  // units of the largest pair: blocks, partial block, drafts
+  int n_units = n_sel + (a.tail > 0 ? 1 : 0) + 1;
+  if (a.vl.on) {
+    n_units = 1;
+    for (int b = 0; b < a.B; ++b)
+      n_units = std::max(n_units, a.vl.n[b] + (a.vl.tail[b] > 0 ? 1 : 0) + 1);
+  }
   const bool tcp = attend_tc_applies(a, dtype);
   const bool fast = !tcp && attend_fast_applies(a, dtype);
   p.path = tcp ? SV_PATH_TCGEN05 : fast ? SV_PATH_MMA_SYNC : SV_PATH_CUDA_CORES;
@@ -310,7 +352,8 @@ static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int 
     // some pairs getting one split more than others
     p.per_sm = attend_tc_ctas_per_sm(a);
     const int slots = sm_count() * (p.per_sm > 0 ? p.per_sm : 1);
-    const int sk = streamk_slots(pairs, n_units, slots);
+    // stream-K cuts equal runs of equal-length pairs: uniform contexts only
+    const int sk = a.vl.on ? 0 : streamk_slots(pairs, n_units, slots);
     if (sk > 0 && sk <= max_slots) {
       p.streamk = 1;
       p.n_splits = slots;
@@ -353,12 +396,20 @@ static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_
                       const int32_t* sel, int n_sel, int sel_stride, const void* dk,
                       const void* dv, const int32_t* parent, void* ws, const WsLayout& L);
 
+static void set_nsel(AttendArgs& a, const int* nsel_b) {
+  // per-sequence selected counts: given, else the call's n_sel (a selection
+  // passed in) or every full block (sel == NULL)
+  if (!a.vl.on) return;
+  for (int b = 0; b < a.B; ++b) a.vl.n[b] = nsel_b ? nsel_b[b] : a.sel ? a.n_sel : a.vl.nb[b];
+}
+
 static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, const int32_t* sel,
                             int n_sel, int sel_stride, const void* dk, const void* dv,
                             const int32_t* parent, void* out, void* ws, const WsLayout& L,
-                            cudaStream_t st) {
+                            cudaStream_t st, const int* nsel_b = nullptr) {
   AttendArgs a{};
   fill_args(a, s, q, kv, sel, n_sel, sel_stride, dk, dv, parent, ws, L);
+  set_nsel(a, nsel_b);
   a.out = out;
   const AttendPlan p = make_plan(a, s->dtype, s->B * s->Hkv, n_sel, L.slots);
   a.n_splits = p.n_splits;
@@ -408,8 +459,10 @@ static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_
   a.blk = s->blk;
   a.R = s->T * a.G;
   a.rpad = L.rpad;
-  a.nb = kv->ctx / s->blk;
-  a.tail = kv->ctx % s->blk;
+  const Ctxs c = ctxs_of(s, kv);
+  a.nb = c.nb;      // the largest sequence's full blocks
+  a.tail = c.tail;  // uniform contexts (per sequence in a.vl otherwise)
+  a.vl = c.vl;
   a.nb_max = kv->nb_max;
   a.num_pages = kv->num_pages;
   a.n_sel = n_sel;
@@ -430,21 +483,24 @@ static sv_status check_ws(const sv_shape* s, int nb_max, int kmax, const void* w
 
 static sv_status do_score_select(const sv_shape* s, const void* q, const float* reps,
                                  const sv_kv* kv, int k, int32_t* sel, int kmax, void* ws,
-                                 const WsLayout& L, cudaStream_t st) {
-  const int nb = kv->ctx / s->blk;
+                                 const WsLayout& L, cudaStream_t st, const int* k_b = nullptr) {
+  Ctxs c = ctxs_of(s, kv);
+  const int nb = c.nb;  // the largest sequence's (score rows keep this stride)
+  if (c.vl.on)
+    for (int b = 0; b < s->B; ++b) c.vl.n[b] = k_b[b];
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(w + L.scores);
   cudaError_t e;
   if (nb == 0) {
     // nothing to score: the selection is empty
-    SelectArgs se{scores, sel, s->B * s->Hkv, 0, 0, kmax};
+    SelectArgs se{scores, sel, s->B * s->Hkv, 0, 0, kmax, s->Hkv, c.vl};
     e = launch_select(se, st);
   } else {
     ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max,
-                 0, sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score)};
+                 0, sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score), c.vl};
     e = launch_score(sa, s->dtype, st);
     if (e == cudaSuccess && nb > kFusedSelectMaxNB) {  // too many keys to fuse
-      SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax};
+      SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax, s->Hkv, c.vl};
       e = launch_select(se, st);
     }
   }
@@ -504,6 +560,19 @@ static WsLayout noalloc_layout(const sv_shape& s, int rpad, int slot_stride) {
   return L;
 }
 
+// The budget of every sequence (k_b[b], per-sequence contexts only) and
+// the largest one; -1 for an invalid rule.
+static int budgets_of(const sv_budget* bd, const sv_kv* kv, const Ctxs& c, int B, int* k_b) {
+  if (!c.var) return budget_blocks(bd, kv->ctx, c.nb);
+  int k = 0;
+  for (int b = 0; b < B; ++b) {
+    k_b[b] = budget_blocks(bd, kv->seq_ctx[b], c.vl.nb[b]);
+    if (k_b[b] < 0) return -1;
+    k = std::max(k, k_b[b]);
+  }
+  return k;
+}
+
 }  // namespace sva
 
 using namespace sva;
@@ -546,14 +615,15 @@ sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block,
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
-  const int nb = kv->ctx / shape->blk;
+  const Ctxs c = ctxs_of(shape, kv);
+  const int nb = c.nb;  // blocks past a shorter sequence's own are skipped
   if (first_block < 0 || n_blocks < 0 || first_block + n_blocks > nb)
     return fail(SV_ERR_INVALID_ARG, "blocks [%d, %d) outside [0, %d)", first_block,
                 first_block + n_blocks, nb);
   if (n_blocks == 0) return SV_OK;
   if (!reps || !aligned(reps, 16)) return fail(SV_ERR_INVALID_ARG, "reps NULL or not 16-byte aligned");
   RepsArgs a{kv->k_pool, kv->block_table, reps, shape->B, shape->Hkv, shape->d, shape->blk,
-             kv->nb_max, kv->num_pages, first_block, n_blocks, nullptr};
+             kv->nb_max, kv->num_pages, first_block, n_blocks, nullptr, c.vl};
   cudaError_t e = launch_build_reps(a, shape->dtype, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "build_reps launch");
 }
@@ -594,13 +664,14 @@ sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* rep
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
-  const int nb = kv->ctx / shape->blk;
+  const Ctxs c = ctxs_of(shape, kv);
+  const int nb = c.nb;
   if (nb == 0) return SV_OK;
   if (!q || !reps || !scores) return fail(SV_ERR_INVALID_ARG, "q/reps/scores is NULL");
   if (!aligned(q, 16) || !aligned(reps, 16))
     return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
   ScoreArgs sa{q, reps, scores, shape->B, shape->T, shape->Hq, shape->Hkv,
-               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, 0, nullptr, 0, 0, nullptr};
+               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, 0, nullptr, 0, 0, nullptr, c.vl};
   cudaError_t e = launch_score(sa, shape->dtype, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "score launch");
 }
@@ -613,7 +684,7 @@ sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, i
   if (k < 0 || k > kmax) return fail(SV_ERR_INVALID_ARG, "k=%d outside [0, kmax=%d]", k, kmax);
   if (kmax == 0) return SV_OK;
   if (!sel || (nb > 0 && !scores)) return fail(SV_ERR_INVALID_ARG, "scores/sel is NULL");
-  SelectArgs se{scores, sel, shape->B * shape->Hkv, nb, k, kmax};
+  SelectArgs se{scores, sel, shape->B * shape->Hkv, nb, k, kmax, shape->Hkv, VarLen{}};
   cudaError_t e = launch_select(se, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "select launch");
 }
@@ -624,8 +695,10 @@ sv_status sv_score_select(const sv_shape* shape, const void* q, const float* rep
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
-  const int nb = kv->ctx / shape->blk;
-  const int k = budget_blocks(budget, kv->ctx, nb);
+  const Ctxs c = ctxs_of(shape, kv);
+  const int nb = c.nb;
+  int k_b[kMaxVarB];
+  const int k = budgets_of(budget, kv, c, shape->B, k_b);
   if (k < 0) return fail(SV_ERR_INVALID_ARG, "invalid budget");
   if (k > kmax) return fail(SV_ERR_INVALID_ARG, "budget k=%d exceeds kmax=%d", k, kmax);
   if (kmax > 0 && !sel) return fail(SV_ERR_INVALID_ARG, "sel is NULL");
@@ -636,7 +709,8 @@ sv_status sv_score_select(const sv_shape* shape, const void* q, const float* rep
   if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
   if (k_out) *k_out = k;
   if (kmax == 0) return SV_OK;
-  return do_score_select(shape, q, reps, kv, k, sel, kmax, workspace, L, (cudaStream_t)stream);
+  return do_score_select(shape, q, reps, kv, k, sel, kmax, workspace, L, (cudaStream_t)stream,
+                         k_b);
 }
 
 sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv, const int32_t* sel,
@@ -646,7 +720,7 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
-  const int nb = kv->ctx / shape->blk;
+  const int nb = ctxs_of(shape, kv).nb;  // sel == NULL: each sequence's own blocks
   if (!sel) {
     n_sel = nb;
     sel_stride = nb;
@@ -673,6 +747,8 @@ sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_p
   const WsLayout L = ws_layout(*shape, kv->nb_max, n_sel);
   AttendArgs a{};
   fill_args(a, shape, nullptr, kv, nullptr, n_sel, n_sel, nullptr, nullptr, nullptr, nullptr, L);
+  if (a.vl.on)
+    for (int b = 0; b < a.B; ++b) a.vl.n[b] = std::min(n_sel, a.vl.nb[b]);
   const AttendPlan p = make_plan(a, shape->dtype, shape->B * shape->Hkv, n_sel, L.slots);
   out->path = p.path;
   out->cluster = p.cluster;
@@ -693,7 +769,8 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
   if (reuse < 0 || reuse > 2)
     return fail(SV_ERR_INVALID_ARG, "reuse=%d must be 0, 1 or 2", reuse);
-  const int nb = kv->ctx / shape->blk;
+  const Ctxs c = ctxs_of(shape, kv);
+  const int nb = c.nb;
   if (reuse == 2) {
     // full verification: every block, no scoring, selection or budget
     if (!q || !draft_k || !draft_v || !out)
@@ -707,7 +784,8 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
     return run_attend(shape, q, kv, nullptr, nb, nb, draft_k, draft_v, draft_parent, out,
                       workspace, L, (cudaStream_t)stream);
   }
-  const int k = budget_blocks(budget, kv->ctx, nb);
+  int k_b[kMaxVarB];
+  const int k = budgets_of(budget, kv, c, shape->B, k_b);
   if (k < 0) return fail(SV_ERR_INVALID_ARG, "invalid budget");
   if (k > kmax) return fail(SV_ERR_INVALID_ARG, "budget k=%d exceeds kmax=%d", k, kmax);
   if (kmax > 0 && !sel_cache) return fail(SV_ERR_INVALID_ARG, "sel_cache is NULL");
@@ -722,12 +800,12 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
   cudaStream_t st = (cudaStream_t)stream;
   if (!reuse && kmax > 0) {
-    r = do_score_select(shape, q, reps, kv, k, sel_cache, kmax, workspace, L, st);
+    r = do_score_select(shape, q, reps, kv, k, sel_cache, kmax, workspace, L, st, k_b);
     if (r != SV_OK) return r;
   }
   if (k_out) *k_out = k;
   return run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out,
-                    workspace, L, st);
+                    workspace, L, st, c.var ? k_b : nullptr);
 }
 
 sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const sv_kv* kv,
@@ -738,7 +816,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
-  const int nb = kv->ctx / shape->blk;
+  const int nb = ctxs_of(shape, kv).nb;  // sel == NULL: each sequence's own blocks
   if (!sel) {
     n_sel = nb;
     sel_stride = nb;
@@ -756,6 +834,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   const WsLayout W = ws_layout(*shape, kv->nb_max, n_sel);
   AttendArgs a{};
   fill_args(a, shape, q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent, nullptr, W);
+  set_nsel(a, nullptr);
   a.out = out;
   const AttendPlan p = make_plan(a, shape->dtype, shape->B * shape->Hkv, n_sel, W.slots);
   const WsLayout L = noalloc_layout(*shape, W.rpad, p.slot_stride);

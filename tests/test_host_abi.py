@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version(L):
-    assert api.sv_abi_version() == api.ABI_VERSION == 2
+    assert api.sv_abi_version() == api.ABI_VERSION == 3
 
 
 def test_budget_matches_oracle_golden(L):
@@ -178,3 +178,46 @@ def test_verify_full_mode_needs_no_selection_buffers(L):
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, None, fake,
                       fake, None, 2, None, 8, None, fake, fake, ws_n - 1, None)
     assert st == api.SV_ERR_WORKSPACE, msg  # got past every selection check
+
+
+def test_per_sequence_context_validation(L):
+    """seq_ctx is checked on the host: negative lengths, a block table too
+    narrow for the longest sequence and more than 64 sequences are refused
+    before anything is launched."""
+    s = api.make_shape(3, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20
+    ws_n = api.sv_workspace_bytes(s, 64, 8)
+
+    def kv(ctxs, nb_max=64):
+        k = api.KV(fake, fake, fake, nb_max, 64, 0)
+        arr = (C.c_int32 * len(ctxs))(*ctxs)
+        k.seq_ctx = C.cast(arr, C.POINTER(C.c_int32))
+        return k, arr
+
+    k1, _a1 = kv([100, -5, 16])
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(s), fake, C.byref(k1), None, 0, 0, fake, fake,
+                      None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "seq_ctx[1]" in msg
+    # the longest sequence (1000 tokens = 62 full blocks + 8) needs 63 columns
+    k2, _a2 = kv([1000, 0, 17], nb_max=62)
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(s), fake, C.byref(k2), None, 0, 0, fake, fake,
+                      None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "nb_max" in msg
+    big = api.make_shape(65, 4, 2, 64, 16, 4, torch.float32)
+    k3, _a3 = kv([16] * 65)
+    st, msg = _status(L, L.sv_sparse_attend, C.byref(big), fake, C.byref(k3), None, 0, 0, fake,
+                      fake, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_UNSUPPORTED and "per-sequence" in msg
+    # the uniform ctx is ignored when seq_ctx is given (here it is negative)
+    k4, _a4 = kv([16, 32, 0])
+    k4.ctx = -1
+    st, msg = _status(L, L.sv_build_reps, C.byref(s), C.byref(k4), 0, 3, fake, None)
+    assert st == api.SV_ERR_INVALID_ARG and "blocks [0, 3) outside [0, 2)" in msg
+
+
+def test_make_kv_keeps_seq_ctx_alive():
+    t = torch.zeros(4, 2, 16, 64)
+    bt = torch.zeros(2, 8, dtype=torch.int32)
+    kv = api.make_kv(t, t, bt, 0, [100, 7])
+    assert [kv.seq_ctx[i] for i in range(2)] == [100, 7]
+    assert not api.make_kv(t, t, bt, 50).seq_ctx  # NULL: the uniform ctx

@@ -1,0 +1,215 @@
+"""Per-sequence prefix lengths (sv_kv.seq_ctx) against the oracle.
+
+A batch whose sequences hold different contexts is the oracle's verification
+layer run on each sequence alone with its own context: its own full blocks
+compete for the budget its own length gives, and its own partial last block is
+always attended. Block-table entries past each sequence's own blocks are set
+to -1 here, so a read of any of them would raise the bad-page flag.
+"""
+from dataclasses import replace
+
+import pytest
+import torch
+
+from oracle import sva_oracle as O
+from sparse_verification_attention_gb300 import api, build_lib
+from sparse_verification_attention_gb300 import workloads as W
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    build_lib.build()
+    api.lib()
+    torch.cuda.set_device(0)
+
+
+def _wl(dtype="bf16", **kw):
+    base = dict(name="varlen", B=5, Hq=8, Hkv=2, d=128, blk=64, ctx=64 * 40 + 13, T=8,
+                dtype=dtype, budget=W.Budget(W.BUDGET_FIXED, 13, 0, 0, 0, 0, 0), seed=41,
+                n_planted=4, permute_pages=True)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+def _layer(wl, seq_ctx, layer=0):
+    """Inputs laid out for the longest context; each sequence's table row
+    ends at its own last block."""
+    assert max(seq_ctx) <= wl.ctx and len(seq_ctx) == wl.B
+    x = W.make_layer(wl, layer=layer)
+    bt = x.block_table.clone()
+    for b, c in enumerate(seq_ctx):
+        bt[b, -(-c // wl.blk):] = -1
+    x.block_table = bt
+    return x
+
+
+def _oracle_seq(wl, x, b, c, sel=None):
+    """(out, sel, scores, k) of sequence b alone with context c."""
+    nb = c // wl.blk
+    qb, btb = x.q[b:b + 1], x.block_table[b:b + 1]
+    if sel is None:
+        reps = O.block_representatives(x.k_pool, btb, nb, wl.blk)
+        scores = O.block_scores(qb, reps, wl.G)
+        k = O.budget_from(wl.budget, c, nb)
+        sel = O.select_all(scores, k)
+    else:
+        scores, k = None, sel.shape[-1]
+    out = O.sparse_attend(qb, x.k_pool, x.v_pool, btb, sel, x.draft_k[b:b + 1],
+                          x.draft_v[b:b + 1], wl.parent_list(), tail_block=nb,
+                          tail_len=c % wl.blk)
+    return out, sel, scores, k
+
+
+def _check_verify(wl, x, seq_ctx, heads=None, st=None):
+    xd = x.to("cuda")
+    st = st or api.LayerState(wl, xd, seq_ctx=seq_ctx)
+    plan = api.sv_attend_plan(st.shape, st.kv, st.kmax)
+    assert plan.streamk == 0  # stream-K runs are cut for equal-length pairs only
+    out = st.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    gsel, gout = st.sel.cpu(), out.cpu()
+    heads = list(range(wl.Hkv)) if heads is None else heads
+    atol = U.out_atol(wl.torch_dtype)
+    for b, c in enumerate(seq_ctx):
+        ref, _, scores, k = _oracle_seq(wl, x, b, c)
+        assert k <= st.kmax
+        differ = U.compare_selection(gsel[b:b + 1, heads], scores[:, heads], k)
+        assert all(int(v) == -1 for v in gsel[b, :, k:].flatten().tolist())
+        for i, h in enumerate(heads):
+            if (0, i) in differ:
+                continue
+            cols = slice(h * wl.G, (h + 1) * wl.G)
+            err = (gout[b:b + 1, :, cols].double() - ref[:, :, cols]).abs().max().item()
+            assert err <= atol, (b, c, h, err)
+    return st
+
+
+CASES = [
+    # name, workload overrides, per-sequence contexts (an empty sequence, one
+    # holding only a partial block, partial and whole last blocks)
+    ("tc", dict(), [64 * 40 + 13, 64 * 7, 30, 0, 64 * 25]),
+    ("tc_tree16", dict(B=4, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS, ctx=64 * 30),
+     [64 * 30, 64 * 2 + 63, 64 * 17, 64]),
+    ("mma", dict(B=3, Hq=4, Hkv=2, T=4, d=64, blk=32, ctx=32 * 50), [32 * 50, 32 * 3 + 5, 32 * 31]),
+    ("generic_f32", dict(B=3, dtype="f32", d=64, blk=16, Hq=4, Hkv=2, T=4, ctx=16 * 64 + 1),
+     [16 * 64 + 1, 16 * 10 + 1, 0]),
+    ("generic_R256", dict(B=2, T=32, Hq=16, Hkv=2, ctx=64 * 20), [64 * 20, 64 * 9 + 1]),
+]
+PATHS = {"tc": api.SV_PATH_TCGEN05, "mma": api.SV_PATH_MMA_SYNC,
+         "generic": api.SV_PATH_CUDA_CORES}
+
+
+@pytest.mark.parametrize("name,over,seq_ctx", CASES, ids=[c[0] for c in CASES])
+def test_verify_per_sequence_contexts(name, over, seq_ctx):
+    over = dict(over)
+    dtype = over.pop("dtype", "bf16")
+    wl = _wl(dtype, **over)
+    x = _layer(wl, seq_ctx)
+    st = api.LayerState(wl, x.to("cuda"), seq_ctx=seq_ctx)
+    assert api.sv_attend_plan(st.shape, st.kv, st.kmax).path == PATHS[name.split("_")[0]]
+    _check_verify(wl, x, seq_ctx, st=st)
+
+
+def test_verify_per_sequence_piecewise_budgets():
+    """Each sequence takes the piecewise rule of its own length: the short
+    one keeps every block, the long ones a fraction."""
+    # all blocks up to 4096 tokens, then 12.5 %, then 6.25 % above 32768,
+    # never fewer than 8: 46, 39 and 40 blocks for the three lengths
+    budget = W.Budget(W.BUDGET_PIECEWISE, 0, 4096, 8, 0.125, 32768, 0.0625)
+    wl = _wl(B=3, ctx=40000, budget=budget, n_planted=8)
+    seq_ctx = [3000, 20000, 40000]
+    ks = [O.budget_from(wl.budget, c, c // wl.blk) for c in seq_ctx]
+    assert ks == [46, 39, 40]
+    x = _layer(wl, seq_ctx)
+    st = _check_verify(wl, x, seq_ctx)
+    assert st.k == max(ks)
+
+
+def test_verify_llama8b_mixed_lengths_sampled():
+    """Llama-3.1-8B-shaped layer, four sequences from 1K to 32K tokens;
+    two KV heads of each sequence recomputed on the oracle."""
+    wl = replace(W.WORKLOADS["llama8b_32k"], B=4, ctx=32768 + 40, permute_pages=True)
+    seq_ctx = [32768 + 40, 8192 + 17, 20000, 1000]
+    x = _layer(wl, seq_ctx)
+    _check_verify(wl, x, seq_ctx, heads=[0, 7])
+
+
+def test_reuse_and_full_modes_per_sequence():
+    """A second layer reusing the first layer's selections, and a full
+    verification step, both with per-sequence contexts."""
+    wl = _wl()
+    seq_ctx = [64 * 40 + 13, 64 * 7, 30, 0, 64 * 25]
+    x0, x1 = _layer(wl, seq_ctx, 0), _layer(wl, seq_ctx, 1)
+    st0 = _check_verify(wl, x0, seq_ctx)
+    st1 = api.LayerState(wl, x1.to("cuda"), seq_ctx=seq_ctx)
+    out_reuse = st1.verify(reuse=api.VERIFY_REUSE, sel_from=st0).clone()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st1.ws) == 0
+    out_full = st1.verify(reuse=api.VERIFY_FULL).clone()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st1.ws) == 0
+    gsel0 = st0.sel.cpu()
+    for b, c in enumerate(seq_ctx):
+        _, sel0, scores0, k = _oracle_seq(wl, x0, b, c)
+        same = [h for h in range(wl.Hkv) if gsel0[b, h, :k].tolist() == sel0[0, h].tolist()]
+        ref, _, _, _ = _oracle_seq(wl, x1, b, c, sel=sel0)
+        for h in same:
+            cols = slice(h * wl.G, (h + 1) * wl.G)
+            err = (out_reuse[b:b + 1, :, cols].double().cpu() - ref[:, :, cols]).abs().max().item()
+            assert err <= U.BF16_ATOL, ("reuse", b, h, err)
+        nb = c // wl.blk
+        every = torch.arange(nb, dtype=torch.int64).expand(1, wl.Hkv, nb)
+        ref_full, _, _, _ = _oracle_seq(wl, x1, b, c, sel=every)
+        U.compare_out(out_full[b:b + 1], ref_full, U.BF16_ATOL)
+
+
+def test_explicit_selection_and_noalloc_per_sequence():
+    """sv_sparse_attend with an explicit selection of n_sel blocks for every
+    sequence, and the allocation-free entry's all-block pass, with
+    per-sequence contexts."""
+    wl = _wl()
+    seq_ctx = [64 * 40 + 13, 64 * 7, 64 * 12 + 5, 64 * 9, 64 * 25]
+    x = _layer(wl, seq_ctx)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd, kmax=wl.NB, build_reps=False, seq_ctx=seq_ctx)
+    n_sel = 6
+    g = torch.Generator().manual_seed(9)
+    sel = torch.stack([torch.stack([
+        torch.sort(torch.randperm(c // wl.blk, generator=g)[:n_sel]).values
+        for _ in range(wl.Hkv)]) for c in seq_ctx]).to(torch.int32)
+    out = torch.zeros_like(xd.q)
+    api.sv_sparse_attend(st.shape, xd.q, st.kv, sel.cuda(), n_sel, n_sel, xd.draft_k, xd.draft_v,
+                         st.parents, out, st.ws)
+    dense = torch.full_like(xd.q, float("nan"))
+    flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    api.sv_sparse_attend_noalloc(st.shape, xd.q, st.kv, None, 0, 0, xd.draft_k, xd.draft_v,
+                                 st.parents, dense, flags)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0 and int(flags.item()) == 0
+    for b, c in enumerate(seq_ctx):
+        ref, _, _, _ = _oracle_seq(wl, x, b, c, sel=sel[b:b + 1].long())
+        U.compare_out(out[b:b + 1], ref, U.BF16_ATOL)
+        nb = c // wl.blk
+        every = torch.arange(nb, dtype=torch.int64).expand(1, wl.Hkv, nb)
+        ref_full, _, _, _ = _oracle_seq(wl, x, b, c, sel=every)
+        U.compare_out(dense[b:b + 1], ref_full, U.BF16_ATOL)
+
+
+def test_uniform_lengths_given_per_sequence_match_uniform_call():
+    """seq_ctx holding one length for every sequence gives the same
+    selection and (to rounding) the same output as the uniform ctx."""
+    wl = _wl(B=2)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    a = api.LayerState(wl, xd)
+    b = api.LayerState(wl, xd, seq_ctx=[wl.ctx] * wl.B)
+    oa, ob = a.verify().clone(), b.verify().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.sel.cpu(), b.sel.cpu())
+    assert (oa.double() - ob.double()).abs().max().item() <= U.BF16_ATOL
