@@ -25,6 +25,13 @@ Readings where the pages are silent (every one is listed in the design doc):
   R3 budget: all blocks when ctx <= short_ctx; otherwise
      min(NB, max(floor, ceil(frac * NB))) with frac = frac_mid up to long_ctx
      and frac_long beyond; FIXED mode gives min(NB, fixed).
+  R3b smooth budget (SMOOTH mode, a variant of R3): the pages say the
+     piecewise control gives a smooth transition from short to long context.
+     Reading: the keep-rate per context token is piecewise constant (1 up to
+     short_ctx, frac_mid up to long_ctx, frac_long beyond), and the kept
+     budget is its integral, so it is continuous and never falls as ctx
+     grows. As a fraction of the blocks, k = min(NB, max(floor,
+     ceil(kept_tokens / ctx * NB))).
   R4 top-k ties go to the lower block index; the selected set is reported in
      ascending block order.
   R5 draft-to-draft mask: draft t sees itself and its ancestors (a chain is
@@ -55,6 +62,7 @@ F64 = torch.float64
 
 BUDGET_FIXED = 0
 BUDGET_PIECEWISE = 1
+BUDGET_SMOOTH = 2
 
 
 # --------------------------------------------------------------------------
@@ -109,12 +117,39 @@ def budget_blocks(ctx: int, nb: int, mode: int, fixed_blocks: int = 0,
     """Number of KV blocks kept for a context of ctx tokens in nb full blocks."""
     if mode == BUDGET_FIXED:
         return min(nb, fixed_blocks)
+    if mode == BUDGET_SMOOTH:
+        return smooth_budget_blocks(ctx, nb, short_ctx, floor_blocks, frac_mid, long_ctx,
+                                    frac_long)
     if ctx <= short_ctx:
         return nb                                # short context: keep everything
     # fractions are decimal percentages (12.5% = 0.125): ceil of the exact
     # decimal product, not of its binary floating-point approximation
     frac = Fraction(repr(frac_mid)) if ctx <= long_ctx else Fraction(repr(frac_long))
     want = math.ceil(frac * nb)
+    return min(nb, max(floor_blocks, want))
+
+
+def smooth_kept_tokens(ctx: int, short_ctx: int, frac_mid: float, long_ctx: int,
+                       frac_long: float) -> Fraction:
+    """Reading R3b: the context tokens' worth of budget kept at length ctx,
+    the integral of a keep-rate of 1 on [0, short_ctx], frac_mid on
+    (short_ctx, long_ctx] and frac_long beyond (fractions as decimals)."""
+    fm, fl = Fraction(repr(frac_mid)), Fraction(repr(frac_long))
+    short_part = min(ctx, short_ctx)
+    mid_part = min(max(ctx - short_ctx, 0), long_ctx - short_ctx)
+    long_part = max(ctx - long_ctx, 0)
+    return short_part + fm * mid_part + fl * long_part
+
+
+def smooth_budget_blocks(ctx: int, nb: int, short_ctx: int, floor_blocks: int,
+                         frac_mid: float, long_ctx: int, frac_long: float) -> int:
+    """Blocks kept under reading R3b: the kept fraction of the context,
+    kept_tokens / ctx, applied to the nb full blocks and rounded up, then
+    at least floor and at most nb. Everything is kept up to short_ctx."""
+    if ctx <= short_ctx:
+        return nb
+    kept = smooth_kept_tokens(ctx, short_ctx, frac_mid, long_ctx, frac_long)
+    want = math.ceil(kept / ctx * nb)
     return min(nb, max(floor_blocks, want))
 
 

@@ -32,6 +32,7 @@ import torch
 # Budget modes, mirrored from the C header (values are part of the ABI).
 BUDGET_FIXED = 0
 BUDGET_PIECEWISE = 1
+BUDGET_SMOOTH = 2
 
 # A 16-node draft tree: root -> 2 children -> 4 grandchildren -> chains, with
 # node 15 a second child of node 3; maximum depth 4. Topology is plain data.

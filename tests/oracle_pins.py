@@ -127,6 +127,33 @@ def pin_budget_properties(O):
                 prev_frac = frac
 
 
+def pin_smooth_budget_properties(O):
+    """Reading R3b: with ctx a whole number of blocks and no floor, one more
+    block of context adds at most one kept block and never removes one
+    (the curve has no jumps), everything is kept up to short_ctx, and the
+    kept fraction tends to frac_long."""
+    b = W.Budget(W.BUDGET_SMOOTH, 0, 4096, 0, 0.125, 32768, 0.0625)
+    for blk in (16, 64):
+        prev = None
+        for nb in range(0, 200_000 // blk + 1, 7):
+            ctx = nb * blk
+            k = O.budget_from(b, ctx, nb)
+            assert 0 <= k <= nb
+            if ctx <= b.short_ctx:
+                assert k == nb
+            if prev is not None:
+                pnb, pk = prev
+                assert pk <= k <= pk + (nb - pnb), (ctx, pk, k)
+            prev = (nb, k)
+    # far beyond long_ctx the kept fraction approaches frac_long from above
+    nb = 10**7
+    k = O.budget_from(b, nb * 64, nb)
+    assert 0.0625 < k / nb < 0.0625 * 1.01
+    # all rates 1: every block kept at any length
+    one = W.Budget(W.BUDGET_SMOOTH, 0, 100, 0, 1.0, 1000, 1.0)
+    assert all(O.budget_from(one, n * 16, n) == n for n in range(0, 500, 13))
+
+
 # ------------------------------------------------------------------ C4 select
 def pin_select_golden(O):
     for ln in _lines("topk_ties.txt"):

@@ -19,6 +19,7 @@ _orig_select = O.select_blocks
 _orig_budget = O.budget_blocks
 _orig_reps = O.block_representatives
 _orig_sparse = O.sparse_attend
+_orig_kept = O.smooth_kept_tokens
 
 
 def _anc_transposed(parents, t):        # sees later drafts instead of earlier ones
@@ -71,6 +72,14 @@ def _budget_floor_division(ctx, nb, mode, fixed=0, short=0, floor=0, fm=0.0, lc=
     return min(nb, max(floor, int(frac * nb)))
 
 
+def _kept_mid_dropped(ctx, short, fm, lc, fl):  # forgets the middle piece
+    return _orig_kept(ctx, short, 0.0, lc, fl)
+
+
+def _kept_rates_swapped(ctx, short, fm, lc, fl):  # long rate on the middle piece
+    return _orig_kept(ctx, short, fl, lc, fm)
+
+
 def _reps_off_by_one(k_pool, block_table, n_blocks, blk):
     return _orig_reps(k_pool, block_table, n_blocks, blk) * blk / (blk + 1)
 
@@ -99,6 +108,8 @@ MUTATIONS = {
     "select_lowest": ("select_blocks", _select_lowest),
     "budget_no_floor": ("budget_blocks", _budget_no_floor),
     "budget_floor_division": ("budget_blocks", _budget_floor_division),
+    "smooth_mid_dropped": ("smooth_kept_tokens", _kept_mid_dropped),
+    "smooth_rates_swapped": ("smooth_kept_tokens", _kept_rates_swapped),
     "reps_wrong_divisor": ("block_representatives", _reps_off_by_one),
     "attend_head_mapping": ("sparse_attend", _sparse_heads_mod),
     "attend_tail_dropped": ("sparse_attend", _sparse_tail_dropped),
