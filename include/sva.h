@@ -82,8 +82,16 @@ typedef struct {
  * but no constants; the caller supplies them. */
 #define SV_BUDGET_FIXED 0
 #define SV_BUDGET_PIECEWISE 1
+/* SMOOTH: the same page says the piecewise control makes the transition from
+ * short to long context smooth. This library's reading of a curve without
+ * jumps: a keep-rate of 1 per context token up to short_ctx, frac_mid up to
+ * long_ctx and frac_long beyond, kept = its integral over [0, ctx), and
+ * k = min(NB, max(floor, ceil(kept / ctx * NB))) (all NB up to short_ctx).
+ * k never falls as ctx grows. Needs long_ctx >= short_ctx >= 0. Fractions are
+ * read as decimals of up to nine places (0.1 is exactly one tenth). */
+#define SV_BUDGET_SMOOTH 2
 typedef struct {
-  int mode;           /* SV_BUDGET_FIXED or SV_BUDGET_PIECEWISE            */
+  int mode;           /* SV_BUDGET_FIXED, SV_BUDGET_PIECEWISE or SMOOTH    */
   int fixed_blocks;   /* FIXED: k = min(NB, fixed_blocks)                  */
   int short_ctx;      /* PIECEWISE: ctx <= short_ctx keeps all NB blocks   */
   int floor_blocks;   /* otherwise k = min(NB, max(floor, ceil(frac*NB)))  */
@@ -127,7 +135,7 @@ const char* sv_last_error(void);
 /* Piecewise budget control [SV-Tut1]: number of blocks kept for a context of
  * ctx tokens in nb blocks. Pure host function, no GPU needed. Returns -1 on
  * an invalid budget (NULL, unknown mode, negative sizes, fractions outside
- * [0, 1]). */
+ * [0, 1], long_ctx < short_ctx in SMOOTH mode). */
 int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
 
 /* Bytes of workspace that score/select/attend/verify calls with this shape
@@ -178,8 +186,11 @@ sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, i
 
 /* Score + budget + select in one call [SV-Fig1], [SV-Tut1]:
  * k = sv_budget_blocks(budget, kv->ctx, NB); scores go to the workspace;
- * sel as in sv_select_blocks; *k_out (host, may be NULL) receives k.
- * SV_ERR_INVALID_ARG if k > kmax. */
+ * sel as in sv_select_blocks; *k_out (host, may be NULL) receives k. With
+ * per-sequence lengths (kv->seq_ctx), sequence b keeps
+ * k_b = sv_budget_blocks(budget, seq_ctx[b], seq_ctx[b] / blk) blocks, its
+ * sel rows hold k_b indices and then -1, and *k_out receives the largest k_b.
+ * SV_ERR_INVALID_ARG if k (the largest k_b) > kmax. */
 sv_status sv_score_select(const sv_shape* shape, const void* q, const float* reps,
                           const sv_kv* kv, const sv_budget* budget, int32_t* sel,
                           int kmax, int* k_out, void* workspace, size_t ws_bytes,

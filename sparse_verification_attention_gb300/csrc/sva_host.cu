@@ -122,16 +122,35 @@ Ctxs ctxs_of(const sv_shape* s, const sv_kv* kv) {
   return c;
 }
 
+// The smooth curve: a keep-rate of 1 per context token up to short_ctx,
+// frac_mid up to long_ctx and frac_long beyond; the kept tokens are its
+// integral and k = min(nb, max(floor, ceil(kept / ctx * nb))). Fractions are
+// taken as decimals of nine places, so the rounding up is exact.
+static int smooth_budget_blocks(const sv_budget* bd, int ctx, int nb) {
+  if (bd->short_ctx < 0 || bd->long_ctx < bd->short_ctx) return -1;
+  if (ctx <= bd->short_ctx) return nb;
+  const long long kDec = 1000000000LL;
+  const long long fm = std::llround(bd->frac_mid * 1e9), fl = std::llround(bd->frac_long * 1e9);
+  const long long mid = std::min<long long>(ctx, bd->long_ctx) - bd->short_ctx;
+  const long long lng = std::max<long long>((long long)ctx - bd->long_ctx, 0);
+  const __int128 kept = (__int128)bd->short_ctx * kDec + (__int128)fm * mid + (__int128)fl * lng;
+  const __int128 num = kept * nb, den = (__int128)kDec * ctx;
+  const long long want = (long long)((num + den - 1) / den);
+  const long long k = want > bd->floor_blocks ? want : bd->floor_blocks;
+  return (int)(k < nb ? k : nb);
+}
+
 int budget_blocks(const sv_budget* bd, int ctx, int nb) {
   if (!bd || ctx < 0 || nb < 0) return -1;
   if (bd->mode == SV_BUDGET_FIXED) {
     if (bd->fixed_blocks < 0) return -1;
     return nb < bd->fixed_blocks ? nb : bd->fixed_blocks;
   }
-  if (bd->mode != SV_BUDGET_PIECEWISE) return -1;
+  if (bd->mode != SV_BUDGET_PIECEWISE && bd->mode != SV_BUDGET_SMOOTH) return -1;
   if (bd->floor_blocks < 0 || !(bd->frac_mid >= 0.0 && bd->frac_mid <= 1.0) ||
       !(bd->frac_long >= 0.0 && bd->frac_long <= 1.0))
     return -1;
+  if (bd->mode == SV_BUDGET_SMOOTH) return smooth_budget_blocks(bd, ctx, nb);
   if (ctx <= bd->short_ctx) return nb;
   const double frac = (ctx <= bd->long_ctx) ? bd->frac_mid : bd->frac_long;
   // ceil(frac * nb) with a guard against products like 0.125*960 landing a

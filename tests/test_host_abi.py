@@ -56,8 +56,8 @@ def test_budget_matches_oracle_golden(L):
 def test_budget_matches_oracle_random(L):
     g = torch.Generator().manual_seed(1)
     fracs = [0.03125, 0.0625, 0.1, 0.125, 0.2, 0.25, 0.3, 0.5, 1.0]
-    for _ in range(3000):
-        mode = int(torch.randint(0, 2, (1,), generator=g))
+    for _ in range(4500):
+        mode = int(torch.randint(0, 3, (1,), generator=g))
         nb = int(torch.randint(0, 5000, (1,), generator=g))
         ctx = nb * int(torch.randint(1, 129, (1,), generator=g))
         b = W.Budget(mode, int(torch.randint(0, 300, (1,), generator=g)),
@@ -66,6 +66,10 @@ def test_budget_matches_oracle_random(L):
                      fracs[int(torch.randint(0, len(fracs), (1,), generator=g))],
                      int(torch.randint(0, 300000, (1,), generator=g)),
                      fracs[int(torch.randint(0, len(fracs), (1,), generator=g))])
+        if mode == W.BUDGET_SMOOTH and b.long_ctx < b.short_ctx:  # invalid for SMOOTH
+            assert api.sv_budget_blocks(b, ctx, nb) == -1
+            b = W.Budget(mode, b.fixed_blocks, b.long_ctx, b.floor_blocks, b.frac_mid,
+                         b.short_ctx, b.frac_long)
         assert api.sv_budget_blocks(b, ctx, nb) == O.budget_from(b, ctx, nb), (b, ctx, nb)
 
 

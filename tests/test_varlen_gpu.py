@@ -116,16 +116,22 @@ def test_verify_per_sequence_contexts(name, over, seq_ctx):
     _check_verify(wl, x, seq_ctx, st=st)
 
 
-def test_verify_per_sequence_piecewise_budgets():
-    """Each sequence takes the piecewise rule of its own length: the short
-    one keeps every block, the long ones a fraction."""
+BUDGETS = [
     # all blocks up to 4096 tokens, then 12.5 %, then 6.25 % above 32768,
     # never fewer than 8: 46, 39 and 40 blocks for the three lengths
-    budget = W.Budget(W.BUDGET_PIECEWISE, 0, 4096, 8, 0.125, 32768, 0.0625)
+    ("piecewise", W.Budget(W.BUDGET_PIECEWISE, 0, 4096, 8, 0.125, 32768, 0.0625), [46, 39, 40]),
+    # the same rates as a smooth curve: 46, 95 and 128 blocks
+    ("smooth", W.Budget(W.BUDGET_SMOOTH, 0, 4096, 8, 0.125, 32768, 0.0625), [46, 95, 128]),
+]
+
+
+@pytest.mark.parametrize("name,budget,ks", BUDGETS, ids=[b[0] for b in BUDGETS])
+def test_verify_per_sequence_budgets(name, budget, ks):
+    """Each sequence takes the budget rule at its own length: the short one
+    keeps every block, the long ones a fraction."""
     wl = _wl(B=3, ctx=40000, budget=budget, n_planted=8)
     seq_ctx = [3000, 20000, 40000]
-    ks = [O.budget_from(wl.budget, c, c // wl.blk) for c in seq_ctx]
-    assert ks == [46, 39, 40]
+    assert [O.budget_from(wl.budget, c, c // wl.blk) for c in seq_ctx] == ks
     x = _layer(wl, seq_ctx)
     st = _check_verify(wl, x, seq_ctx)
     assert st.k == max(ks)
