@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   // barrier orders every thread's score stores before thread 0's
   // acquire-release arrival; the last arrival thereby sees every score.
   __shared__ unsigned s_last;
-  __shared__ TopkSmem<kScoreThreads> tsm;
+  __shared__ TopkSmem<kScoreThreads, kScoreKeys> tsm;
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned ctas = (unsigned)((nbb + a.rows_per_cta - 1) / a.rows_per_cta);
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   }
   __syncthreads();
   if (s_last) {
-    cta_topk<kScoreThreads, kScoreKeys>(srow, nbb, n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax,
+    cta_topk_fit<kScoreThreads, kScoreKeys>(srow, nbb, n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax,
                                         a.kmax, tsm);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }

@@ -22,11 +22,11 @@ constexpr int kSelKeys = kMaxNB / kSelThreads;  // keys per thread
 static_assert(kSelThreads * kSelKeys >= kMaxNB, "select must hold every score");
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const __grid_constant__ SelectArgs a) {
-  __shared__ TopkSmem<kSelThreads> tsm;
+  __shared__ TopkSmem<kSelThreads, kSelKeys> tsm;
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   const int pair = blockIdx.x, b = pair / a.Hkv;
-  cta_topk<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, nb_of(a.vl, b, a.nb),
+  cta_topk_fit<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, nb_of(a.vl, b, a.nb),
                                   n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
 }
 

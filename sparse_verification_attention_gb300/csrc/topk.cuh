@@ -8,10 +8,25 @@
 // Ties go to the lower block index (this library's reading); the kept set is
 // written in ascending block order.
 //
-// Method. Scores become order-preserving 32-bit keys held in registers. Warp
-// w owns the index range [w*32*per, (w+1)*32*per); lane l holds the indices
-// w*32*per + 32*e + l for e < per, so every load is coalesced and index order
-// inside a warp is (e, lane) order. The k-th largest key is found two bits
+// Method. Scores become order-preserving 32-bit keys held in registers, KPT
+// per thread. Warp w owns the index range [w*32*KPT, (w+1)*32*KPT); lane l
+// holds the indices w*32*KPT + 32*e + l for e < KPT, so every load is
+// coalesced and index order inside a warp is (e, lane) order. KPT is a
+// compile-time constant (cta_topk_fit picks the smallest that holds nb), so
+// every per-key loop unrolls without branches and the independent loads and
+// latency chains of a thread's keys overlap.
+//
+// Bucketed path (tried first). The scores are binned linearly over
+// [min, max] into kTopkBins bins. The binning is monotone: a higher bin only
+// holds strictly larger scores. One shared histogram and a suffix scan give
+// the bin b* holding the k-th largest score. Every key above b* is kept, and
+// every key below it is dropped. The keys of b* (at most kTopkMaxCand) are
+// ranked exactly against each other by (score descending, index
+// ascending), and the first k - (keys above b*) of them are kept. A boundary
+// bin with more keys, equal scores everywhere, or non-finite extremes fall
+// back to the radix search below.
+//
+// Radix search. The k-th largest key is found two bits
 // per pass from the most significant end: each warp counts its keys at or
 // above the three candidates that extend the current prefix, the per-warp
 // counts meet in shared memory behind one barrier, and every warp picks the
@@ -34,22 +49,49 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The score an order key stands for (-0 comes back as +0).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 constexpr int kTopkRadixBits = 2;
 constexpr int kTopkCands = (1 << kTopkRadixBits) - 1;  // candidates per pass
+constexpr int kTopkBins = 1024;                        // bucketed path: histogram bins
+constexpr int kTopkMaxCand = 256;                      // largest boundary bin it ranks
 
-template <int NT>
+// Bin of a key for scores in [lo, lo + kTopkBins / scale]: monotone in the
+// key (rounded subtraction and multiplication are monotone, truncation of a
+// non-negative value is a floor), and the same instructions wherever used.
+__device__ __forceinline__ int key_bin(uint32_t key, float lo, float scale) {
+  const float x = __fmul_rn(__fsub_rn(key_value(key), lo), scale);  // >= 0
+  const int i = __float2int_rz(x);
+  return i < kTopkBins - 1 ? i : kTopkBins - 1;
+}
+
+template <int NT, int KPT>
 struct TopkSmem {
   uint32_t cnt[2][kTopkCands][NT / 32];  // per-pass per-candidate per-warp counts
   uint32_t above[NT / 32], ties[NT / 32], kept[NT / 32];
+  uint32_t wmin[NT / 32], wmax[NT / 32], wsum[NT / 32];
+  uint32_t hist[kTopkBins];
+  uint32_t keepbits[(NT * KPT + 31) / 32];  // kept keys of the boundary bin, by index
+  uint32_t cand_key[kTopkMaxCand];
+  int32_t cand_idx[kTopkMaxCand];
+  int bstar;
+  uint32_t bstar_above, ncand;
 };
 
 // All NT threads of the CTA call this once. sc: nb scores (global, read
 // through L2 only: other CTAs of the grid may have just written them);
-// nb <= NT * KPT. out: kmax entries, the k kept indices ascending then -1.
-template <int NT, int KPT>
+// nb <= NT * KPT <= NT * KMAX. out: kmax entries, the k kept indices
+// ascending then -1.
+template <int NT, int KPT, int KMAX>
 __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int kmax,
-                         TopkSmem<NT>& sm) {
+                         TopkSmem<NT, KMAX>& sm) {
+  static_assert(KPT <= KMAX, "shared memory sized for fewer keys");
   constexpr int NW = NT / 32;
+  constexpr int BPT = kTopkBins / NT;  // histogram bins per thread in the scan
+  static_assert(kTopkBins % NT == 0 && NT >= kTopkMaxCand, "bucketed top-k layout");
   using Mask = std::conditional_t<(KPT > 32), unsigned long long, uint32_t>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = k_req < nb ? k_req : nb;
@@ -59,19 +101,134 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     for (int i = tid; i < nb; i += NT) out[i] = i;
     return;
   }
-  const int per = (nb + NT - 1) / NT;
-  const int wbase = warp * 32 * per;
+  const int wbase = warp * 32 * KPT;
   // padding entries hold key 0, below every candidate tested
   uint32_t rk[KPT];
   Mask valid = 0;
 #pragma unroll
   for (int e = 0; e < KPT; ++e) {
     const int j = wbase + 32 * e + lane;
-    const bool ok = e < per && j < nb;
+    const bool ok = j < nb;
     rk[e] = ok ? order_key(__ldcg(sc + j)) : 0u;
     valid |= (Mask)(ok ? 1u : 0u) << e;
   }
 
+  const unsigned lt = (1u << lane) - 1u;
+  Mask keep = 0;
+  bool done = false;
+
+  // ---- bucketed path
+  {
+    uint32_t lmin = 0xffffffffu, lmax = 0u;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      if ((valid >> e) & 1u) {
+        lmin = min(lmin, rk[e]);
+        lmax = max(lmax, rk[e]);
+      }
+    }
+    lmin = __reduce_min_sync(0xffffffffu, lmin);
+    lmax = __reduce_max_sync(0xffffffffu, lmax);
+    if (lane == 0) {
+      sm.wmin[warp] = lmin;
+      sm.wmax[warp] = lmax;
+    }
+    for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0u;
+    for (int i = tid; i < (nb + 31) / 32; i += NT) sm.keepbits[i] = 0u;
+    if (tid == 0) sm.ncand = 0u;
+    __syncthreads();
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      kmn = min(kmn, sm.wmin[w]);
+      kmx = max(kmx, sm.wmax[w]);
+    }
+    const float lo = key_value(kmn);
+    const float range = __fsub_rn(key_value(kmx), lo);
+    const float scale = (float)kTopkBins / range;
+    // the same decision in every thread: a finite, non-zero spread
+    if (range > 0.f && scale > 0.f && scale <= 3.0e38f) {
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) {
+        if ((valid >> e) & 1u) atomicAdd(&sm.hist[key_bin(rk[e], lo, scale)], 1u);
+      }
+      __syncthreads();
+      // suffix counts: thread t scans bins kTopkBins-1-BPT*t-j (j < BPT), so
+      // thread order runs from the highest bin down
+      uint32_t hb[BPT], s = 0;
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) {
+        hb[j] = sm.hist[kTopkBins - 1 - BPT * tid - j];
+        s += hb[j];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+      __syncthreads();
+#pragma unroll
+      for (int w = 0; w < NW; ++w) incl += (w < warp) ? sm.wsum[w] : 0u;
+      uint32_t cum = incl - s;  // keys in bins above this thread's
+      if (cum < (uint32_t)k && (uint32_t)k <= incl) {  // exactly one thread
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+          if (cum + hb[j] >= (uint32_t)k) {
+            sm.bstar = kTopkBins - 1 - BPT * tid - j;
+            sm.bstar_above = cum;
+            break;
+          }
+          cum += hb[j];
+        }
+      }
+      __syncthreads();
+      const int bstar = sm.bstar;
+      const uint32_t above = sm.bstar_above;
+      if (sm.hist[bstar] <= (uint32_t)kTopkMaxCand) {  // same value in every thread
+        // the keys of the boundary bin, in any order
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          if (((valid >> e) & 1u) && key_bin(rk[e], lo, scale) == bstar) {
+            const uint32_t slot = atomicAdd(&sm.ncand, 1u);
+            if (slot < (uint32_t)kTopkMaxCand) {
+              sm.cand_key[slot] = rk[e];
+              sm.cand_idx[slot] = wbase + 32 * e + lane;
+            }
+          }
+        }
+        __syncthreads();
+        // exact rank inside the bin: larger score first, then lower index
+        const uint32_t need = (uint32_t)k - above;  // >= 1
+        const int nc = (int)min(sm.ncand, (uint32_t)kTopkMaxCand);
+        if (tid < nc) {
+          const uint32_t key = sm.cand_key[tid];
+          const int idx = sm.cand_idx[tid];
+          uint32_t rank = 0;
+          for (int j = 0; j < nc; ++j) {
+            const uint32_t kj = sm.cand_key[j];
+            rank += (kj > key || (kj == key && sm.cand_idx[j] < idx)) ? 1u : 0u;
+          }
+          if (rank < need) atomicOr(&sm.keepbits[idx >> 5], 1u << (idx & 31));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          const int j = wbase + 32 * e + lane;
+          bool kp = false;
+          if ((valid >> e) & 1u) {
+            const int bin = key_bin(rk[e], lo, scale);
+            kp = bin > bstar || (bin == bstar && ((sm.keepbits[j >> 5] >> (j & 31)) & 1u));
+          }
+          keep |= (Mask)(kp ? 1u : 0u) << e;
+        }
+        done = true;
+      }
+    }
+  }
+
+  if (!done) {
   // k-th largest key, two bits per pass: thr holds the digits found so far
   // (lower bits zero), cnt = #keys >= thr.
   uint32_t thr = 0, cnt = (uint32_t)nb;
@@ -84,7 +241,6 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     for (int v = 0; v < kTopkCands; ++v) c[v] = 0;
 #pragma unroll
     for (int e = 0; e < KPT; ++e) {
-      if (e >= per) break;
       const uint32_t dk = rk[e] >> shift;
 #pragma unroll
       for (int v = 0; v < kTopkCands; ++v) c[v] += (dk >= P + (uint32_t)(v + 1));
@@ -117,12 +273,9 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     }
   }
 
-  const unsigned lt = (1u << lane) - 1u;
-  Mask keep = 0;
   if (exact) {  // exactly the keys >= thr
 #pragma unroll
     for (int e = 0; e < KPT; ++e) {
-      if (e >= per) break;
       const bool kp = ((valid >> e) & 1u) && rk[e] >= thr;
       keep |= (Mask)(kp ? 1u : 0u) << e;
     }
@@ -130,7 +283,6 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     uint32_t a_w = 0, t_w = 0;
 #pragma unroll
     for (int e = 0; e < KPT; ++e) {
-      if (e >= per) break;
       const bool v = (valid >> e) & 1u;
       a_w += __popc(__ballot_sync(0xffffffffu, v && rk[e] > thr));
       t_w += __popc(__ballot_sync(0xffffffffu, v && rk[e] == thr));
@@ -149,7 +301,6 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     const uint32_t need = (uint32_t)k - above;  // >= 1: thr is the k-th largest
 #pragma unroll
     for (int e = 0; e < KPT; ++e) {
-      if (e >= per) break;
       const bool v = (valid >> e) & 1u;
       const bool tie = v && rk[e] == thr;
       const unsigned b = __ballot_sync(0xffffffffu, tie);
@@ -158,11 +309,11 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
       rank += __popc(b);
     }
   }
+  }  // radix search
   // compaction in index order: exactly k entries are kept
   uint32_t k_w = 0;
 #pragma unroll
   for (int e = 0; e < KPT; ++e) {
-    if (e >= per) break;
     k_w += __popc(__ballot_sync(0xffffffffu, (keep >> e) & 1u));
   }
   if (lane == 0) sm.kept[warp] = k_w;
@@ -172,12 +323,24 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
   for (int w = 0; w < NW; ++w) pos += (w < warp) ? sm.kept[w] : 0u;
 #pragma unroll
   for (int e = 0; e < KPT; ++e) {
-    if (e >= per) break;
     const bool kp = (keep >> e) & 1u;
     const unsigned b = __ballot_sync(0xffffffffu, kp);
     if (kp) out[pos + __popc(b & lt)] = wbase + 32 * e + lane;
     pos += __popc(b);
   }
+}
+
+// cta_topk with the fewest keys per thread that hold nb scores (the same
+// choice in every thread of the CTA).
+template <int NT, int KMAX>
+__device__ void cta_topk_fit(const float* sc, int nb, int k_req, int32_t* out, int kmax,
+                             TopkSmem<NT, KMAX>& sm) {
+  if (KMAX > 4 && nb <= NT * 4)
+    cta_topk<NT, (KMAX > 4 ? 4 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm);
+  else if (KMAX > 8 && nb <= NT * 8)
+    cta_topk<NT, (KMAX > 8 ? 8 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm);
+  else
+    cta_topk<NT, KMAX, KMAX>(sc, nb, k_req, out, kmax, sm);
 }
 
 }  // namespace sva

@@ -103,6 +103,64 @@ def test_select_blocks_exact(nb, k):
             assert (s[b, h, kk:] == -1).all()
 
 
+def _score_patterns(nb, g):
+    """Score rows that stress the selection: outliers, many ties, extreme
+    and tiny ranges, signed zeros, one-ulp steps, a wide plateau at the
+    boundary, all equal."""
+    rows = []
+    rows.append(torch.randn(nb, generator=g) * 3)
+    x = torch.randn(nb, generator=g)
+    x[torch.randint(0, nb, (17,), generator=g)] += 40.0
+    rows.append(x)
+    rows.append(torch.randint(-20, 21, (nb,), generator=g).float() * 0.25)
+    x = torch.randn(nb, generator=g)
+    x[0], x[1] = 3e37, -3e37
+    rows.append(x)
+    rows.append(torch.full((nb,), 1.5))
+    rows.append(torch.randn(nb, generator=g) * 1e-30)
+    x = torch.zeros(nb)
+    x[::3] = -0.0
+    x[5] = 1.0
+    rows.append(x)
+    rows.append(1.0 + torch.randint(0, 4, (nb,), generator=g).float() * 2.0**-23)
+    x = torch.randn(nb, generator=g)
+    x[: nb // 2] = 7.0
+    rows.append(x)
+    return torch.stack(rows).float()
+
+
+@pytest.mark.parametrize("nb,k", [(2048, 128), (2048, 1), (8192, 512), (300, 299), (9000, 700)])
+def test_score_select_adversarial_scores(nb, k):
+    """Scores planted exactly through the representatives (one non-zero
+    dimension, draft-0 queries of 1.0, so score = G * value in fp32) run
+    through the fused score + select kernel (nb <= 8192) or the score
+    kernel and the standalone select: the selection must equal the
+    oracle's bit for bit."""
+    g = torch.Generator().manual_seed(nb + k)
+    vals = _score_patterns(nb, g)                  # [H, nb]
+    H, G, d, blk = vals.shape[0], 4, 64, 16
+    shape = api.make_shape(1, H * G, H, d, blk, 2, torch.bfloat16)
+    q = torch.zeros(1, 2, H * G, d, dtype=torch.bfloat16)
+    q[0, 0, :, 0] = 1.0
+    reps = torch.zeros(1, H, nb, d)
+    reps[0, :, :, 0] = vals
+    pool = torch.zeros(1, H, blk, d, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(1, nb, dtype=torch.int32, device="cuda")
+    kv = api.make_kv(pool, pool, bt, nb * blk)
+    kmax = k + 2
+    sel = torch.full((1, H, kmax), 7, dtype=torch.int32, device="cuda")
+    ws = api.alloc_workspace(shape, nb, kmax)
+    got_k = api.sv_score_select(shape, q.cuda(), reps.cuda(), kv,
+                                W.Budget(W.BUDGET_FIXED, k, 0, 0, 0, 0, 0), sel, kmax, ws)
+    torch.cuda.synchronize()
+    assert got_k == k and api.sv_read_status(ws) == 0
+    s = sel.cpu()
+    for h in range(H):
+        want = O.select_blocks((vals[h] * G).tolist(), k)
+        assert s[0, h, :k].tolist() == want, (h, nb, k)
+        assert (s[0, h, k:] == -1).all()
+
+
 def test_score_select_vs_oracle():
     wl = small_wl(ctx=64 * 150, budget=W.Budget(W.BUDGET_FIXED, 21, 0, 0, 0, 0, 0))
     x = W.make_layer(wl)
