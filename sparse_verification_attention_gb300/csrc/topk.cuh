@@ -20,11 +20,14 @@
 // [min, max] into kTopkBins bins. The binning is monotone: a higher bin only
 // holds strictly larger scores. One shared histogram and a suffix scan give
 // the bin b* holding the k-th largest score. Every key above b* is kept, and
-// every key below it is dropped. The keys of b* (at most kTopkMaxCand) are
-// ranked exactly against each other by (score descending, index
-// ascending), and the first k - (keys above b*) of them are kept. A boundary
-// bin with more keys, equal scores everywhere, or non-finite extremes fall
-// back to the radix search below.
+// every key below it is dropped. Order keys by the composite
+// (key << 32 | ~index): a larger score first, then the lower index. The keys
+// of b* (at most kTopkMaxCand) are ranked against each other by that
+// composite. The one of rank k - (keys above b*) - 1 is the threshold T, and
+// a key is kept if and only if its composite is >= T. Keys above b* pass and
+// keys below it fail automatically. A boundary bin with more keys, equal
+// scores everywhere, or non-finite extremes fall back to the radix search
+// below.
 //
 // Radix search. The k-th largest key is found two bits
 // per pass from the most significant end: each warp counts its keys at or
@@ -74,12 +77,16 @@ struct TopkSmem {
   uint32_t above[NT / 32], ties[NT / 32], kept[NT / 32];
   uint32_t wmin[NT / 32], wmax[NT / 32], wsum[NT / 32];
   uint32_t hist[kTopkBins];
-  uint32_t keepbits[(NT * KPT + 31) / 32];  // kept keys of the boundary bin, by index
-  uint32_t cand_key[kTopkMaxCand];
-  int32_t cand_idx[kTopkMaxCand];
+  unsigned long long cand[kTopkMaxCand];  // composites of the boundary bin's keys
+  unsigned long long thr;                 // the threshold composite T
   int bstar;
   uint32_t bstar_above, ncand;
 };
+
+// Larger score first, then the lower index: (key << 32) | ~index.
+__device__ __forceinline__ unsigned long long topk_composite(uint32_t key, int idx) {
+  return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)idx;
+}
 
 // All NT threads of the CTA call this once. sc: nb scores (global, read
 // through L2 only: other CTAs of the grid may have just written them);
@@ -134,7 +141,6 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
       sm.wmax[warp] = lmax;
     }
     for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0u;
-    for (int i = tid; i < (nb + 31) / 32; i += NT) sm.keepbits[i] = 0u;
     if (tid == 0) sm.ncand = 0u;
     __syncthreads();
     uint32_t kmn = 0xffffffffu, kmx = 0u;
@@ -192,35 +198,28 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
         for (int e = 0; e < KPT; ++e) {
           if (((valid >> e) & 1u) && key_bin(rk[e], lo, scale) == bstar) {
             const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-            if (slot < (uint32_t)kTopkMaxCand) {
-              sm.cand_key[slot] = rk[e];
-              sm.cand_idx[slot] = wbase + 32 * e + lane;
-            }
+            if (slot < (uint32_t)kTopkMaxCand)
+              sm.cand[slot] = topk_composite(rk[e], wbase + 32 * e + lane);
           }
         }
         __syncthreads();
-        // exact rank inside the bin: larger score first, then lower index
+        // the composites are distinct, so exactly one candidate has rank
+        // need - 1 (need <= the bin's count)
         const uint32_t need = (uint32_t)k - above;  // >= 1
         const int nc = (int)min(sm.ncand, (uint32_t)kTopkMaxCand);
         if (tid < nc) {
-          const uint32_t key = sm.cand_key[tid];
-          const int idx = sm.cand_idx[tid];
+          const unsigned long long c = sm.cand[tid];
           uint32_t rank = 0;
-          for (int j = 0; j < nc; ++j) {
-            const uint32_t kj = sm.cand_key[j];
-            rank += (kj > key || (kj == key && sm.cand_idx[j] < idx)) ? 1u : 0u;
-          }
-          if (rank < need) atomicOr(&sm.keepbits[idx >> 5], 1u << (idx & 31));
+#pragma unroll 4
+          for (int j = 0; j < nc; ++j) rank += (sm.cand[j] > c) ? 1u : 0u;
+          if (rank == need - 1) sm.thr = c;
         }
         __syncthreads();
+        const unsigned long long thr_c = sm.thr;
 #pragma unroll
         for (int e = 0; e < KPT; ++e) {
-          const int j = wbase + 32 * e + lane;
-          bool kp = false;
-          if ((valid >> e) & 1u) {
-            const int bin = key_bin(rk[e], lo, scale);
-            kp = bin > bstar || (bin == bstar && ((sm.keepbits[j >> 5] >> (j & 31)) & 1u));
-          }
+          const bool kp = ((valid >> e) & 1u) &&
+                          topk_composite(rk[e], wbase + 32 * e + lane) >= thr_c;
           keep |= (Mask)(kp ? 1u : 0u) << e;
         }
         done = true;
