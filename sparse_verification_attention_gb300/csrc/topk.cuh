@@ -67,8 +67,8 @@ constexpr int kTopkMaxCand = 256;                      // largest boundary bin i
 // non-negative value is a floor), and the same instructions wherever used.
 __device__ __forceinline__ int key_bin(uint32_t key, float lo, float scale) {
   const float x = __fmul_rn(__fsub_rn(key_value(key), lo), scale);  // >= 0
-  const int i = __float2int_rz(x);
-  return i < kTopkBins - 1 ? i : kTopkBins - 1;
+  const int i = __float2int_rz(x);  // NaN gives 0; the clamps keep any value in range
+  return i <= 0 ? 0 : (i < kTopkBins - 1 ? i : kTopkBins - 1);
 }
 
 template <int NT, int KPT>
@@ -141,7 +141,11 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
       sm.wmax[warp] = lmax;
     }
     for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0u;
-    if (tid == 0) sm.ncand = 0u;
+    if (tid == 0) {
+      sm.ncand = 0u;
+      sm.bstar = 0;  // overwritten below; a valid index whatever happens
+      sm.bstar_above = 0u;
+    }
     __syncthreads();
     uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
