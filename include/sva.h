@@ -36,7 +36,8 @@
  *     non-OK status of the calling thread.
  *   - Limits: 1 <= T <= 64; Hq % Hkv == 0; d % 8 == 0 and 8 <= d <= 256;
  *     NB = ctx/blk full blocks <= 16384; a partial last block (ctx % blk
- *     tokens) is allowed.
+ *     tokens) is allowed; B <= 64 when the cache gives per-sequence
+ *     lengths (sv_kv.seq_ctx).
  */
 #ifndef SVA_H_
 #define SVA_H_

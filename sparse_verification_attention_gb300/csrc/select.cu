@@ -9,7 +9,7 @@
 //
 // Method: one CTA per (b, h) running the CTA top-k of topk.cuh with every
 // score held in registers (512 threads x 32 keys covers the largest block
-// count the library accepts).
+// count the library accepts; smaller counts take 4 or 8 keys per thread).
 #include "internal.h"
 #include "ptx.h"
 #include "topk.cuh"
