@@ -163,7 +163,8 @@ sv_status sv_read_status(const void* workspace, uint32_t* flags, void* stream);
  * sequence. reps: [B, Hkv, nb_max, d] fp32, written only at those j. Call it
  * over all full blocks after prefill and again for each block that fills
  * up. Requires first_block >= 0, n_blocks >= 0, first_block + n_blocks <=
- * ctx/blk. */
+ * ctx/blk (with per-sequence lengths: the longest sequence's full blocks;
+ * blocks at or past a shorter sequence's own ctx_b/blk are skipped for it). */
 sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block,
                         int n_blocks, float* reps, void* stream);
 
@@ -172,7 +173,10 @@ sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block,
  *   scores[b][h][j] = sum_{g<G} < Q[b][0][h*G+g][:], reps[b][h][j][:] >
  * (draft 0's query; a KV head's score sums its G query heads' dot products;
  * no 1/sqrt(d), which does not change the ranking).
- * q: [B, T, Hq, d]; reps: [B, Hkv, nb_max, d]; scores: [B, Hkv, NB] fp32. */
+ * q: [B, T, Hq, d]; reps: [B, Hkv, nb_max, d]; scores: [B, Hkv, NB] fp32.
+ * With per-sequence lengths NB is the longest sequence's full blocks (the
+ * row stride); entries at or past sequence b's own ctx_b/blk are not
+ * written. */
 sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* reps,
                           const sv_kv* kv, float* scores, void* stream);
 
@@ -208,6 +212,10 @@ sv_status sv_score_select(const sv_shape* shape, const void* q, const float* rep
  * sel == NULL selects all NB blocks in order: dense full verification
  * attention [SpecPV], the comparison baseline (n_sel is then ignored).
  * A partial last block (ctx % blk tokens) is attended in every case.
+ * With per-sequence lengths, sel == NULL takes each sequence's own full
+ * blocks, and a given sel must hold n_sel valid blocks of that sequence in
+ * every row (the same n_sel for all; sv_verify_layer instead uses each
+ * sequence's own budget).
  * sel: [B, Hkv, sel_stride] int32 with n_sel <= sel_stride.
  * q: [B, T, Hq, d]; draft_k, draft_v: [B, T, Hkv, d]; out: [B, T, Hq, d].
  * The workspace holds the split-KV partial results (its size from
