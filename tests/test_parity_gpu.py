@@ -80,7 +80,8 @@ def test_score_blocks(dtype, d, G):
 
 
 @pytest.mark.parametrize("nb,k", [(64, 8), (512, 64), (2048, 128), (1000, 999), (37, 37), (37, 50),
-                                  (1, 1), (16384, 1024), (300, 0)])
+                                  (1, 1), (16384, 1024), (300, 0), (3000, 200), (4096, 4000),
+                                  (5000, 1)])
 def test_select_blocks_exact(nb, k):
     """Host-made scores with many ties (small integers), +-0 and negatives:
     the GPU selection must equal the oracle's, bit for bit."""
