@@ -16,7 +16,7 @@ Sources (page title, then the part of the page):
              generation via partial verification", introduction (full vs.
              partial verification).
 
-Readings where the pages are silent (every one is listed in the design doc):
+Readings where the pages are silent, ambiguous or garbled:
   R1 block representative = mean of the block's keys (the pages never define
      it); computed in fp64.
   R2 the scoring query is draft 0's (tree root's) query; with grouped-query
