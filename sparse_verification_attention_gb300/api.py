@@ -144,10 +144,14 @@ def make_kv(k_pool: torch.Tensor, v_pool: Optional[torch.Tensor], block_table: t
             ctx: int, seq_ctx: Optional[Sequence[int]] = None) -> KV:
     """The cache descriptor. seq_ctx (one prefix length per sequence, kept on
     the host) replaces the uniform ctx; the returned structure owns the
-    array it points to."""
+    array it points to. The library reads B entries of it, so it must have
+    one per row of the block table."""
     kv = KV(k_pool.data_ptr(), None if v_pool is None else v_pool.data_ptr(),
             block_table.data_ptr(), block_table.shape[1], k_pool.shape[0], ctx)
     if seq_ctx is not None:
+        if len(seq_ctx) != block_table.shape[0]:
+            raise ValueError(f"seq_ctx has {len(seq_ctx)} entries for "
+                             f"{block_table.shape[0]} sequences")
         arr = (C.c_int32 * len(seq_ctx))(*[int(c) for c in seq_ctx])
         kv._seq_ctx_keep = arr
         kv.seq_ctx = C.cast(arr, C.POINTER(C.c_int32))

@@ -225,3 +225,35 @@ def test_make_kv_keeps_seq_ctx_alive():
     kv = api.make_kv(t, t, bt, 0, [100, 7])
     assert [kv.seq_ctx[i] for i in range(2)] == [100, 7]
     assert not api.make_kv(t, t, bt, 50).seq_ctx  # NULL: the uniform ctx
+
+
+def test_make_kv_rejects_short_seq_ctx():
+    t = torch.zeros(4, 2, 16, 64)
+    bt = torch.zeros(3, 8, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        api.make_kv(t, t, bt, 0, [100, 7])  # 2 lengths for 3 sequences
+
+
+def test_per_sequence_budget_checked_against_kmax(L):
+    """With per-sequence lengths the largest per-sequence budget must fit
+    kmax; it is checked before anything is launched."""
+    s = api.make_shape(2, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20
+    kv = api.KV(fake, fake, fake, 64, 64, 0)
+    arr = (C.c_int32 * 2)(16 * 10, 16 * 40)  # 10 and 40 full blocks
+    kv.seq_ctx = C.cast(arr, C.POINTER(C.c_int32))
+    b = api.make_budget(W.Budget(W.BUDGET_FIXED, 30, 0, 0, 0, 0, 0))  # k_b = 10, 30
+    k = C.c_int(-1)
+    ws_n = api.sv_workspace_bytes(s, 64, 30)
+    st, msg = _status(L, L.sv_score_select, C.byref(s), fake, fake, C.byref(kv), C.byref(b),
+                      fake, 29, C.byref(k), fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "k=30 exceeds kmax=29" in msg
+    st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), fake, C.byref(b), fake,
+                      fake, None, 0, fake, 29, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "k=30 exceeds kmax=29" in msg
+    # one sequence too long for the block table's width
+    arr2 = (C.c_int32 * 2)(16, 16 * 64 + 1)  # needs 65 columns
+    kv.seq_ctx = C.cast(arr2, C.POINTER(C.c_int32))
+    st, msg = _status(L, L.sv_score_select, C.byref(s), fake, fake, C.byref(kv), C.byref(b),
+                      fake, 30, C.byref(k), fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "nb_max" in msg
