@@ -339,7 +339,14 @@ def test_value_ones_gives_ones():
 # ------------------------------------------------------------------ verify layer
 def _verify_vs_oracle(wl, x, xd, pairs=None):
     """Run sv_verify_layer on the device, recompute (b, h) pairs on the CPU
-    oracle (all pairs by default) and compare selection and outputs."""
+    oracle (all pairs by default) and compare selection and outputs.
+
+    The selection must equal the oracle's bit for bit, except inside a
+    boundary band (oracle boundary gap below 1e-4 relative), where either
+    choice is correct. Outputs are then compared element by element for
+    every pair against the oracle's attention over the set the GPU actually
+    used: that set is the oracle's own wherever the two agree, so no pair
+    goes unchecked. Returns (max abs error, pairs whose set differed)."""
     st = api.LayerState(wl, xd)
     out = st.verify()
     torch.cuda.synchronize()
@@ -352,26 +359,23 @@ def _verify_vs_oracle(wl, x, xd, pairs=None):
     by_b = {}
     for b, h in pairs:
         by_b.setdefault(b, []).append(h)
-    worst = 0.0
+    worst, n_differ = 0.0, 0
     for b, hs in by_b.items():
         qb = x.q[b:b + 1]
         btb = x.block_table[b:b + 1]
         reps = O.block_representatives(x.k_pool, btb, wl.NB, wl.blk)
         scores = O.block_scores(qb, reps, wl.G)
-        sub_scores = scores[:, hs]
-        differ = U.compare_selection(gsel[b:b + 1, hs], sub_scores, k)
-        sel = O.select_all(scores, k)
-        ref = O.sparse_attend(qb, x.k_pool, x.v_pool, btb, sel, x.draft_k[b:b + 1],
+        n_differ += len(U.compare_selection(gsel[b:b + 1, hs], scores[:, hs], k))
+        used = gsel[b:b + 1, :, :k].long()
+        ref = O.sparse_attend(qb, x.k_pool, x.v_pool, btb, used, x.draft_k[b:b + 1],
                               x.draft_v[b:b + 1], wl.parent_list(), tail_block=wl.NB,
                               tail_len=wl.ctx % wl.blk)
-        for i, h in enumerate(hs):
-            if (0, i) in differ:
-                continue
+        for h in hs:
             cols = slice(h * wl.G, (h + 1) * wl.G)
             err = (gout[b:b + 1, :, cols].double() - ref[:, :, cols]).abs().max().item()
             worst = max(worst, err)
             assert err <= U.out_atol(wl.torch_dtype), (b, h, err)
-    return worst
+    return worst, n_differ
 
 
 def test_repeated_calls_identical():
@@ -444,31 +448,37 @@ def test_verify_short_context_keeps_all_blocks():
 
 
 @pytest.mark.slow
-def test_verify_llama8b_128k_b4_sampled():
+def test_verify_llama8b_128k_b4_all_pairs():
+    """The benchmark workload (B4, 128K context, 128 of 2048 blocks), every
+    (sequence, KV head) pair against the oracle."""
     wl = W.WORKLOADS["llama8b_128k_b4"]
     xd = W.make_layer(wl, device="cuda")
     x = xd.to("cpu")
-    _verify_vs_oracle(wl, x, xd, pairs=[(0, 0), (1, 5), (3, 7), (2, 2)])
+    _verify_vs_oracle(wl, x, xd)
 
 
 @pytest.mark.slow
-def test_verify_qwen3moe_tree_sampled():
+def test_verify_qwen3moe_tree_all_pairs():
+    """Qwen3-MoE-shaped tree workload (B8, G8, T16 tree, 128 of 1024 blocks),
+    every pair against the oracle."""
     wl = W.WORKLOADS["qwen3moe_64k_b8_tree16"]
     xd = W.make_layer(wl, device="cuda")
     x = xd.to("cpu")
-    _verify_vs_oracle(wl, x, xd, pairs=[(0, 0), (3, 1), (7, 3), (5, 2)])
+    _verify_vs_oracle(wl, x, xd)
 
 
 @pytest.mark.slow
 def test_stack_llama8b_60k_reuse():
-    """32-layer stack with selection recomputed every 2nd layer: reuse layers
-    attend to exactly the previous layer's selection; layers 0..3 against the
-    oracle stack, every layer's output finite."""
+    """32-layer stack with the selection recomputed every 2nd layer, every
+    layer against the oracle: a computing layer's selection against the
+    oracle's top-k of that layer (bit-exact outside a boundary band), a reuse
+    layer's selection bit-identical to the computing layer's, and every
+    layer's output against the oracle layer (oracle.verify_layer, which is
+    what oracle.verify_stack runs per layer) attending over that selection."""
     wl = W.WORKLOADS["llama8b_60k_32layer"]
     ps = W.planted_sets(wl)
-    sels, outs, states = [], [], []
-    cpu_layers = []
     prev = None
+    oracle_sel = None
     for l in range(wl.layers):
         xd = W.make_layer(wl, l, device="cuda", planted=ps[l])
         st = api.LayerState(wl, xd)
@@ -477,26 +487,28 @@ def test_stack_llama8b_60k_reuse():
             st.sel = prev.sel.clone()
         st.verify(reuse=int(reuse))
         torch.cuda.synchronize()
-        sels.append(st.sel.cpu())
-        outs.append(st.out.cpu())
-        if l < 4:
-            x = xd.to("cpu")
-            cpu_layers.append((x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k, x.draft_v))
-        prev = st
-        del xd
-    for l in range(1, wl.layers, 2):
-        assert torch.equal(sels[l], sels[l - 1])
-    for o in outs:
-        assert torch.isfinite(o.float()).all()
-    ref_outs, ref_sels = O.verify_stack(cpu_layers, wl.parent_list(), wl.ctx, wl.blk, wl.budget,
-                                        wl.compute_every)
-    for l in range(4):
-        if l % 2 == 0:
-            reps = O.block_representatives(cpu_layers[l][1], cpu_layers[l][3], wl.NB, wl.blk)
-            scores = O.block_scores(cpu_layers[l][0], reps, wl.G)
-            differ = U.compare_selection(sels[l], scores, ref_sels[l].shape[-1])
-            assert not differ
-        U.compare_out(outs[l], ref_outs[l], U.BF16_ATOL)
+        assert api.sv_read_status(st.ws) == 0
+        gsel, gout = st.sel.cpu(), st.out.cpu()
+        x = xd.to("cpu")
+        if reuse:
+            assert torch.equal(gsel, prev_sel), l
+            ref, _, _ = O.verify_layer(x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k,
+                                       x.draft_v, wl.parent_list(), wl.ctx, wl.blk, wl.budget,
+                                       reuse_sel=used)
+        else:
+            ref, oracle_sel, scores = O.verify_layer(x.q, x.k_pool, x.v_pool, x.block_table,
+                                                     x.draft_k, x.draft_v, wl.parent_list(),
+                                                     wl.ctx, wl.blk, wl.budget)
+            k = oracle_sel.shape[-1]
+            differ = U.compare_selection(gsel, scores, k)
+            used = gsel[:, :, :k].long()
+            if differ:  # the oracle's attention over the set the GPU used
+                ref, _, _ = O.verify_layer(x.q, x.k_pool, x.v_pool, x.block_table, x.draft_k,
+                                           x.draft_v, wl.parent_list(), wl.ctx, wl.blk,
+                                           wl.budget, reuse_sel=used)
+        U.compare_out(gout, ref, U.BF16_ATOL)
+        prev, prev_sel = st, gsel
+        del xd, x
 
 
 # ------------------------------------------------------------------ device-side checks
@@ -632,8 +644,11 @@ def test_verify_append_verify_loop():
     assert torch.equal(xd.k_pool.cpu(), kn) and torch.equal(xd.v_pool.cpu(), vn)
     ref2, sel2, scores2 = O.verify_layer(q2, kn, vn, x.block_table, dk2, dv2, wl.parent_list(),
                                          wl2.ctx, wl.blk, wl.budget)
-    differ = U.compare_selection(st2.sel.cpu(), scores2, st2.k)
-    assert not differ
+    if U.compare_selection(st2.sel.cpu(), scores2, st2.k):
+        # a boundary-band difference: the oracle over the set the GPU used
+        ref2, _, _ = O.verify_layer(q2, kn, vn, x.block_table, dk2, dv2, wl.parent_list(),
+                                    wl2.ctx, wl.blk, wl.budget,
+                                    reuse_sel=st2.sel.cpu()[:, :, :st2.k].long())
     U.compare_out(out2, ref2, U.BF16_ATOL)
 
 

@@ -77,13 +77,14 @@ def _check_verify(wl, x, seq_ctx, heads=None, st=None):
     heads = list(range(wl.Hkv)) if heads is None else heads
     atol = U.out_atol(wl.torch_dtype)
     for b, c in enumerate(seq_ctx):
-        ref, _, scores, k = _oracle_seq(wl, x, b, c)
+        _, _, scores, k = _oracle_seq(wl, x, b, c)
         assert k <= st.kmax
-        differ = U.compare_selection(gsel[b:b + 1, heads], scores[:, heads], k)
+        U.compare_selection(gsel[b:b + 1, heads], scores[:, heads], k)
         assert all(int(v) == -1 for v in gsel[b, :, k:].flatten().tolist())
-        for i, h in enumerate(heads):
-            if (0, i) in differ:
-                continue
+        # every pair against the oracle's attention over the set the GPU used
+        # (the oracle's own outside a boundary band)
+        ref, _, _, _ = _oracle_seq(wl, x, b, c, sel=gsel[b:b + 1, :, :k].long())
+        for h in heads:
             cols = slice(h * wl.G, (h + 1) * wl.G)
             err = (gout[b:b + 1, :, cols].double() - ref[:, :, cols]).abs().max().item()
             assert err <= atol, (b, c, h, err)
@@ -137,13 +138,13 @@ def test_verify_per_sequence_budgets(name, budget, ks):
     assert st.k == max(ks)
 
 
-def test_verify_llama8b_mixed_lengths_sampled():
-    """Llama-3.1-8B-shaped layer, four sequences from 1K to 32K tokens;
-    two KV heads of each sequence recomputed on the oracle."""
+def test_verify_llama8b_mixed_lengths():
+    """Llama-3.1-8B-shaped layer, four sequences from 1K to 32K tokens; every
+    KV head of every sequence recomputed on the oracle."""
     wl = replace(W.WORKLOADS["llama8b_32k"], B=4, ctx=32768 + 40, permute_pages=True)
     seq_ctx = [32768 + 40, 8192 + 17, 20000, 1000]
     x = _layer(wl, seq_ctx)
-    _check_verify(wl, x, seq_ctx, heads=[0, 7])
+    _check_verify(wl, x, seq_ctx)
 
 
 def test_reuse_and_full_modes_per_sequence():
@@ -162,13 +163,11 @@ def test_reuse_and_full_modes_per_sequence():
     assert api.sv_read_status(st1.ws) == 0
     gsel0 = st0.sel.cpu()
     for b, c in enumerate(seq_ctx):
-        _, sel0, scores0, k = _oracle_seq(wl, x0, b, c)
-        same = [h for h in range(wl.Hkv) if gsel0[b, h, :k].tolist() == sel0[0, h].tolist()]
-        ref, _, _, _ = _oracle_seq(wl, x1, b, c, sel=sel0)
-        for h in same:
-            cols = slice(h * wl.G, (h + 1) * wl.G)
-            err = (out_reuse[b:b + 1, :, cols].double().cpu() - ref[:, :, cols]).abs().max().item()
-            assert err <= U.BF16_ATOL, ("reuse", b, h, err)
+        _, _, scores0, k = _oracle_seq(wl, x0, b, c)
+        U.compare_selection(gsel0[b:b + 1], scores0, k)  # checked again: the set reused
+        # the reuse layer attends over layer 0's selection as the GPU made it
+        ref, _, _, _ = _oracle_seq(wl, x1, b, c, sel=gsel0[b:b + 1, :, :k].long())
+        U.compare_out(out_reuse[b:b + 1], ref, U.BF16_ATOL)
         nb = c // wl.blk
         every = torch.arange(nb, dtype=torch.int64).expand(1, wl.Hkv, nb)
         ref_full, _, _, _ = _oracle_seq(wl, x1, b, c, sel=every)
