@@ -311,10 +311,10 @@ class StepSet:
             x = W.make_layer(wl, index * wl.layers + l, device="cuda",
                              planted=layers_planted[l])
             self.layers.append(api.LayerState(wl, x))
-        # reuse layers share the computing layer's selection buffer
+        # reuse layers share the computing layer's selection slot
         for l in range(wl.layers):
             if l % wl.compute_every:
-                self.layers[l].sel = self.layers[l - (l % wl.compute_every)].sel
+                self.layers[l].slot = self.layers[l - (l % wl.compute_every)].slot
 
 
 def run_step(wl, ss: StepSet, ev=None):
@@ -536,7 +536,7 @@ def run_e2e(args, wl, sets, dist):
             st.x.draft_v.copy_(hv, non_blocking=True)
             reuse = int(l % wl.compute_every != 0)
             api.sv_verify_layer(st.shape, st.x.q, st.kv, st.reps, wl.budget, st.x.draft_k,
-                                st.x.draft_v, st.parents, reuse, st.sel, st.kmax, st.out, st.ws)
+                                st.x.draft_v, st.parents, reuse, st.slot, st.out, st.ws)
             ho.copy_(st.out, non_blocking=True)
 
     for i in range(3):

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 3
+#define SV_ABI_VERSION 4
 
 typedef enum {
   SV_OK = 0,
@@ -253,25 +253,47 @@ typedef struct {
 } sv_plan;
 sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_plan* out);
 
+/* Selection cache slot for inter-layer retrieval reuse [SV-Tut1] (core
+ * technique 1, the paragraph on letting some layers reuse the previous
+ * layer's retrieval): a layer may reuse only a selection that a computing
+ * layer actually wrote for the same problem.
+ *   sel:   DEVICE int32 [B, Hkv, kmax], caller-owned;
+ *   kmax:  its row length (>= every budget it will hold);
+ *   stamp: HOST-side digest, written by sv_verify_layer when it computes a
+ *          selection into the slot (reuse == 0): a digest of B, Hkv, blk,
+ *          kmax, the context length of every sequence and the budget k of
+ *          every sequence. A reuse call (reuse == 1) computes the same digest
+ *          for its own arguments and returns SV_ERR_INVALID_ARG, launching
+ *          nothing, when the slot's stamp differs (a slot never written, or
+ *          written for another context length, budget or shape). Set it to 0
+ *          when the slot is created; copy it with the device contents when
+ *          the slot is copied. */
+typedef struct {
+  int32_t* sel;
+  int kmax;
+  uint64_t stamp;
+} sv_sel_slot;
+
 /* One layer of sparse verification [SV-Fig1], [SV-Tut1], [SV-Abs]:
- *   reuse == 0: sv_score_select into sel_cache, then sv_sparse_attend on it;
+ *   reuse == 0: sv_score_select into slot->sel, then sv_sparse_attend on it,
+ *               and slot->stamp set for this call;
  *   reuse == 1: inter-layer retrieval reuse -- no scoring or selection; the
- *               selection already in sel_cache (written by an earlier
- *               reuse == 0 call with the same shape, kv->ctx and budget) is
- *               attended to as is.
+ *               selection already in slot->sel, written by an earlier
+ *               reuse == 0 call for the same shape, context lengths and
+ *               budget (checked through slot->stamp), is attended to as is.
  *   reuse == 2: full verification [SpecPV] -- every block of the context is
  *               attended (as sv_sparse_attend with sel == NULL), for the
  *               periodic full-verification steps that partial verification
- *               interleaves; reps, budget and sel_cache are not used (may be
- *               NULL) and sel_cache keeps its contents.
- * reps may be NULL when reuse != 0. sel_cache: [B, Hkv, kmax] int32, in/out.
- * *k_out (host, may be NULL) receives the number of blocks attended. */
+ *               interleaves; reps, budget and the slot are not used (slot may
+ *               be NULL) and the slot keeps its contents and stamp.
+ * reps may be NULL when reuse != 0. *k_out (host, may be NULL) receives the
+ * number of blocks attended. */
 sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           const float* reps, const sv_budget* budget,
                           const void* draft_k, const void* draft_v,
-                          const int32_t* draft_parent, int reuse, int32_t* sel_cache,
-                          int kmax, int* k_out, void* out, void* workspace,
-                          size_t ws_bytes, void* stream);
+                          const int32_t* draft_parent, int reuse, sv_sel_slot* slot,
+                          int* k_out, void* out, void* workspace, size_t ws_bytes,
+                          void* stream);
 
 /* Acceptance write-back: the step after verification. The pages have no
  * formula for it; it closes the loop that [SV-Fig1] verifies one step of:
@@ -295,6 +317,28 @@ sv_status sv_append_kv(const sv_shape* shape, void* k_pool, void* v_pool,
                        const int32_t* seq_ctx, const int32_t* n_accept,
                        const int32_t* accept_idx, const void* draft_k, const void* draft_v,
                        float* reps, void* workspace, void* stream);
+
+/* Overlap of per-draft block selections: the measurement behind the figure
+ * that follows the Figure 1 caption of [SV-Fig1] (overlap of the KV block
+ * selection for draft-token pairs at different position distances), which
+ * is the evidence that draft 0's set can serve every draft. The caller
+ * scores and selects once per draft t with draft t's own query (for
+ * example sv_score_blocks and sv_select_blocks on a T = 1 view of q) and
+ * passes the T selections:
+ *   sels: DEVICE int32 [T, pairs, kmax]; row (t, p) holds draft t's k kept
+ *         blocks of pair p in ascending order (entries past k are ignored);
+ *   draft_parent: HOST int[T] as in sv_sparse_attend (NULL = chain). A
+ *         draft's position is ctx + its depth in the tree, so the position
+ *         distance of drafts t and u is |depth(t) - depth(u)| (|t - u| in a
+ *         chain); this is the library's reading of "position distance".
+ * Writes (DEVICE float32):
+ *   overlap0[p][t]    = |S_0 ∩ S_t| / k;
+ *   by_distance[p][d] = mean of |S_t ∩ S_u| / k over draft pairs t < u at
+ *                       distance d, NaN where no pair has distance d.
+ * 1 <= T <= 64, 1 <= k <= kmax. Asynchronous on stream. */
+sv_status sv_selection_overlap(const int32_t* sels, int T, int pairs, int kmax, int k,
+                               const int32_t* draft_parent, float* overlap0,
+                               float* by_distance, void* stream);
 
 /* sv_sparse_attend without a workspace. The paper has no counterpart: this
  * entry exists for callers that cannot allocate device memory, such as an

@@ -44,6 +44,9 @@ Readings where the pages are silent, ambiguous or garbled:
      get representatives and compete for the budget; the partial block's
      ctx % blk tokens are always attended, outside the budget. Accepted drafts
      are appended at positions ctx, ctx+1, ... in the order accepted.
+  R10 the position distance of two drafts (the overlap diagnostic) is the
+     difference of their depths in the draft tree: a draft sits at position
+     ctx + depth; in a chain that is |t - u|.
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
 against closed forms, brute force, invariants or torch SDPA, except R1's
@@ -362,6 +365,48 @@ def draft_selection_overlap(q: torch.Tensor, reps: torch.Tensor, G: int, k: int)
             s0 = set(sets[0][b, h].tolist())
             for t in range(T):
                 out[b, h, t] = len(s0 & set(sets[t][b, h].tolist())) / kk if kk else 1.0
+    return out
+
+
+def draft_depths(parents: Sequence[int]) -> list[int]:
+    """Depth of every draft in its tree (root 0); a chain's draft t has depth t."""
+    depth = []
+    for t, p in enumerate(parents):
+        depth.append(0 if p < 0 else depth[p] + 1)
+    return depth
+
+
+def draft_overlap_by_distance(q: torch.Tensor, reps: torch.Tensor, G: int, k: int,
+                              parents: Sequence[int]) -> torch.Tensor:
+    """The figure after [SV-Fig1]'s caption plots, for pairs of draft tokens, how much
+    the block sets their own queries would select overlap, against the pairs'
+    position distance. For every unordered pair of drafts t != u this takes
+    |S_t ∩ S_u| / k (S_t: the top-k blocks of draft t's own query, same
+    scoring and tie rule as draft 0's) and averages it over the pairs whose
+    distance is delta = |depth(t) - depth(u)| (reading R10: a draft sits at
+    position ctx + depth in its tree; in a chain delta = |t - u|).
+
+    q [B,T,Hq,d]; reps [B,Hkv,NB,d]. Returns fp64 [B, Hkv, T]: entry delta is
+    the mean overlap at that distance, NaN where no pair has it."""
+    B, T = q.shape[0], q.shape[1]
+    Hkv, NB = reps.shape[1], reps.shape[2]
+    kk = min(k, NB)
+    depth = draft_depths(parents)
+    sets = [select_all(block_scores(q[:, t:t + 1], reps, G), kk) for t in range(T)]
+    out = torch.full((B, Hkv, T), float("nan"), dtype=F64)
+    for b in range(B):
+        for h in range(Hkv):
+            sums, counts = [0.0] * T, [0] * T
+            for t in range(T):
+                st = set(sets[t][b, h].tolist())
+                for u in range(t + 1, T):
+                    delta = abs(depth[t] - depth[u])
+                    su = set(sets[u][b, h].tolist())
+                    sums[delta] += len(st & su) / kk if kk else 1.0
+                    counts[delta] += 1
+            for delta in range(T):
+                if counts[delta]:
+                    out[b, h, delta] = sums[delta] / counts[delta]
     return out
 
 

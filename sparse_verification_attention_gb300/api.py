@@ -25,12 +25,13 @@ SV_BF16, SV_F32 = 0, 1
 SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
 
 SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
-ABI_VERSION = 3  # SV_ABI_VERSION the structures below match
+ABI_VERSION = 4  # SV_ABI_VERSION the structures below match
 
 EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace_bytes",
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
             "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
-            "sv_verify_layer", "sv_sparse_attend_noalloc", "sv_append_kv")
+            "sv_verify_layer", "sv_sparse_attend_noalloc", "sv_append_kv",
+            "sv_selection_overlap")
 
 
 class SvError(RuntimeError):
@@ -54,6 +55,31 @@ class KV(C.Structure):
     _fields_ = [("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("block_table", C.c_void_p),
                 ("nb_max", C.c_int), ("num_pages", C.c_int), ("ctx", C.c_int),
                 ("seq_ctx", C.POINTER(C.c_int32))]
+
+
+class SelSlotC(C.Structure):
+    _fields_ = [("sel", C.c_void_p), ("kmax", C.c_int), ("stamp", C.c_uint64)]
+
+
+class SelSlot:
+    """A selection cache slot (sv_sel_slot): the device selection [B, Hkv,
+    kmax] int32 and the host-side stamp the library writes when a computing
+    layer fills it and checks when a reuse layer reads it."""
+
+    def __init__(self, B: int, Hkv: int, kmax: int, device="cuda"):
+        self.tensor = torch.full((B, Hkv, max(kmax, 1)), -1, dtype=torch.int32, device=device)
+        self.c = SelSlotC(self.tensor.data_ptr(), kmax, 0)
+
+    def copy(self) -> "SelSlot":
+        """A new slot holding a copy of this one's selection and stamp."""
+        new = SelSlot.__new__(SelSlot)
+        new.tensor = self.tensor.clone()
+        new.c = SelSlotC(new.tensor.data_ptr(), self.c.kmax, self.c.stamp)
+        return new
+
+    @property
+    def kmax(self) -> int:
+        return self.c.kmax
 
 
 class Plan(C.Structure):
@@ -90,12 +116,13 @@ def lib() -> C.CDLL:
                                      C.POINTER(C.c_int32), vp, vp, sz, vp]),
             "sv_attend_plan": (i, [C.POINTER(Shape), C.POINTER(KV), i, C.POINTER(Plan)]),
             "sv_verify_layer": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, C.POINTER(BudgetC),
-                                    vp, vp, C.POINTER(C.c_int32), i, vp, i, C.POINTER(C.c_int),
-                                    vp, vp, sz, vp]),
+                                    vp, vp, C.POINTER(C.c_int32), i, C.POINTER(SelSlotC),
+                                    C.POINTER(C.c_int), vp, vp, sz, vp]),
             "sv_sparse_attend_noalloc": (i, [C.POINTER(Shape), vp, C.POINTER(KV), vp, i, i, vp,
                                              vp, C.POINTER(C.c_int32), vp, vp, vp]),
             "sv_append_kv": (i, [C.POINTER(Shape), vp, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp,
                                  vp]),
+            "sv_selection_overlap": (i, [vp, i, i, i, i, C.POINTER(C.c_int32), vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -254,24 +281,32 @@ def sv_append_kv(shape: Shape, k_pool, v_pool, block_table, seq_ctx, n_accept, a
                               _ptr(reps), _ptr(ws), _stream(stream)))
 
 
+def sv_selection_overlap(sels, k: int, parents, overlap0, by_distance, stream=None):
+    """Overlaps of T per-draft selections. sels: device int32 [T, pairs, kmax]
+    (each row ascending in its first k entries); overlap0, by_distance:
+    device float32 [pairs, T], written."""
+    T, pairs, kmax = sels.shape
+    _check(lib().sv_selection_overlap(_ptr(sels), T, pairs, kmax, k, _parents(parents),
+                                      _ptr(overlap0), _ptr(by_distance), _stream(stream)))
+
+
 def sv_attend_plan(shape: Shape, kv: KV, n_sel: int) -> Plan:
     p = Plan()
     _check(lib().sv_attend_plan(C.byref(shape), C.byref(kv), n_sel, C.byref(p)))
     return p
 
 
-def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: W.Budget, draft_k, draft_v, parents,
-                    reuse: int, sel_cache, kmax: int, out, ws, stream=None) -> int:
-    b = make_budget(budget)
+def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: Optional[W.Budget], draft_k, draft_v,
+                    parents, reuse: int, slot: Optional[SelSlot], out, ws, stream=None) -> int:
+    b = None if budget is None else C.byref(make_budget(budget))
     k = C.c_int(-1)
-    _check(lib().sv_verify_layer(C.byref(shape), _ptr(q), C.byref(kv), _ptr(reps), C.byref(b),
+    _check(lib().sv_verify_layer(C.byref(shape), _ptr(q), C.byref(kv), _ptr(reps), b,
                                  _ptr(draft_k), _ptr(draft_v), _parents(parents), int(reuse),
-                                 _ptr(sel_cache), kmax, C.byref(k), _ptr(out), _ptr(ws),
-                                 0 if ws is None else ws.numel(), _stream(stream)))
+                                 None if slot is None else C.byref(slot.c), C.byref(k), _ptr(out),
+                                 _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
     return k.value
 
 
-# ------------------------------------------------------------ convenience
 VERIFY_COMPUTE, VERIFY_REUSE, VERIFY_FULL = 0, 1, 2  # sv_verify_layer's reuse values
 
 
@@ -317,7 +352,7 @@ class LayerState:
         # table's width as stride (a partial last block gets a row, unused)
         nb_max = max(x.block_table.shape[1], 1)
         self.reps = torch.zeros(wl.B, wl.Hkv, nb_max, wl.d, dtype=torch.float32, device=dev)
-        self.sel = torch.full((wl.B, wl.Hkv, max(self.kmax, 1)), -1, dtype=torch.int32, device=dev)
+        self.slot = SelSlot(wl.B, wl.Hkv, self.kmax, device=dev)
         self.out = torch.empty_like(x.q)
         # sized for the budgeted selection and for a dense (all-block) pass
         # sized for the block table's width (nb_max), as the calls check it
@@ -326,10 +361,16 @@ class LayerState:
         if build_reps and nb:
             sv_build_reps(self.shape, self.kv, 0, nb, self.reps, stream)
 
+    @property
+    def sel(self) -> torch.Tensor:
+        """The layer's selection (its slot's device tensor)."""
+        return self.slot.tensor
+
     def verify(self, reuse: int = 0, sel_from: Optional["LayerState"] = None, stream=None):
+        """One sv_verify_layer call; sel_from shares that layer's selection
+        slot (inter-layer reuse)."""
         if sel_from is not None:
-            self.sel = sel_from.sel
+            self.slot = sel_from.slot
         sv_verify_layer(self.shape, self.x.q, self.kv, self.reps, self.wl.budget, self.x.draft_k,
-                        self.x.draft_v, self.parents, reuse, self.sel, self.kmax, self.out,
-                        self.ws, stream)
+                        self.x.draft_v, self.parents, reuse, self.slot, self.out, self.ws, stream)
         return self.out

@@ -63,8 +63,11 @@ __host__ __device__ constexpr uint32_t col_p(int x) { return x ? 416u : 384u; }
 // column), the A operand of that segment's S = Q K^T
 constexpr uint32_t kColQ1 = 448;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kMaxMergeSplits = 8;  // partials merged with all loads in flight
 constexpr int kMaxSeg = 2;          // pair segments per CTA
+#ifndef SVA_SPEC_UNITS
+#define SVA_SPEC_UNITS 12
+#endif
+constexpr int kSpecUnits = SVA_SPEC_UNITS;  // units prefetched speculatively before the wait
 
 constexpr int r1024(int x) { return (x + 1023) / 1024 * 1024; }
 
@@ -82,6 +85,8 @@ struct TcCfg {
   static constexpr int kCtrlOff = kRingOff + kRing;
   static constexpr int kSmem = kCtrlOff + 256 + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  // a merge pass of two rows of the most slots a pair can have fits the ring
+  static_assert(2 * (kMaxSplits * (TD * 4 + 8 + 4) + 4) <= kRing, "merge staging");
 };
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -174,7 +179,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
   uint64_t* q_ready = mma_done + 1; // Q landed (TMA) and padding rows zeroed
   uint64_t* q1_ready = q_ready + 1; // second segment's Q written into TMEM
   uint64_t* mid_done = q1_ready + 1; // the mid-stream segment's partials are written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mid_done + 1);
+  uint64_t* merge_bar = mid_done + 1; // a merge's partials have landed (bulk copies)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(merge_bar + 1);
   int* stage_info = reinterpret_cast<int*>(tmem_slot + 1);  // bit0 valid, bit1 draft tile
   volatile int* abort_flag = stage_info + NS;
   volatile int* pair_done = abort_flag + 1;  // [kMaxSeg]: this CTA saw the pair complete
@@ -202,6 +208,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
     mbar_init(smem_u32(q_ready), 5);  // producer's expect_tx + 4 zeroing warps
     mbar_init(smem_u32(q1_ready), 4);
     mbar_init(smem_u32(mid_done), 2 * NSW);
+    mbar_init(smem_u32(merge_bar), 1);
     *abort_flag = 0;
     for (int j = 0; j < kMaxSeg; ++j) pair_done[j] = 0;
     fence_barrier_init();
@@ -228,6 +235,28 @@ __global__ void __launch_bounds__(32 * 10, 1)
     for (int j = 0; j < sp.n; ++j) {
       const int32_t* row = a.block_table + (size_t)(sp.pair[j] / a.Hkv) * a.nb_max;
       for (int e = 32 * lane; e < a.nb; e += 32 * 32) prefetch_l2(row + e);
+    }
+    if (a.spec_prefetch && lane < kSpecUnits && lane < ntot) {
+      // Speculative: the pages of this CTA's first units, looked up with
+      // relaxed reads that may see an earlier selection if the preceding
+      // kernel rewrites it. Only L2 is touched, so a wrong guess costs
+      // bandwidth and nothing else; the copies below re-read after the wait.
+      const int j = lane < n0 ? 0 : 1;
+      const int u = sp.u0[j] + lane - (j ? n0 : 0);
+      const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+      const int nsel = n_of(a.vl, b, a.n_sel), nbb = nb_of(a.vl, b, a.nb);
+      int page = -1;
+      if (u < nsel) {
+        const int jb = a.sel ? load_relaxed(a.sel + (size_t)pair * a.sel_stride + u) : u;
+        if (jb >= 0 && jb < nbb) page = load_relaxed(a.block_table + (size_t)b * a.nb_max + jb);
+      } else if (u == nsel && tail_of(a.vl, b, a.tail) > 0) {
+        page = load_relaxed(a.block_table + (size_t)b * a.nb_max + nbb);
+      }
+      if (page >= 0 && page < a.num_pages) {
+        const size_t off = (size_t)((page * a.Hkv + h) * TBLK) * TD * 2;
+        prefetch_bulk_l2(static_cast<const uint8_t*>(a.k_pool) + off, kTileBytes);
+        prefetch_bulk_l2(static_cast<const uint8_t*>(a.v_pool) + off, kTileBytes);
+      }
     }
   }
   pdl_wait();     // everything below may read what earlier kernels wrote
@@ -299,7 +328,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
       const int nblk = max(0, min(sp.u1[j], nsel) - ub);
       for (int base = 0; base < nblk && !stop; base += 32) {
         int row = oob_row, ok = 0;
-        if (base + lane < nblk) {
+        if (base + lane < nblk && a.rows) {
+          // resolved by the select step (which flagged any bad page as -1)
+          const int rr = a.rows[(size_t)pair * a.sel_stride + ub + base + lane];
+          if (rr >= 0 && rr < oob_row) {
+            row = rr;
+            ok = 1;
+          }
+        } else if (base + lane < nblk) {
           const int jb = a.sel ? a.sel[(size_t)pair * a.sel_stride + ub + base + lane] : ub + base + lane;
           if (jb < 0 || jb >= nbb) {
             atomicOr(a.status, SV_FLAG_BAD_BLOCK_INDEX);
@@ -416,8 +452,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
       // the last arrival sees the pair complete (and acquires its partials)
-      if ((arrive_acq_rel(&a.counters[sp.pair[0]]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0])
-        pair_done[0] = 1;
+      if (arrive_acq_rel(&a.counters[sp.pair[0]]) + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -712,102 +747,96 @@ __global__ void __launch_bounds__(32 * 10, 1)
     // mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0) {
-      if ((arrive_acq_rel(&a.counters[pair]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf])
-        pair_done[jf] = 1;
+      if (arrive_acq_rel(&a.counters[pair]) + 1u == (unsigned)sp.nseg[jf]) pair_done[jf] = 1;
     }
   }
   __syncthreads();
 
-  // ------------------------------------------------------- merge of a pair
-  // Every CTA merges its share of the rows of each pair it worked on, once
-  // all of the pair's segments have arrived:
+  // ------------------------------------------------- merge by the last arrival
+  // The CTA whose arrival completed a pair (the count reached the pair's
+  // segment count) merges every row of that pair; all other CTAs are done.
+  // No CTA ever waits for another, so nothing here depends on which CTAs
+  // are resident at the same time.
   //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s.
-  // The pair's count word holds the arrivals (low 16 bits) and the finished
-  // row shares (high bits); whoever finishes the last share resets it. All
-  // of a CTA's arrivals come before any of its waits, and an arrival depends
-  // only on that CTA's own stream, so the waits end; they are bounded too.
+  // The partials come into the idle ring by bulk copies (one per slot and
+  // row range), so one CTA reads them at the copy engine's rate rather than
+  // at the rate its threads can keep loads in flight. The merging CTA also
+  // returns the count word to zero for the next call: every arrival of this
+  // call is in by then.
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  // this CTA's slice [r0, r1) of the rows of each of its pairs
-  int r0[kMaxSeg], r1[kMaxSeg], nitem[kMaxSeg];
-  for (int j = 0; j < kMaxSeg; ++j) {
-    r0[j] = r1[j] = nitem[j] = 0;
-    if (j < sp.n) {
-      const int share = ((a.R + sp.nseg[j] - 1) / sp.nseg[j] + 1) & ~1;
-      r0[j] = min(a.R, sp.slot[j] * share);
-      r1[j] = min(a.R, r0[j] + share);
-      nitem[j] = (r1[j] - r0[j]) * (TD / 4);
-    }
-  }
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    for (int j = 0; j < sp.n; ++j) {
-      if (pair_done[j]) continue;  // this CTA's own arrival completed it
-      while ((load_acquire(&a.counters[sp.pair[j]]) & 0xFFFFu) < (unsigned)sp.nseg[j]) {
-        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
-          atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-          break;
-        }
-        __nanosleep(32);
-      }
-    }
-  }
-  __syncthreads();  // thread 0's acquires cover the whole CTA's reads below
-  // the slices of both pairs in one pass, so all of their loads overlap
-  for (int idx = threadIdx.x; idx < nitem[0] + nitem[1]; idx += NT) {
-    const int j = idx < nitem[0] ? 0 : 1;
-    const int k = idx - (j ? nitem[0] : 0);
+  uint32_t mphase = 0;
+  for (int j = 0; j < sp.n; ++j) {
+    if (!pair_done[j]) continue;  // the same in every thread (set before a barrier)
     const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
     const int ns = sp.nseg[j] + sp.mid[j];
     const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    const int rr = r0[j] + k / (TD / 4), c = (k % (TD / 4)) * 4;
-    float M = -INFINITY, Lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += kMaxMergeSplits) {
-      // kMaxMergeSplits partials' loads in flight together
-      float2 ml[kMaxMergeSplits];
-      float4 o[kMaxMergeSplits];
-#pragma unroll
-      for (int q = 0; q < kMaxMergeSplits; ++q) {
-        ml[q] = make_float2(-INFINITY, 0.f);
-        o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s0 + q < ns) {
-          const size_t row = pbase + (size_t)(s0 + q) * a.rpad + rr;
-          ml[q] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + row * 2));
-          o[q] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * TD + c));
+    // rows per pass: the staging holds, per slot and row, its o row (512 B),
+    // its (m, l) (8 B) and its weight (4 B), plus a normaliser per row; an
+    // even count, so that every (m, l) copy is a multiple of 16 bytes. With
+    // at most 64 slots two rows always fit.
+    constexpr int kRowBytes = TD * 4 + 8;  // copied per slot and row
+    int rpp = (C::kRing / (ns * (kRowBytes + 4) + 4)) & ~1;
+    rpp = rpp < 2 ? 2 : (rpp > a.rpad ? a.rpad : rpp);
+    float* so = reinterpret_cast<float*>(ring);                 // [ns][rpp][TD]
+    float2* sml = reinterpret_cast<float2*>(so + (size_t)ns * rpp * TD);  // [ns][rpp]
+    float* sw = reinterpret_cast<float*>(sml + (size_t)ns * rpp);          // [ns][rpp]
+    float* sinv = sw + (size_t)ns * rpp;                                   // [rpp]
+    for (int r0 = 0; r0 < a.R; r0 += rpp) {
+      const int nr = min(rpp, a.rpad - r0);  // rows copied (padding rows included)
+      if (threadIdx.x == 0) {
+        // the partials were written by other CTAs through the generic proxy
+        // and acquired by the arrival; order that before the copy engine reads
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        fence_async_smem();
+        const uint32_t mb = smem_u32(merge_bar);
+        mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kRowBytes));
+        for (int sl = 0; sl < ns; ++sl) {
+          const size_t row0 = pbase + (size_t)sl * a.rpad + r0;
+          bulk_load(smem_u32(so + (size_t)sl * rpp * TD), a.part_o + row0 * TD,
+                    (uint32_t)(nr * TD * 4), mb);
+          bulk_load(smem_u32(sml + (size_t)sl * rpp), a.part_ml + row0 * 2, (uint32_t)(nr * 8), mb);
         }
       }
-      float Mc = M;
-#pragma unroll
-      for (int q = 0; q < kMaxMergeSplits; ++q) Mc = fmaxf(Mc, ml[q].x);
-      if (Mc > M) {
-        const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
-        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-        Lsum *= sc;
-        M = Mc;
+      const bool got = mbar_wait_drain(smem_u32(merge_bar), mphase);
+      mphase ^= 1u;
+      if (!got && threadIdx.x == 0) atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+      const int nv = min(rpp, a.R - r0);  // real rows of this pass
+      for (int r = threadIdx.x; r < nv; r += NT) {
+        float M = -INFINITY;
+        for (int sl = 0; sl < ns; ++sl) M = fmaxf(M, sml[sl * rpp + r].x);
+        float L = 0.f;
+        for (int sl = 0; sl < ns; ++sl) {
+          const float2 ml = sml[sl * rpp + r];
+          const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+          L += w * ml.y;
+          sw[sl * rpp + r] = w;
+        }
+        sinv[r] = 1.0f / L;
       }
-#pragma unroll
-      for (int q = 0; q < kMaxMergeSplits; ++q) {
-        const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
-        Lsum += w * ml[q].y;
-        acc.x += w * o[q].x; acc.y += w * o[q].y; acc.z += w * o[q].z; acc.w += w * o[q].w;
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < nv * (TD / 4); idx += NT) {
+        const int r = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sl = 0; sl < ns; ++sl) {
+          const float w = sw[sl * rpp + r];
+          const float4 o = *reinterpret_cast<const float4*>(so + ((size_t)sl * rpp + r) * TD + c);
+          acc.x += w * o.x;
+          acc.y += w * o.y;
+          acc.z += w * o.z;
+          acc.w += w * o.w;
+        }
+        const float inv = sinv[r];
+        const int rr = r0 + r, t = rr / a.G, gq = rr % a.G;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
       }
+      __syncthreads();  // the next pass's copies overwrite the staging area
     }
-    const float inv = 1.0f / Lsum;
-    const int t = rr / a.G, gq = rr % a.G;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
-  }
-  if (threadIdx.x == 0) {
-    // every CTA of a pair has seen all arrivals before counting its slice,
-    // so the last slice may clear the word for the next call
-    for (int j = 0; j < sp.n; ++j) {
-      unsigned* ctr = &a.counters[sp.pair[j]];
-      if ((atomicAdd(ctr, 1u << 16) >> 16) == (unsigned)sp.nseg[j] - 1u) *ctr = 0u;
-    }
+    if (threadIdx.x == 0) a.counters[pair] = 0u;
   }
 }
 

@@ -47,7 +47,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace carve-up (offsets in bytes from the workspace base).
 struct WsLayout {
-  size_t status, ctr_score, ctr_attend, scores, part_o, part_ml, total;
+  size_t status, ctr_score, ctr_attend, scores, rows, part_o, part_ml, total;
   int rpad, slots;
 };
 WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax);
@@ -104,6 +104,11 @@ struct ScoreArgs {
   int k, kmax;
   unsigned* counters;  // [B*Hkv], zero between calls
   VarLen vl;           // per-sequence nb (rows) and k; score rows keep stride nb
+  // optional pool rows of the kept blocks (rows[b][h][0..kmax), beside sel)
+  const int32_t* block_table;  // null: no rows
+  int32_t* rows;
+  int blk, num_pages;
+  unsigned* status;
 };
 cudaError_t launch_score(ScoreArgs a, int dtype, cudaStream_t st);
 // Largest block count whose selection the score kernel fuses (its 256
@@ -116,6 +121,11 @@ struct SelectArgs {
   int pairs, nb, k, kmax;
   int Hkv;             // pairs are (b, h) with b = pair / Hkv
   VarLen vl;           // per-sequence nb and k; score rows keep stride nb
+  // optional pool rows of the kept blocks, as in ScoreArgs
+  const int32_t* block_table;
+  int32_t* rows;
+  int nb_max, blk, num_pages;
+  unsigned* status;
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
@@ -127,10 +137,14 @@ struct AttendArgs {
   const void* draft_v;
   const int32_t* block_table;
   const int32_t* sel;   // null: identity selection over NB blocks
+  // optional pool rows of the selected blocks ([pairs][sel_stride], written by
+  // the select step of the same call): the producer reads them instead of
+  // resolving sel through the block table
+  const int32_t* rows;
   float* part_o;        // [B,Hkv,S,Rpad,d]
   float* part_ml;       // [B,Hkv,S,Rpad,2]
   void* out;            // [B,T,Hq,d]
-  unsigned* counters;   // [B*Hkv] split arrivals (tcgen05 path), zero between calls
+  unsigned* counters;   // [B*Hkv] segment arrivals (tcgen05 path), zero between calls
   unsigned* status;
   int B, T, Hq, Hkv, G, d, blk, R, rpad;
   int nb, nb_max, num_pages, n_sel, sel_stride;
@@ -147,10 +161,25 @@ struct AttendArgs {
   // tcgen05 path: 1 = stream-K (n_splits CTAs, each an equal run of the
   // flattened (pair, unit) sequence; split_extra unused)
   int streamk;
+  // 1: before the dependency wait, the producer may read sel and the block
+  // table (relaxed; possibly stale) and prefetch the first pages into L2.
+  // Set only when this call's selection was not just written by the
+  // preceding kernel; a stale guess only costs bandwidth, never results.
+  int spec_prefetch;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
   VarLen vl;  // per-sequence nb, tail and n_sel (on = 0: the uniform ones)
 };
+
+// Overlap of per-draft selections (the shared-set diagnostic).
+struct OverlapArgs {
+  const int32_t* sels;  // [T][pairs][kmax], each row ascending in its first k
+  float* overlap0;      // [pairs][T]: |S_0 ∩ S_t| / k
+  float* by_distance;   // [pairs][T]: mean |S_t ∩ S_u| / k over t < u at each depth distance
+  int T, pairs, kmax, k;
+  int depth[kMaxT];     // depth of each draft in its tree
+};
+cudaError_t launch_overlap(const OverlapArgs& a, cudaStream_t st);
 
 // The contexts of one call: uniform (var = false) or per sequence.
 struct Ctxs {
@@ -199,9 +228,9 @@ int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster);
 // splits write global partials for launch_merge.
 cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st);
 // tcgen05 path: bf16, d == 128, blk == 64, R <= 128, T <= 64.
-// Writes global split partials (split map above, 1-D grid of pairs *
-// n_splits + split_extra CTAs); the last CTA of each (b, h) to finish merges
-// them into out (no separate merge launch).
+// Writes global split partials (stream-K runs, or the split map above); the
+// CTA whose arrival completes a (b, h) merges that pair's partials into out
+// (no separate merge launch, and no CTA waits for another).
 bool attend_tc_applies(const AttendArgs& a, int dtype);
 int attend_tc_ctas_per_sm(const AttendArgs& a);
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t st);

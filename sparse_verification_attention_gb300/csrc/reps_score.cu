@@ -237,8 +237,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   }
   __syncthreads();
   if (s_last) {
+    const TopkRows tr{a.block_table ? a.block_table + (size_t)b * a.nb_max : nullptr,
+                      a.rows ? a.rows + (size_t)pair * a.kmax : nullptr, a.Hkv, h, a.blk,
+                      a.num_pages, a.status};
     cta_topk_fit<kScoreThreads, kScoreKeys>(srow, nbb, n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax,
-                                        a.kmax, tsm);
+                                        a.kmax, tsm, tr);
     if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
   }
 }

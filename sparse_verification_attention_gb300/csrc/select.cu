@@ -26,8 +26,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const __grid_con
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   const int pair = blockIdx.x, b = pair / a.Hkv;
+  const TopkRows tr{a.block_table ? a.block_table + (size_t)b * a.nb_max : nullptr,
+                    a.rows ? a.rows + (size_t)pair * a.kmax : nullptr, a.Hkv, pair % a.Hkv,
+                    a.blk, a.num_pages, a.status};
   cta_topk_fit<kSelThreads, kSelKeys>(a.scores + (size_t)pair * a.nb, nb_of(a.vl, b, a.nb),
-                                  n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax, a.kmax, tsm);
+                                  n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax, a.kmax, tsm,
+                                  tr);
 }
 
 }  // namespace

@@ -253,7 +253,8 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   L.ctr_score = kStatusBytes;
   L.ctr_attend = L.ctr_score + align256(pairs * sizeof(uint32_t));
   L.scores = L.ctr_attend + align256(pairs * sizeof(uint32_t));
-  L.part_o = L.scores + align256(pairs * (size_t)(nb_max > 0 ? nb_max : 1) * sizeof(float));
+  L.rows = L.scores + align256(pairs * (size_t)(nb_max > 0 ? nb_max : 1) * sizeof(float));
+  L.part_o = L.rows + align256(pairs * (size_t)(kmax > 0 ? kmax : 1) * sizeof(int32_t));
   L.part_ml = L.part_o + align256(pairs * L.slots * (size_t)L.rpad * s.d * sizeof(float));
   L.total = L.part_ml + align256(pairs * L.slots * (size_t)L.rpad * 2 * sizeof(float));
   return L;
@@ -422,13 +423,20 @@ static void set_nsel(AttendArgs& a, const int* nsel_b) {
   for (int b = 0; b < a.B; ++b) a.vl.n[b] = nsel_b ? nsel_b[b] : a.sel ? a.n_sel : a.vl.nb[b];
 }
 
+// fresh_sel: the selection was written by the kernel launched just before
+// (score + select in the same call), so no speculative prefetch from it.
+// rows: pool rows of sel written by the select step of this call (then no
+// speculative prefetch either: the selection is fresh).
 static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, const int32_t* sel,
                             int n_sel, int sel_stride, const void* dk, const void* dv,
                             const int32_t* parent, void* out, void* ws, const WsLayout& L,
-                            cudaStream_t st, const int* nsel_b = nullptr) {
+                            cudaStream_t st, const int* nsel_b = nullptr,
+                            const int32_t* rows = nullptr) {
   AttendArgs a{};
   fill_args(a, s, q, kv, sel, n_sel, sel_stride, dk, dv, parent, ws, L);
   set_nsel(a, nsel_b);
+  a.rows = rows;
+  a.spec_prefetch = rows ? 0 : 1;
   a.out = out;
   const AttendPlan p = make_plan(a, s->dtype, s->B * s->Hkv, n_sel, L.slots);
   a.n_splits = p.n_splits;
@@ -500,26 +508,35 @@ static sv_status check_ws(const sv_shape* s, int nb_max, int kmax, const void* w
   return SV_OK;
 }
 
+// Scores, budget and selection into sel; with `rows`, the kept blocks' pool
+// rows too (the attention of the same call reads those instead of resolving
+// sel through the block table).
 static sv_status do_score_select(const sv_shape* s, const void* q, const float* reps,
                                  const sv_kv* kv, int k, int32_t* sel, int kmax, void* ws,
-                                 const WsLayout& L, cudaStream_t st, const int* k_b = nullptr) {
+                                 const WsLayout& L, cudaStream_t st, const int* k_b = nullptr,
+                                 int32_t* rows = nullptr) {
   Ctxs c = ctxs_of(s, kv);
   const int nb = c.nb;  // the largest sequence's (score rows keep this stride)
   if (c.vl.on)
     for (int b = 0; b < s->B; ++b) c.vl.n[b] = k_b[b];
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(w + L.scores);
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+  const int32_t* bt = rows ? kv->block_table : nullptr;
   cudaError_t e;
   if (nb == 0) {
     // nothing to score: the selection is empty
-    SelectArgs se{scores, sel, s->B * s->Hkv, 0, 0, kmax, s->Hkv, c.vl};
+    SelectArgs se{scores, sel, s->B * s->Hkv, 0, 0, kmax, s->Hkv, c.vl,
+                  nullptr, nullptr, kv->nb_max, s->blk, kv->num_pages, status};
     e = launch_select(se, st);
   } else {
     ScoreArgs sa{q, reps, scores, s->B, s->T, s->Hq, s->Hkv, s->Hq / s->Hkv, s->d, nb, kv->nb_max,
-                 0, sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score), c.vl};
+                 0, sel, k, kmax, reinterpret_cast<unsigned*>(w + L.ctr_score), c.vl,
+                 nb > kFusedSelectMaxNB ? nullptr : bt, rows, s->blk, kv->num_pages, status};
     e = launch_score(sa, s->dtype, st);
     if (e == cudaSuccess && nb > kFusedSelectMaxNB) {  // too many keys to fuse
-      SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax, s->Hkv, c.vl};
+      SelectArgs se{scores, sel, s->B * s->Hkv, nb, k, kmax, s->Hkv, c.vl,
+                    bt, rows, kv->nb_max, s->blk, kv->num_pages, status};
       e = launch_select(se, st);
     }
   }
@@ -574,9 +591,40 @@ static WsLayout noalloc_layout(const sv_shape& s, int rpad, int slot_stride) {
   L.ctr_score = L.ctr_attend;  // unused: this entry does not score
   L.part_o = L.ctr_attend + align256(pairs * sizeof(uint32_t));
   L.scores = L.part_o;  // unused
+  L.rows = L.part_o;    // unused
   L.part_ml = L.part_o + align256(rows * s.d * sizeof(float));
   L.total = L.part_ml + align256(rows * 2 * sizeof(float));
   return L;
+}
+
+// Digest of what a computed selection depends on beyond the inputs'
+// values: batch and head layout, block size, row length, every sequence's
+// context length and budget (FNV-1a, 64 bit; never 0, which marks a slot
+// that no computing call has written).
+static uint64_t selection_stamp(const sv_shape* s, const sv_kv* kv, const Ctxs& c, int kmax, int k,
+                                const int* k_b) {
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&](long long v) {
+    for (int i = 0; i < 8; ++i) {
+      h ^= (uint64_t)((v >> (8 * i)) & 0xff);
+      h *= 1099511628211ull;
+    }
+  };
+  mix(s->B);
+  mix(s->Hkv);
+  mix(s->blk);
+  mix(kmax);
+  mix(c.var ? 1 : 0);
+  if (c.var) {
+    for (int b = 0; b < s->B; ++b) {
+      mix(kv->seq_ctx[b]);
+      mix(k_b[b]);
+    }
+  } else {
+    mix(kv->ctx);
+    mix(k);
+  }
+  return h ? h : 1ull;
 }
 
 // The budget of every sequence (k_b[b], per-sequence contexts only) and
@@ -690,7 +738,8 @@ sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* rep
   if (!aligned(q, 16) || !aligned(reps, 16))
     return fail(SV_ERR_INVALID_ARG, "q and reps must be 16-byte aligned");
   ScoreArgs sa{q, reps, scores, shape->B, shape->T, shape->Hq, shape->Hkv,
-               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, 0, nullptr, 0, 0, nullptr, c.vl};
+               shape->Hq / shape->Hkv, shape->d, nb, kv->nb_max, 0, nullptr, 0, 0, nullptr, c.vl,
+               nullptr, nullptr, shape->blk, kv->num_pages, nullptr};
   cudaError_t e = launch_score(sa, shape->dtype, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "score launch");
 }
@@ -703,7 +752,8 @@ sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, i
   if (k < 0 || k > kmax) return fail(SV_ERR_INVALID_ARG, "k=%d outside [0, kmax=%d]", k, kmax);
   if (kmax == 0) return SV_OK;
   if (!sel || (nb > 0 && !scores)) return fail(SV_ERR_INVALID_ARG, "scores/sel is NULL");
-  SelectArgs se{scores, sel, shape->B * shape->Hkv, nb, k, kmax, shape->Hkv, VarLen{}};
+  SelectArgs se{scores, sel, shape->B * shape->Hkv, nb, k, kmax, shape->Hkv, VarLen{},
+                nullptr, nullptr, 0, shape->blk, 0, nullptr};
   cudaError_t e = launch_select(se, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "select launch");
 }
@@ -781,13 +831,17 @@ sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_p
 
 sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,
                           const sv_budget* budget, const void* draft_k, const void* draft_v,
-                          const int32_t* draft_parent, int reuse, int32_t* sel_cache, int kmax,
-                          int* k_out, void* out, void* workspace, size_t ws_bytes, void* stream) {
+                          const int32_t* draft_parent, int reuse, sv_sel_slot* slot, int* k_out,
+                          void* out, void* workspace, size_t ws_bytes, void* stream) {
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
   if (reuse < 0 || reuse > 2)
     return fail(SV_ERR_INVALID_ARG, "reuse=%d must be 0, 1 or 2", reuse);
+  if (reuse != 2 && !slot) return fail(SV_ERR_INVALID_ARG, "selection slot is NULL");
+  const int kmax = slot ? slot->kmax : 0;
+  int32_t* sel_cache = slot ? slot->sel : nullptr;
+  if (kmax < 0) return fail(SV_ERR_INVALID_ARG, "slot kmax=%d is negative", kmax);
   const Ctxs c = ctxs_of(shape, kv);
   const int nb = c.nb;
   if (reuse == 2) {
@@ -797,8 +851,12 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
     if (!aligned(q, 16) || !aligned(draft_k, 16) || !aligned(draft_v, 16) || !aligned(out, 16))
       return fail(SV_ERR_INVALID_ARG, "q/draft_k/draft_v/out must be 16-byte aligned");
     if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
+    // partial slots for all nb blocks when the workspace holds them (as
+    // sv_sparse_attend with sel == NULL), else for the slot's kmax
     WsLayout L;
-    if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+    const int kws = ws_layout(*shape, kv->nb_max, std::max(kmax, nb)).total <= ws_bytes
+                        ? std::max(kmax, nb) : kmax;
+    if ((r = check_ws(shape, kv->nb_max, kws, workspace, ws_bytes, &L)) != SV_OK) return r;
     if (k_out) *k_out = nb;
     return run_attend(shape, q, kv, nullptr, nb, nb, draft_k, draft_v, draft_parent, out,
                       workspace, L, (cudaStream_t)stream);
@@ -817,14 +875,23 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   if ((r = check_parents(draft_parent, shape->T)) != SV_OK) return r;
   WsLayout L;
   if ((r = check_ws(shape, kv->nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+  const uint64_t stamp = selection_stamp(shape, kv, c, kmax, k, k_b);
+  if (reuse == 1 && slot->stamp != stamp)
+    return fail(SV_ERR_INVALID_ARG,
+                slot->stamp ? "reuse of a selection computed for another shape, context or budget"
+                            : "reuse of a selection slot that no computing call has written");
   cudaStream_t st = (cudaStream_t)stream;
+  int32_t* rows = nullptr;
   if (!reuse && kmax > 0) {
-    r = do_score_select(shape, q, reps, kv, k, sel_cache, kmax, workspace, L, st, k_b);
+    rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.rows);
+    r = do_score_select(shape, q, reps, kv, k, sel_cache, kmax, workspace, L, st, k_b, rows);
     if (r != SV_OK) return r;
   }
   if (k_out) *k_out = k;
-  return run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out,
-                    workspace, L, st, c.var ? k_b : nullptr);
+  r = run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out, workspace,
+                 L, st, c.var ? k_b : nullptr, rows);
+  if (r == SV_OK && reuse == 0) slot->stamp = stamp;
+  return r;
 }
 
 sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const sv_kv* kv,
@@ -855,6 +922,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   fill_args(a, shape, q, kv, sel, n_sel, sel_stride, draft_k, draft_v, draft_parent, nullptr, W);
   set_nsel(a, nullptr);
   a.out = out;
+  a.spec_prefetch = 1;
   const AttendPlan p = make_plan(a, shape->dtype, shape->B * shape->Hkv, n_sel, W.slots);
   const WsLayout L = noalloc_layout(*shape, W.rpad, p.slot_stride);
   if (L.total > kNoAllocScratchBytes)
@@ -894,6 +962,24 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
     if (e != cudaSuccess) return cuda_fail(e, "status copy");
   }
   return SV_OK;
+}
+
+sv_status sv_selection_overlap(const int32_t* sels, int T, int pairs, int kmax, int k,
+                               const int32_t* draft_parent, float* overlap0, float* by_distance,
+                               void* stream) {
+  if (T < 1 || T > kMaxT) return fail(SV_ERR_UNSUPPORTED, "T=%d outside [1, %d]", T, kMaxT);
+  if (pairs < 0 || kmax < 1 || k < 1 || k > kmax)
+    return fail(SV_ERR_INVALID_ARG, "pairs=%d, k=%d, kmax=%d: need pairs >= 0, 1 <= k <= kmax",
+                pairs, k, kmax);
+  if (pairs > 0 && (!sels || !overlap0 || !by_distance))
+    return fail(SV_ERR_INVALID_ARG, "sels/overlap0/by_distance is NULL");
+  sv_status r = check_parents(draft_parent, T);
+  if (r != SV_OK) return r;
+  OverlapArgs a{sels, overlap0, by_distance, T, pairs, kmax, k, {}};
+  for (int t = 0; t < T; ++t)
+    a.depth[t] = t == 0 ? 0 : a.depth[draft_parent ? draft_parent[t] : t - 1] + 1;
+  const cudaError_t e = launch_overlap(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "overlap launch");
 }
 
 }  // extern "C"

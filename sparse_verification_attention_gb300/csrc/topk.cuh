@@ -83,6 +83,27 @@ struct TopkSmem {
   uint32_t bstar_above, ncand;
 };
 
+// Optional second output of a selection: the pool row of every kept block,
+// row = (page * Hkv + h) * blk with page = bt[index] (the first token row of
+// that block's tile for KV head h), written beside the index; -1 (and
+// SV_FLAG_BAD_PAGE) for a page outside [0, num_pages). The attention then
+// needs one load per block instead of two dependent ones. bt == nullptr:
+// no rows.
+struct TopkRows {
+  const int32_t* bt;  // block-table row of the sequence
+  int32_t* out;       // kmax entries, beside the indices
+  int Hkv, h, blk, num_pages;
+  unsigned* status;   // may be null
+};
+
+__device__ __forceinline__ int32_t topk_row(const TopkRows& tr, int page) {
+  if (page < 0 || page >= tr.num_pages) {
+    if (tr.status) atomicOr(tr.status, SV_FLAG_BAD_PAGE);
+    return -1;
+  }
+  return (page * tr.Hkv + tr.h) * tr.blk;
+}
+
 // Larger score first, then the lower index: (key << 32) | ~index.
 __device__ __forceinline__ unsigned long long topk_composite(uint32_t key, int idx) {
   return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)idx;
@@ -94,7 +115,7 @@ __device__ __forceinline__ unsigned long long topk_composite(uint32_t key, int i
 // ascending then -1.
 template <int NT, int KPT, int KMAX>
 __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int kmax,
-                         TopkSmem<NT, KMAX>& sm) {
+                         TopkSmem<NT, KMAX>& sm, const TopkRows& tr) {
   static_assert(KPT <= KMAX, "shared memory sized for fewer keys");
   constexpr int NW = NT / 32;
   constexpr int BPT = kTopkBins / NT;  // histogram bins per thread in the scan
@@ -102,13 +123,23 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
   using Mask = std::conditional_t<(KPT > 32), unsigned long long, uint32_t>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = k_req < nb ? k_req : nb;
-  for (int i = k + tid; i < kmax; i += NT) out[i] = -1;
+  for (int i = k + tid; i < kmax; i += NT) {
+    out[i] = -1;
+    if (tr.bt) tr.out[i] = -1;
+  }
   if (k == 0) return;
   if (k == nb) {
-    for (int i = tid; i < nb; i += NT) out[i] = i;
+    for (int i = tid; i < nb; i += NT) {
+      out[i] = i;
+      if (tr.bt) tr.out[i] = topk_row(tr, tr.bt[i]);
+    }
     return;
   }
   const int wbase = warp * 32 * KPT;
+  // With few keys per thread, every key's page is loaded beside its score (the
+  // same round trip); with more, a kept key's page is loaded at the end.
+  constexpr bool kPagesInRegs = KPT <= 8;
+  int32_t pg[kPagesInRegs ? KPT : 1];
   // padding entries hold key 0, below every candidate tested
   uint32_t rk[KPT];
   Mask valid = 0;
@@ -117,6 +148,7 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     const int j = wbase + 32 * e + lane;
     const bool ok = j < nb;
     rk[e] = ok ? order_key(__ldcg(sc + j)) : 0u;
+    if constexpr (kPagesInRegs) pg[e] = (ok && tr.bt) ? tr.bt[j] : -1;
     valid |= (Mask)(ok ? 1u : 0u) << e;
   }
 
@@ -328,7 +360,15 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
   for (int e = 0; e < KPT; ++e) {
     const bool kp = (keep >> e) & 1u;
     const unsigned b = __ballot_sync(0xffffffffu, kp);
-    if (kp) out[pos + __popc(b & lt)] = wbase + 32 * e + lane;
+    if (kp) {
+      const int j = wbase + 32 * e + lane;
+      const int at = pos + __popc(b & lt);
+      out[at] = j;
+      if (tr.bt) {
+        if constexpr (kPagesInRegs) tr.out[at] = topk_row(tr, pg[e]);
+        else tr.out[at] = topk_row(tr, tr.bt[j]);
+      }
+    }
     pos += __popc(b);
   }
 }
@@ -337,13 +377,13 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
 // choice in every thread of the CTA).
 template <int NT, int KMAX>
 __device__ void cta_topk_fit(const float* sc, int nb, int k_req, int32_t* out, int kmax,
-                             TopkSmem<NT, KMAX>& sm) {
+                             TopkSmem<NT, KMAX>& sm, const TopkRows& tr) {
   if (KMAX > 4 && nb <= NT * 4)
-    cta_topk<NT, (KMAX > 4 ? 4 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm);
+    cta_topk<NT, (KMAX > 4 ? 4 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm, tr);
   else if (KMAX > 8 && nb <= NT * 8)
-    cta_topk<NT, (KMAX > 8 ? 8 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm);
+    cta_topk<NT, (KMAX > 8 ? 8 : KMAX), KMAX>(sc, nb, k_req, out, kmax, sm, tr);
   else
-    cta_topk<NT, KMAX, KMAX>(sc, nb, k_req, out, kmax, sm);
+    cta_topk<NT, KMAX, KMAX>(sc, nb, k_req, out, kmax, sm, tr);
 }
 
 }  // namespace sva

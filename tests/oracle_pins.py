@@ -458,4 +458,39 @@ def pin_draft_overlap_closed_form(O):
     assert ov[0, 0].tolist() == [1.0, 0.0, 0.0, 0.0, 1.0]
 
 
+def _onehot_reps(NB=8, d=4):
+    reps = torch.zeros(1, 1, NB, d, dtype=F64)
+    for j in range(NB):
+        reps[0, 0, j, j % d] = j + 1.0
+    return reps
+
+
+def pin_overlap_by_distance_chain(O):
+    """One-hot representatives as above: a query e_i keeps blocks {i, i + 4}
+    (k = 2). Chain drafts with queries e0, e0, e1, e0: the pairs at distance
+    1 are (0,1) -> 1, (1,2) -> 0, (2,3) -> 0, mean 1/3; at distance 2 (0,2)
+    -> 0 and (1,3) -> 1, mean 1/2; at distance 3 (0,3) -> 1. No pair has
+    distance 0."""
+    q = torch.zeros(1, 4, 1, 4, dtype=F64)
+    for t, i in enumerate([0, 0, 1, 0]):
+        q[0, t, 0, i] = 1.0
+    got = O.draft_overlap_by_distance(q, _onehot_reps(), 1, 2, [-1, 0, 1, 2])[0, 0]
+    assert math.isnan(got[0])
+    assert torch.allclose(got[1:], torch.tensor([1 / 3, 1 / 2, 1.0], dtype=F64))
+
+
+def pin_overlap_by_distance_tree(O):
+    """Tree drafts (parents -1, 0, 0, 1: depths 0, 1, 1, 2) with queries
+    e0, e0, e1, e1. By depth difference: distance 0 is the sibling pair
+    (1,2) -> 0; distance 1 is (0,1) -> 1, (0,2) -> 0, (1,3) -> 0, (2,3) -> 1,
+    mean 1/2; distance 2 is (0,3) -> 0. (Index distance would give 2/3 at
+    distance 1.)"""
+    q = torch.zeros(1, 4, 1, 4, dtype=F64)
+    for t, i in enumerate([0, 0, 1, 1]):
+        q[0, t, 0, i] = 1.0
+    got = O.draft_overlap_by_distance(q, _onehot_reps(), 1, 2, [-1, 0, 0, 1])[0, 0]
+    assert torch.allclose(got[:3], torch.tensor([0.0, 0.5, 0.0], dtype=F64))
+    assert math.isnan(got[3])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_abi_version(L):
-    assert api.sv_abi_version() == api.ABI_VERSION == 3
+    assert api.sv_abi_version() == api.ABI_VERSION == 4
 
 
 def test_budget_matches_oracle_golden(L):
@@ -83,19 +83,21 @@ def test_budget_rejects_invalid(L):
 def test_workspace_sizes(L):
     s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
     n = api.sv_workspace_bytes(s, 2048, 128)
-    # status + two per-(b,h) counter arrays + scores + split partials o and
-    # (m, l); 130 work units (128 blocks, a partial block, the draft tile)
-    # capped at 64 slots
+    # status + two per-(b,h) counter arrays + scores + the kept blocks' pool
+    # rows (kmax per pair) + split partials o and (m, l); 130 work units (128
+    # blocks, a partial block, the draft tile) capped at 64 slots
     pairs = 4 * 8
     ctrs = 2 * 256
     scores = pairs * 2048 * 4
+    rows = pairs * 128 * 4
     part = pairs * 64 * 32 * 128 * 4
     ml = pairs * 64 * 32 * 2 * 4
-    assert n == 256 + ctrs + scores + part + ml
+    assert n == 256 + ctrs + scores + rows + part + ml
     # 8 selected blocks + a partial last block + the draft tile + one slot
     # for a run that leaves a pair mid-stream = 11 partial slots
     n8 = api.sv_workspace_bytes(s, 2048, 8)
-    assert n8 == 256 + ctrs + scores + pairs * 11 * 32 * 128 * 4 + pairs * 11 * 32 * 2 * 4
+    assert n8 == (256 + ctrs + scores + pairs * 8 * 4 + pairs * 11 * 32 * 128 * 4
+                  + pairs * 11 * 32 * 2 * 4)
     bad = api.make_shape(4, 30, 8, 128, 64, 8, torch.bfloat16)  # Hq % Hkv != 0
     assert api.sv_workspace_bytes(bad, 2048, 128) == 0
     assert api.sv_workspace_bytes(api.make_shape(1, 4, 2, 12, 16, 4, 1), 64, 8) == 0  # d % 8
@@ -141,8 +143,9 @@ def test_invalid_arguments_rejected_before_launch(L):
     st, msg = _status(L, L.sv_sparse_attend, C.byref(s), fake, C.byref(kv), fake, 8, 8, fake, fake,
                       bad_par, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "draft_parent" in msg
+    slot8 = api.SelSlotC(fake, 8, 0)
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), fake, C.byref(b), fake,
-                      fake, None, 3, fake, 8, None, fake, fake, ws_n, None)
+                      fake, None, 3, C.byref(slot8), None, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "reuse" in msg
     big_t = api.make_shape(1, 4, 2, 64, 16, 65, torch.float32)
     st, msg = _status(L, L.sv_sparse_attend, C.byref(big_t), fake, C.byref(kv), fake, 8, 8, fake,
@@ -177,11 +180,32 @@ def test_verify_full_mode_needs_no_selection_buffers(L):
     kv = api.KV(fake, fake, fake, 64, 64, 1024)
     ws_n = api.sv_workspace_bytes(s, 64, 8)
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, None, fake,
-                      fake, None, 3, None, 0, None, fake, fake, ws_n, None)
+                      fake, None, 3, None, None, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "reuse" in msg
+    slot8 = api.SelSlotC(None, 8, 0)
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, None, fake,
-                      fake, None, 2, None, 8, None, fake, fake, ws_n - 1, None)
+                      fake, None, 2, C.byref(slot8), None, fake, fake, ws_n - 1, None)
     assert st == api.SV_ERR_WORKSPACE, msg  # got past every selection check
+
+
+def test_reuse_of_unwritten_or_stale_slot_is_refused(L):
+    """Inter-layer reuse may only read a selection that a computing call
+    wrote for the same shape, context and budget: a slot whose stamp is 0
+    (never written) or another call's digest is refused on the host, before
+    anything is launched."""
+    s = api.make_shape(1, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20
+    kv = api.KV(fake, fake, fake, 64, 64, 1024)
+    b = api.make_budget(W.Budget(W.BUDGET_FIXED, 8, 0, 0, 0, 0, 0))
+    ws_n = api.sv_workspace_bytes(s, 64, 8)
+    for stamp, words in ((0, "no computing call"), (0x1234, "another shape")):
+        slot = api.SelSlotC(fake, 8, stamp)
+        st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, C.byref(b),
+                          fake, fake, None, 1, C.byref(slot), None, fake, fake, ws_n, None)
+        assert st == api.SV_ERR_INVALID_ARG and words in msg, msg
+    st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), None, C.byref(b),
+                      fake, fake, None, 1, None, None, fake, fake, ws_n, None)
+    assert st == api.SV_ERR_INVALID_ARG and "slot" in msg
 
 
 def test_per_sequence_context_validation(L):
@@ -248,8 +272,9 @@ def test_per_sequence_budget_checked_against_kmax(L):
     st, msg = _status(L, L.sv_score_select, C.byref(s), fake, fake, C.byref(kv), C.byref(b),
                       fake, 29, C.byref(k), fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "k=30 exceeds kmax=29" in msg
+    slot29 = api.SelSlotC(fake, 29, 0)
     st, msg = _status(L, L.sv_verify_layer, C.byref(s), fake, C.byref(kv), fake, C.byref(b), fake,
-                      fake, None, 0, fake, 29, None, fake, fake, ws_n, None)
+                      fake, None, 0, C.byref(slot29), None, fake, fake, ws_n, None)
     assert st == api.SV_ERR_INVALID_ARG and "k=30 exceeds kmax=29" in msg
     # one sequence too long for the block table's width
     arr2 = (C.c_int32 * 2)(16, 16 * 64 + 1)  # needs 65 columns

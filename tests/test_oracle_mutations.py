@@ -20,6 +20,7 @@ _orig_budget = O.budget_blocks
 _orig_reps = O.block_representatives
 _orig_sparse = O.sparse_attend
 _orig_kept = O.smooth_kept_tokens
+_orig_depths = O.draft_depths
 
 
 def _anc_transposed(parents, t):        # sees later drafts instead of earlier ones
@@ -97,6 +98,10 @@ def _sparse_tail_dropped(q, k_pool, v_pool, bt, sel, dk, dv, parents, tail_block
     return _orig_sparse(q, k_pool, v_pool, bt, sel, dk, dv, parents)  # forgets the partial block
 
 
+def _depths_as_index(parents):          # position distance = index distance, not depth
+    return list(range(len(parents)))
+
+
 MUTATIONS = {
     "mask_transposed": ("ancestors", _anc_transposed),
     "mask_without_self": ("ancestors", _anc_without_self),
@@ -113,6 +118,7 @@ MUTATIONS = {
     "reps_wrong_divisor": ("block_representatives", _reps_off_by_one),
     "attend_head_mapping": ("sparse_attend", _sparse_heads_mod),
     "attend_tail_dropped": ("sparse_attend", _sparse_tail_dropped),
+    "overlap_index_distance": ("draft_depths", _depths_as_index),
 }
 
 

@@ -484,7 +484,7 @@ def test_stack_llama8b_60k_reuse():
         st = api.LayerState(wl, xd)
         reuse = l % wl.compute_every != 0
         if reuse:
-            st.sel = prev.sel.clone()
+            st.slot = prev.slot.copy()
         st.verify(reuse=int(reuse))
         torch.cuda.synchronize()
         assert api.sv_read_status(st.ws) == 0
@@ -668,7 +668,7 @@ def test_stack_reuse_schedules(every):
         st = api.LayerState(wl, xd)
         reuse = l % every != 0
         if reuse:
-            st.sel = prev.sel.clone()
+            st.slot = prev.slot.copy()
         st.verify(reuse=int(reuse))
         torch.cuda.synchronize()
         assert api.sv_read_status(st.ws) == 0
@@ -707,6 +707,60 @@ def test_draft_selection_overlap_vs_oracle():
     # to within one block
     assert (got - want).abs().max().item() <= 1.0 / k + 1e-12
     assert (got - want).abs().mean().item() < 0.02
+
+
+def test_reuse_guard_on_device():
+    """A reuse layer may read a slot only after a computing layer wrote it for
+    the same context and budget: the matching reuse attends over it, while a
+    slot written for another context, or never written, is refused."""
+    from dataclasses import replace
+    wl = small_wl(ctx=64 * 30)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st0 = api.LayerState(wl, xd)
+    st0.verify()
+    st1 = api.LayerState(wl, xd, build_reps=False)
+    out1 = st1.verify(reuse=api.VERIFY_REUSE, sel_from=st0)
+    torch.cuda.synchronize()
+    U.compare_out(out1, st0.out.cpu().double(), 0.0)  # same inputs, same set: same output
+    st2 = api.LayerState(replace(wl, ctx=wl.ctx - 64), xd, build_reps=False)
+    with pytest.raises(api.SvError) as e:
+        st2.verify(reuse=api.VERIFY_REUSE, sel_from=st0)
+    assert e.value.status == api.SV_ERR_INVALID_ARG
+    fresh = api.LayerState(wl, xd, build_reps=False)
+    with pytest.raises(api.SvError) as e:
+        fresh.verify(reuse=api.VERIFY_REUSE)
+    assert e.value.status == api.SV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("tree", [False, True], ids=["chain", "tree16"])
+def test_overlap_by_distance_vs_oracle(tree):
+    """The overlap of draft pairs' own block sets by position distance (the
+    figure after the Figure 1 caption), on the device: every draft's own
+    selection against the oracle's (bit-exact outside a boundary band), and
+    the per-distance means against the oracle's when the sets agree."""
+    from sparse_verification_attention_gb300 import diagnostics
+    over = dict(B=2, Hq=16, Hkv=2, T=16, parents=W.TREE16_PARENTS) if tree else dict(B=2, T=8)
+    wl = small_wl(ctx=64 * 40, **over)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    k = 10
+    sels = diagnostics.draft_selections(st.shape, xd.q, st.reps, st.kv, k).cpu()
+    reps = O.block_representatives(x.k_pool, x.block_table, wl.NB, wl.blk)
+    differ = 0
+    for t in range(wl.T):
+        scores = O.block_scores(x.q[:, t:t + 1], reps, wl.G)
+        differ += len(U.compare_selection(sels[t].view(wl.B, wl.Hkv, k), scores, k))
+    ov0, byd = diagnostics.selection_overlaps(st.shape, xd.q, st.reps, st.kv, k, wl.parents)
+    want = O.draft_overlap_by_distance(x.q, reps, wl.G, k, wl.parent_list())
+    assert torch.equal(torch.isnan(byd), torch.isnan(want))
+    assert torch.all(ov0[:, :, 0] == 1.0)
+    if differ == 0:
+        ok = ~torch.isnan(want)
+        assert torch.allclose(byd[ok], want[ok], rtol=0, atol=1e-6)
+        assert torch.allclose(ov0, O.draft_selection_overlap(x.q, reps, wl.G, k), rtol=0,
+                              atol=1e-6)
 
 
 def test_verify_full_mode_equals_dense():
