@@ -1,10 +1,13 @@
 """Benchmark: sparse verification attention on one GB300 (or N replicas).
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-incremental representative build for the newest full block of every
-sequence, block scoring, budgeted top-k selection, split-KV sparse attention
-and the log-sum-exp merge (for a multi-layer stack: every layer, with the
-selection recomputed on computing layers and reused on the others).
+One step = one verification layer per layer of the workload through the
+public per-layer call (sv_verify_layer): on a computing layer the fused
+block scoring + budgeted top-k selection kernel, then the split-KV
+tensor-core attention whose last CTA per (sequence, KV head) merges the
+partials; on a reuse layer (the 32-layer stack) only the attention, over the
+previous computing layer's selection. Representatives are built at prefill
+and rebuilt when a block fills (every blk / T steps), outside the step; that
+update is timed on its own (`rep_update`).
 
 Prints ONE JSON line (rank 0). Timing: W warm-up steps, then exactly K steps
 replayed from CUDA graphs, bracketed by a barrier and a device synchronize on
@@ -12,11 +15,16 @@ both sides, CUDA events on the launching stream, max over ranks. L2: the
 steps rotate over enough independent input sets that their working set is
 >= 4x the L2 size, so every step reads cold HBM.
 
-Roofline: the attention launch (selected-block gather + tensor-core
-attention + in-cluster merge) is timed with CUDA events on its stream over a
-second timed loop of graph-replayed attention launches (rotating input sets);
-algorithmic bytes per launch are the selected K/V pages, the draft K/V, Q and
-O.
+Roofline: the attention launch alone is timed with CUDA events on its stream
+over a second loop of graph-replayed attention launches (rotating input sets,
+at least 100 ms so the clock sampler sees it under load); algorithmic bytes
+per launch are the selected K/V pages, the draft K/V, Q and O. The step's own
+fraction (all algorithmic bytes of a step over the step time) is reported
+beside it.
+
+per_config: the same measurements, briefly, on the other workloads the
+metric spans (32K, the 64K tree, the 32-layer stack); the tiny fp32 workload
+is a parity case only.
 
 --impl reference runs the CPU oracle (the only reference this method has) on
 a bounded sample of the same workload and reports the same metric.
@@ -285,9 +293,9 @@ def run_reference(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(wl, None),
-        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": torch.get_num_threads(),
-                         "kind": "oracle", "sample": desc},
+        "data": "synthetic", "config": config_of(wl, o.O.budget_from(wl.budget, wl.ctx, wl.NB)),
+        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": os.cpu_count(),
+                         "threads": torch.get_num_threads(), "kind": "oracle", "sample": desc},
         "e2e": {"value": tok_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -317,32 +325,94 @@ class StepSet:
                 self.layers[l].slot = self.layers[l - (l % wl.compute_every)].slot
 
 
-def run_step(wl, ss: StepSet, ev=None):
-    """Launch one step on the current stream (graph-capturable): per layer,
-    score + select on computing layers, then the sparse attention."""
+def run_step(wl, ss: StepSet):
+    """Launch one step on the current stream (graph-capturable): one
+    sv_verify_layer call per layer, computing or reusing the selection."""
     from sparse_verification_attention_gb300 import api
     for l, st in enumerate(ss.layers):
-        computing = l % wl.compute_every == 0
-        if computing:
-            api.sv_score_select(st.shape, st.x.q, st.reps, st.kv, wl.budget, st.sel, st.kmax,
-                                st.ws)
-        if ev is not None:
-            ev[0].record()
-        api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
-                             st.x.draft_v, st.parents, st.out, st.ws)
-        if ev is not None:
-            ev[1].record()
+        reuse = api.VERIFY_COMPUTE if l % wl.compute_every == 0 else api.VERIFY_REUSE
+        api.sv_verify_layer(st.shape, st.x.q, st.kv, st.reps, wl.budget, st.x.draft_k,
+                            st.x.draft_v, st.parents, reuse, st.slot, st.out, st.ws)
 
 
-def run_gpu(args, wl, rank, world, dist):
-    from sparse_verification_attention_gb300 import api, build_lib
-    build_lib.build()
-    dev = args.local_rank
-    torch.cuda.set_device(dev)
+def attend_launch(st):
+    """The attention of one layer alone, over the layer's own selection."""
+    from sparse_verification_attention_gb300 import api
+    api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
+                         st.x.draft_v, st.parents, st.out, st.ws)
+
+
+def timed_replays(graph_fn, min_ms: float, per_replay_units: int):
+    """Replay a graph until at least min_ms of device time (after one
+    untimed replay); returns ms per unit. CUDA events on the current stream."""
+    graph_fn()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    graph_fn()
+    a1.record()
+    torch.cuda.synchronize()
+    once = max(a0.elapsed_time(a1), 1e-3)
+    n = max(3, int(math.ceil(min_ms / once)))
+    a0.record()
+    for _ in range(n):
+        graph_fn()
+    a1.record()
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) / (n * per_replay_units)
+
+
+def sdpa_dense(wl, st):
+    """torch SDPA over the whole context gathered into logical order, with the
+    draft mask (a dense yardstick from a library kernel; the gather is done
+    once, outside the timing). Returns ms per call, or a reason string."""
+    import torch.nn.functional as F
+    x = st.x
+    try:
+        nbt = wl.NBT
+        pages = x.block_table[:, :nbt].long()                              # [B, nbt]
+        def ctx_of(pool):
+            g = pool[pages]                                                # [B, nbt, Hkv, blk, d]
+            g = g.permute(0, 2, 1, 3, 4).reshape(wl.B, wl.Hkv, nbt * wl.blk, wl.d)
+            return g[:, :, :wl.ctx]
+        k = torch.cat([ctx_of(x.k_pool), x.draft_k.transpose(1, 2)], dim=2).contiguous()
+        v = torch.cat([ctx_of(x.v_pool), x.draft_v.transpose(1, 2)], dim=2).contiguous()
+        q = x.q.transpose(1, 2).contiguous()                               # [B, Hq, T, d]
+        mask = torch.zeros(wl.T, wl.ctx + wl.T, dtype=torch.bool, device=q.device)
+        mask[:, :wl.ctx] = True
+        par = wl.parent_list()
+        for t in range(wl.T):
+            u = t
+            while u >= 0:
+                mask[t, wl.ctx + u] = True
+                u = par[u]
+        call = lambda: F.scaled_dot_product_attention(q, k, v, attn_mask=mask, enable_gqa=True)
+        call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(5)]
+        for a, b in ev:
+            a.record()
+            call()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        del k, v, q
+        torch.cuda.empty_cache()
+        return ms
+    except (RuntimeError, TypeError) as e:  # backend without this mask/GQA form
+        return f"unavailable: {str(e).splitlines()[0][:160]}"
+
+
+def measure(args, wl, dist, steps: int, warmup: int, full: bool, clocks=None):
+    """Every GPU number of one workload: the timed steps, the attention
+    roofline loop, the e2e loop; with full=True also the dense yardsticks and
+    the rep update. Returns (fields, sets, k)."""
+    from sparse_verification_attention_gb300 import api
     k = budget_k(wl)
     sbytes = step_bytes(wl, k)
     abytes = attend_bytes(wl, k)
-    props = torch.cuda.get_device_properties(dev)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
     l2 = getattr(props, "L2_cache_size", 129 * 2 ** 20)
     n_sets = max(2, math.ceil(4 * l2 / sbytes))
     if args.sets:
@@ -350,11 +420,10 @@ def run_gpu(args, wl, rank, world, dist):
     ps = W.planted_sets(wl)
     sets = [StepSet(wl, i, ps) for i in range(n_sets)]
     torch.cuda.synchronize()
-    log(f"{n_sets} input sets resident")
+    log(f"{wl.name}: {n_sets} input sets resident")
     stream = torch.cuda.current_stream()
 
     # one CUDA graph per input set, each holding one whole step
-    graphs = []
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -362,6 +431,7 @@ def run_gpu(args, wl, rank, world, dist):
             run_step(wl, ss)
     stream.wait_stream(side)
     torch.cuda.synchronize()
+    graphs = []
     for ss in sets:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -369,143 +439,189 @@ def run_gpu(args, wl, rank, world, dist):
         graphs.append(g)
     torch.cuda.synchronize()
     check_status(sets, "graph capture")
-    log("graphs captured")
 
-    clocks = ClockSampler(dev)
-    clocks.start()
-    for i in range(args.warmup):
+    if clocks is not None:
+        clocks.start()
+    for i in range(warmup):
         graphs[i % n_sets].replay()
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(args.steps):
+    for i in range(steps):
         graphs[i % n_sets].replay()
     e1.record()
     torch.cuda.synchronize()
     barrier(dist)
-    ms_total = e0.elapsed_time(e1)
-    clk = clocks.stop()
+    ms_total = max_over_ranks(dist, e0.elapsed_time(e1))
     check_status(sets, "timed steps")
-    log(f"timed steps done: {ms_total / args.steps * 1e3:.1f} us/step")
-    ms_total = max_over_ranks(dist, ms_total)
-    ms_step = ms_total / args.steps
-    tokens = sum_over_ranks(dist, wl.B * wl.T * args.steps)
-    value = tokens / (ms_total / 1e3)
+    ms_step = ms_total / steps
+    tokens = sum_over_ranks(dist, wl.B * wl.T * steps)
+    log(f"{wl.name}: timed steps {ms_step * 1e3:.1f} us/step")
 
     # roofline: the attention launches alone, back to back as in a layer
-    # stack: one CUDA graph of kRoofLaunches launches rotating over the input
-    # sets (cold L2), replayed; CUDA events on the launching stream
+    # stack, one CUDA graph of kRoofLaunches launches rotating over the input
+    # sets (cold L2), replayed for at least 100 ms; CUDA events on the stream
     kRoofLaunches = 20
     att_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(att_graph):
         for i in range(kRoofLaunches):
             for st in sets[i % n_sets].layers:
-                api.sv_sparse_attend(st.shape, st.x.q, st.kv, st.sel, st.k, st.kmax, st.x.draft_k,
-                                     st.x.draft_v, st.parents, st.out, st.ws)
-    n_rep = max(3, min(args.steps // kRoofLaunches, 100))
-    att_graph.replay()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record()
-    for i in range(n_rep):
-        att_graph.replay()
-    a1.record()
-    torch.cuda.synchronize()
-    attend_ms = a0.elapsed_time(a1) / (n_rep * kRoofLaunches * wl.layers)
+                attend_launch(st)
+    attend_ms = timed_replays(att_graph.replay, 100.0 if full else 20.0,
+                              kRoofLaunches * wl.layers)
+    if clocks is not None:
+        clk = clocks.stop()
+    else:
+        clk = None
     check_status(sets, "attention-only replays")
-    log(f"attention launches: {attend_ms * 1e3:.1f} us")
+    log(f"{wl.name}: attention launches {attend_ms * 1e3:.1f} us")
     peak, peak_kind = read_peaks()
     achieved = abytes / (attend_ms / 1e3) / 1e9
-
-    # dense full-KV verification (same kernels, every block) for comparison
+    step_gbs = sbytes / (ms_step / 1e3) / 1e9
     st0 = sets[0].layers[0]
-    dense = None
-    if args.dense and wl.NB:
+    plan = api.sv_attend_plan(st0.shape, st0.kv, k)
+    f = {
+        "value": tokens / (ms_total / 1e3), "ms_per_step": ms_step, "k": k,
+        "n_sets": n_sets, "l2": l2, "step_bytes": sbytes, "step_gbs": step_gbs,
+        "step_frac": step_gbs / peak, "attend_bytes": abytes, "attend_ms": attend_ms,
+        "attend_gbs": achieved, "attend_frac": achieved / peak, "peak": peak,
+        "peak_kind": peak_kind, "plan": plan, "clocks": clk,
+    }
+
+    if full and args.dense and wl.NB:
+        # dense full-KV verification: the same kernels with every block kept,
+        # and torch SDPA over the gathered context
         dws = api.alloc_workspace(st0.shape, wl.NB, wl.NB)
         dout = torch.empty_like(st0.out)
+        dcall = lambda: api.sv_sparse_attend(st0.shape, st0.x.q, st0.kv, None, 0, 0,
+                                             st0.x.draft_k, st0.x.draft_v, st0.parents, dout, dws)
+        dcall()
         de = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(5)]
-        api.sv_sparse_attend(st0.shape, st0.x.q, st0.kv, None, 0, 0, st0.x.draft_k,
-                             st0.x.draft_v, st0.parents, dout, dws)
         for a, b in de:
             a.record()
-            api.sv_sparse_attend(st0.shape, st0.x.q, st0.kv, None, 0, 0, st0.x.draft_k,
-                                 st0.x.draft_v, st0.parents, dout, dws)
+            dcall()
             b.record()
         torch.cuda.synchronize()
         dms = statistics.median(a.elapsed_time(b) for a, b in de)
         dbytes = attend_bytes(wl, wl.NB)
-        dense = {"attend_ms": dms, "gbs": dbytes / (dms / 1e3) / 1e9,
-                 "sparse_speedup": dms / attend_ms, "note": "same kernels, all blocks kept"}
+        sd = sdpa_dense(wl, st0)
+        f["dense"] = {"attend_ms": dms, "gbs": dbytes / (dms / 1e3) / 1e9,
+                      "sparse_speedup": dms / attend_ms, "note": "same kernels, all blocks kept",
+                      "torch_sdpa_ms": sd if isinstance(sd, float) else None,
+                      "torch_sdpa_note": ("torch scaled_dot_product_attention over the "
+                                          "gathered context + drafts with the draft mask, GQA"
+                                          if isinstance(sd, float) else sd),
+                      "sparse_speedup_vs_sdpa": (sd / attend_ms) if isinstance(sd, float) else None}
+        del dws, dout
 
-    # the incremental rep update (one newly filled block per (b, h)), outside
-    # the step: a block fills every blk / T steps
-    rep_update = None
-    if wl.NB:
+    if full and wl.NB:
+        # the incremental rep update (one newly filled block per (b, h)),
+        # outside the step: a block fills every blk / T steps
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(kRoofLaunches):
                 st = sets[i % n_sets].layers[0]
                 api.sv_build_reps(st.shape, st.kv, wl.NB - 1, 1, st.reps)
-        g.replay()
-        torch.cuda.synchronize()
-        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        r0.record()
-        for i in range(n_rep):
-            g.replay()
-        r1.record()
-        torch.cuda.synchronize()
-        rus = r0.elapsed_time(r1) / (n_rep * kRoofLaunches) * 1e3
-        rep_update = {"us_per_layer": rus, "bytes_per_layer": rep_update_bytes(wl),
-                      "every_steps": wl.blk / max(1, wl.T),
-                      "note": "sv_build_reps of one newly filled block per (b, h); not in the step"}
+        rms = timed_replays(g.replay, 5.0, kRoofLaunches)
+        f["rep_update"] = {"us_per_layer": rms * 1e3, "bytes_per_layer": rep_update_bytes(wl),
+                           "every_steps": wl.blk / max(1, wl.T),
+                           "note": "sv_build_reps of one newly filled block per (b, h); "
+                                   "not in the step"}
 
     # e2e: the public call with host buffers, copies inside the timed region
-    e2e = run_e2e(args, wl, sets, dist)
+    f["e2e"] = run_e2e(args, wl, sets, dist)
     check_status(sets, "e2e")
-    log("e2e done")
+    f["launches_per_step"] = sum((1 if l % wl.compute_every == 0 else 0) +
+                                 (1 if (plan.path == api.SV_PATH_TCGEN05 or plan.cluster > 0)
+                                  else 2) for l in range(wl.layers))
+    return f, sets, k
 
-    # CPU oracle baseline on a bounded sample (rank 0, N=1 only)
+
+def run_gpu(args, wl, rank, world, dist):
+    from sparse_verification_attention_gb300 import api, build_lib
+    build_lib.build()
+    dev = args.local_rank
+    torch.cuda.set_device(dev)
+    clocks = ClockSampler(dev)
+    f, sets, k = measure(args, wl, dist, args.steps, args.warmup, True, clocks)
+    log("headline done")
+
+    # CPU oracle baseline on a bounded sample (rank 0, N=1 only): all host
+    # cores, and one thread
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         o = OracleSample(wl, sets[0].layers[0].x.to("cpu"))
         n, el = o.timed(seconds=args.cpu_seconds)
-        cpu = {"value": n * o.tokens_per_unit() / el, "unit": UNIT,
-               "cores": torch.get_num_threads(), "kind": "oracle", "sample": o.describe(n, el)}
+        threads = torch.get_num_threads()
+        torch.set_num_threads(1)
+        try:
+            n1, el1 = o.timed(seconds=max(2.0, args.cpu_seconds / 3))
+        finally:
+            torch.set_num_threads(threads)
+        cpu = {"value": n * o.tokens_per_unit() / el, "unit": UNIT, "cores": os.cpu_count(),
+               "threads": threads, "kind": "oracle", "sample": o.describe(n, el),
+               "single_thread": {"value": n1 * o.tokens_per_unit() / el1, "unit": UNIT,
+                                 "sample": o.describe(n1, el1)}}
+    del sets
+    torch.cuda.empty_cache()
+
+    # the other workloads of the metric's range, briefly (the same kernels,
+    # the same measurements; no dense yardsticks)
+    per_config = {}
+    if args.per_config:
+        for name in ("llama8b_32k", "qwen3moe_64k_b8_tree16", "llama8b_60k_32layer"):
+            if name == wl.name:
+                continue
+            owl = W.WORKLOADS[name]
+            of, osets, ok_ = measure(args, owl, dist, args.per_config_steps, 3, False)
+            del osets
+            torch.cuda.empty_cache()
+            per_config[name] = {
+                "metric": METRIC, "unit": UNIT, "value": of["value"],
+                "ms_per_step": of["ms_per_step"], "budget_blocks": ok_,
+                "step_bytes": of["step_bytes"], "step_frac": of["step_frac"],
+                "attend_us": of["attend_ms"] * 1e3, "attend_frac": of["attend_frac"],
+                "e2e": {"value": of["e2e"]["value"], "ms_per_step": of["e2e"]["ms_per_step"]},
+                "config": config_of(owl, ok_)}
+        per_config["tiny_f32"] = {"parity_only": True,
+                                  "note": "oracle-sized fp32 case; checked element by element "
+                                          "in the GPU tests, not timed"}
 
     traffic = traffic_from_profile(wl.name)
-    # kernels per layer: the fused score+select on computing layers, the
-    # attention (plus a merge kernel on paths that do not merge in-kernel)
-    plan = api.sv_attend_plan(st0.shape, st0.kv, k)
-    att_launches = 1 if (plan.path == api.SV_PATH_TCGEN05 or plan.cluster > 0) else 2
-    launches_per_step = sum((1 if l % wl.compute_every == 0 else 0) + att_launches
-                            for l in range(wl.layers))
+    plan = f["plan"]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "metric": METRIC, "value": f["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": f["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded Gaussian Q/K/V, planted high-affinity blocks + sink)",
         "config": dict(config_of(wl, k), l2=(
-            f"rotating {n_sets} input sets, {n_sets * sbytes / 1e6:.0f} MB touched per "
-            f"rotation vs {l2 / 1e6:.0f} MB L2 (inputs larger than L2, no flush)")),
-        "step_bytes": sbytes, "step_gbs": sbytes / (ms_step / 1e3) / 1e9,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+            f"rotating {f['n_sets']} input sets, {f['n_sets'] * f['step_bytes'] / 1e6:.0f} MB "
+            f"touched per rotation vs {f['l2'] / 1e6:.0f} MB L2 (inputs larger than L2, "
+            f"no flush)")),
+        "step_bytes": f["step_bytes"], "step_gbs": f["step_gbs"],
+        "step_frac": f["step_frac"],
+        "roofline": {"bound": "hbm", "achieved": f["attend_gbs"], "peak": f["peak"],
+                     "unit": "GB/s", "frac": f["attend_frac"], "traffic": traffic,
                      "kernel": {api.SV_PATH_TCGEN05: "attend_tc_kernel (tcgen05 split-KV "
-                                "attention, in-kernel LSE merge)",
+                                "attention, LSE merge by the last CTA of each pair)",
                                 api.SV_PATH_MMA_SYNC: "attend_fast_kernel (mma.sync split-KV)",
                                 api.SV_PATH_CUDA_CORES: "attend_generic_kernel + merge_kernel"
                                 }[plan.path],
-                     "bytes_per_launch": abytes, "launch_ms": attend_ms,
-                     "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
-                     "frac_of_nominal_8tbs": achieved / 8000.0},
-        "dense": dense,
-        "rep_update": rep_update,
-        "e2e": e2e,
+                     "bytes_per_launch": f["attend_bytes"], "launch_ms": f["attend_ms"],
+                     "peak_kind": f"{f['peak_kind']} HBM copy bandwidth (burst)",
+                     "frac_of_nominal_8tbs": f["attend_gbs"] / 8000.0,
+                     "step_frac": f["step_frac"],
+                     "step_frac_of_nominal_8tbs": f["step_gbs"] / 8000.0},
+        "dense": f.get("dense"),
+        "rep_update": f.get("rep_update"),
+        "e2e": f["e2e"],
         "cpu_baseline": cpu,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "per_config": per_config or None,
+        "gpu_launches": f["launches_per_step"] * args.steps,
+        "clocks": f["clocks"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -568,6 +684,8 @@ def main():
     ap.add_argument("--dense", type=int, default=1)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--per-config", type=int, default=1)
+    ap.add_argument("--per-config-steps", type=int, default=200)
     args = ap.parse_args()
     rank, world, local = dist_env()
     args.local_rank = local

@@ -86,7 +86,7 @@ struct TcCfg {
   static constexpr int kSmem = kCtrlOff + 256 + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // a merge pass of two rows of the most slots a pair can have fits the ring
-  static_assert(2 * (kMaxSplits * (TD * 4 + 8 + 4) + 4) <= kRing, "merge staging");
+  static_assert(2 * kMaxSplits * (TD * 4 + 8) <= kRing, "merge staging");
 };
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -95,6 +95,64 @@ __device__ __forceinline__ void fence_async_smem() {
 
 __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
   return row * 128 + ((chunk16 ^ (row & 7)) << 4);
+}
+
+constexpr int kMergeRowBytes = TD * 4 + 8;  // a partial row's o and (m, l)
+
+// Log-sum-exp combine of rows [r0, r0 + nv) of one pair from partials staged
+// in shared memory: o at so[(s * ld + r) * TD], (m, l) at sml[s * ld + r] for
+// slots s < ns (r relative to r0). Eight threads per row, each with four
+// float4 columns, so every load of a slot is independent of the others;
+// the weights are formed in place (slot order, so the sums do not depend on
+// which CTA merges). All threads of the CTA call it.
+__device__ __forceinline__ void combine_rows(const AttendArgs& a, int b, int h, int ns, int ld,
+                                             int r0, int nv, const float* so, const float2* sml) {
+  constexpr int NT = 32 * 10;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  const int cg = threadIdx.x & 7;
+  for (int r = threadIdx.x >> 3; r < nv; r += NT / 8) {
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < ns) M = fmaxf(M, sml[(s0 + q) * ld + r].x);
+    }
+    float L = 0.f;
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (s0 + q < ns) {
+          const float2 ml = sml[(s0 + q) * ld + r];
+          const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+          L += w * ml.y;
+          const float* orow = so + ((size_t)(s0 + q) * ld + r) * TD;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 o = *reinterpret_cast<const float4*>(orow + (cg + 8 * i) * 4);
+            acc[i].x += w * o.x;
+            acc[i].y += w * o.y;
+            acc[i].z += w * o.z;
+            acc[i].w += w * o.w;
+          }
+        }
+      }
+    }
+    const float inv = 1.0f / L;
+    const int rr = r0 + r, t = rr / a.G, gq = rr % a.G;
+    __nv_bfloat16* dst = out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst + (cg + 8 * i) * 4) = u;
+    }
+  }
 }
 
 // The work of one CTA: up to kMaxSeg segments, each a run of consecutive work
@@ -706,6 +764,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
   if (jf >= 0) {
     const int pair = sp.pair[jf];
     const size_t slot = ((size_t)pair * a.slot_stride + sp.slot[jf]) * a.rpad;
+    float* own_o = a.part_o + slot * TD;
+    float2* own_ml = reinterpret_cast<float2*>(a.part_ml) + slot;
     if (warp < 8 && (warp & 3) < NSW) {
       const int row = (warp >> 2) * KR + 32 * (warp & 3) + lane;
 #pragma unroll
@@ -724,8 +784,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
       const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
       const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
       *reinterpret_cast<float2*>(pw + 2 * rr) = make_float2(wa, wb);
-      if (rr < a.rpad)
-        *reinterpret_cast<float2*>(a.part_ml + (slot + rr) * 2) = make_float2(M, wa * ma.y + wb * mb.y);
+      if (rr < a.rpad) own_ml[rr] = make_float2(M, wa * ma.y + wb * mb.y);
     }
     __syncthreads();
     // folded rows straight to the workspace (rows past kRows are zero padding)
@@ -739,7 +798,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         v = make_float4(w.x * oa.x + w.y * ob.x, w.x * oa.y + w.y * ob.y, w.x * oa.z + w.y * ob.z,
                         w.x * oa.w + w.y * ob.w);
       }
-      *reinterpret_cast<float4*>(a.part_o + (slot + rr) * TD + c4) = v;
+      *reinterpret_cast<float4*>(own_o + (size_t)rr * TD + c4) = v;
     }
     // CTA barrier, then one thread's acquire-release arrival publishes
     // every thread's partial writes (the barrier orders them before it); the
@@ -757,30 +816,23 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // segment count) merges every row of that pair; all other CTAs are done.
   // No CTA ever waits for another, so nothing here depends on which CTAs
   // are resident at the same time.
-  //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s.
-  // The partials come into the idle ring by bulk copies (one per slot and
-  // row range), so one CTA reads them at the copy engine's rate rather than
-  // at the rate its threads can keep loads in flight. The merging CTA also
-  // returns the count word to zero for the next call: every arrival of this
-  // call is in by then.
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
+  // summed in slot order whichever CTA merges, so results do not depend on
+  // timing. The partials come into the idle ring by bulk copies (one per slot
+  // and row range). The merging CTA also returns the count word to zero for
+  // the next call: every arrival of this call is in by then.
   uint32_t mphase = 0;
   for (int j = 0; j < sp.n; ++j) {
     if (!pair_done[j]) continue;  // the same in every thread (set before a barrier)
-    const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
+    const int pair = sp.pair[j];
     const int ns = sp.nseg[j] + sp.mid[j];
     const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    // rows per pass: the staging holds, per slot and row, its o row (512 B),
-    // its (m, l) (8 B) and its weight (4 B), plus a normaliser per row; an
-    // even count, so that every (m, l) copy is a multiple of 16 bytes. With
-    // at most 64 slots two rows always fit.
-    constexpr int kRowBytes = TD * 4 + 8;  // copied per slot and row
-    int rpp = (C::kRing / (ns * (kRowBytes + 4) + 4)) & ~1;
+    // rows per pass: an even count (every (m, l) copy a multiple of 16
+    // bytes); with at most 64 slots two rows always fit
+    int rpp = (C::kRing / (ns * kMergeRowBytes)) & ~1;
     rpp = rpp < 2 ? 2 : (rpp > a.rpad ? a.rpad : rpp);
-    float* so = reinterpret_cast<float*>(ring);                 // [ns][rpp][TD]
+    float* so = reinterpret_cast<float*>(ring);                           // [ns][rpp][TD]
     float2* sml = reinterpret_cast<float2*>(so + (size_t)ns * rpp * TD);  // [ns][rpp]
-    float* sw = reinterpret_cast<float*>(sml + (size_t)ns * rpp);          // [ns][rpp]
-    float* sinv = sw + (size_t)ns * rpp;                                   // [rpp]
     for (int r0 = 0; r0 < a.R; r0 += rpp) {
       const int nr = min(rpp, a.rpad - r0);  // rows copied (padding rows included)
       if (threadIdx.x == 0) {
@@ -789,7 +841,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         asm volatile("fence.proxy.async.global;" ::: "memory");
         fence_async_smem();
         const uint32_t mb = smem_u32(merge_bar);
-        mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kRowBytes));
+        mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kMergeRowBytes));
         for (int sl = 0; sl < ns; ++sl) {
           const size_t row0 = pbase + (size_t)sl * a.rpad + r0;
           bulk_load(smem_u32(so + (size_t)sl * rpp * TD), a.part_o + row0 * TD,
@@ -797,43 +849,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
           bulk_load(smem_u32(sml + (size_t)sl * rpp), a.part_ml + row0 * 2, (uint32_t)(nr * 8), mb);
         }
       }
-      const bool got = mbar_wait_drain(smem_u32(merge_bar), mphase);
+      if (!mbar_wait_drain(smem_u32(merge_bar), mphase) && threadIdx.x == 0)
+        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
       mphase ^= 1u;
-      if (!got && threadIdx.x == 0) atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      const int nv = min(rpp, a.R - r0);  // real rows of this pass
-      for (int r = threadIdx.x; r < nv; r += NT) {
-        float M = -INFINITY;
-        for (int sl = 0; sl < ns; ++sl) M = fmaxf(M, sml[sl * rpp + r].x);
-        float L = 0.f;
-        for (int sl = 0; sl < ns; ++sl) {
-          const float2 ml = sml[sl * rpp + r];
-          const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-          L += w * ml.y;
-          sw[sl * rpp + r] = w;
-        }
-        sinv[r] = 1.0f / L;
-      }
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < nv * (TD / 4); idx += NT) {
-        const int r = idx / (TD / 4), c = (idx % (TD / 4)) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sl = 0; sl < ns; ++sl) {
-          const float w = sw[sl * rpp + r];
-          const float4 o = *reinterpret_cast<const float4*>(so + ((size_t)sl * rpp + r) * TD + c);
-          acc.x += w * o.x;
-          acc.y += w * o.y;
-          acc.z += w * o.z;
-          acc.w += w * o.w;
-        }
-        const float inv = sinv[r];
-        const int rr = r0 + r, t = rr / a.G, gq = rr % a.G;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&lo);
-        u.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c) = u;
-      }
+      combine_rows(a, pair / a.Hkv, pair % a.Hkv, ns, rpp, r0, min(rpp, a.R - r0), so, sml);
       __syncthreads();  // the next pass's copies overwrite the staging area
     }
     if (threadIdx.x == 0) a.counters[pair] = 0u;
