@@ -141,16 +141,25 @@ int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
 
 /* Bytes of workspace that score/select/attend/verify calls with this shape
  * need, for selections of up to kmax blocks over up to nb_max blocks. The
- * first 256 bytes hold the device status word; after it come two arrays of
- * per-(b, h) arrival counters (the last CTA of a pair to arrive does that
- * pair's selection or split merge). The whole workspace must be zero before
- * its first use (allocate it zeroed). Every call returns the counters to
- * zero; the status word keeps its flags until sv_clear_status. Returns 0 on
- * an invalid shape. Host only. */
+ * first 256 bytes hold the device status word; after it come three arrays
+ * of per-(b, h) words, one 128-byte line each (scoring and attention
+ * counts, a merge claim word), then scores, pool rows and split partials. The whole workspace
+ * must be zero before its first use (allocate it zeroed). Every call that
+ * completes returns the per-(b, h) words to zero; the status word keeps its
+ * flags until sv_clear_status. A call that raised SV_FLAG_WAIT_TIMEOUT may
+ * leave those words non-zero: call sv_reset_workspace before the workspace
+ * is used again. Returns 0 on an invalid shape. Host only. */
 size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax);
 
 /* Zero the workspace status word (async on stream). */
 sv_status sv_clear_status(void* workspace, void* stream);
+
+/* Zero the status word and every per-(b, h) count and flag of a workspace
+ * laid out for (shape, nb_max, kmax) (async on stream): what a workspace
+ * needs after a call that raised SV_FLAG_WAIT_TIMEOUT. Scores, rows and
+ * partials need no reset (every call writes them before it reads them). */
+sv_status sv_reset_workspace(const sv_shape* shape, int nb_max, int kmax, void* workspace,
+                             size_t ws_bytes, void* stream);
 
 /* Synchronously read the workspace status word into *flags (host). Returns
  * SV_ERR_DEVICE_FAULT when any flag is set. */

@@ -31,7 +31,7 @@ EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
             "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
             "sv_verify_layer", "sv_sparse_attend_noalloc", "sv_append_kv",
-            "sv_selection_overlap")
+            "sv_selection_overlap", "sv_reset_workspace")
 
 
 class SvError(RuntimeError):
@@ -123,6 +123,7 @@ def lib() -> C.CDLL:
             "sv_append_kv": (i, [C.POINTER(Shape), vp, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp,
                                  vp]),
             "sv_selection_overlap": (i, [vp, i, i, i, i, C.POINTER(C.c_int32), vp, vp, vp]),
+            "sv_reset_workspace": (i, [C.POINTER(Shape), i, i, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -215,6 +216,13 @@ def alloc_workspace(shape: Shape, nb_max: int, kmax: int, device="cuda") -> torc
 
 def sv_clear_status(ws: torch.Tensor, stream=None):
     _check(lib().sv_clear_status(_ptr(ws), _stream(stream)))
+
+
+def sv_reset_workspace(shape: Shape, nb_max: int, kmax: int, ws: torch.Tensor, stream=None):
+    """Zero the workspace's status word and per-(b, h) counts and flags (what
+    a workspace needs after a call that raised SV_FLAG_WAIT_TIMEOUT)."""
+    _check(lib().sv_reset_workspace(C.byref(shape), nb_max, kmax, _ptr(ws), ws.numel(),
+                                    _stream(stream)))
 
 
 def sv_read_status(ws: torch.Tensor, stream=None) -> int:

@@ -98,6 +98,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
 }
 
 constexpr int kMergeRowBytes = TD * 4 + 8;  // a partial row's o and (m, l)
+constexpr size_t kSoloMergeBytes = 128 * 1024;  // see launch_attend_tc
 
 // Log-sum-exp combine of rows [r0, r0 + nv) of one pair from partials staged
 // in shared memory: o at so[(s * ld + r) * TD], (m, l) at sml[s * ld + r] for
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
   int* stage_info = reinterpret_cast<int*>(tmem_slot + 1);  // bit0 valid, bit1 draft tile
   volatile int* abort_flag = stage_info + NS;
   volatile int* pair_done = abort_flag + 1;  // [kMaxSeg]: this CTA saw the pair complete
+  volatile int* merge_got = pair_done + kMaxSeg;  // merge slices this CTA claimed
   // ancestor masks of the drafts, copied out of the parameter space with
   // warp-uniform indices (per-lane indices into it would serialize)
   __shared__ unsigned long long s_anc[kMaxT];
@@ -317,6 +319,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
       }
     }
   }
+  if (warp == MMAW) {
+    // touch every line of the parameter block while the previous kernel
+    // drains, so that no role pays a cold parameter read after the wait
+    const uint32_t* pw = reinterpret_cast<const uint32_t*>(&a);
+    uint32_t acc = 0;
+    for (int w = lane * 16; w < (int)(sizeof(AttendArgs) / 4); w += 32 * 16) acc ^= pw[w];
+    asm volatile("" ::"r"(acc));  // keeps the reads
+  }
   pdl_wait();     // everything below may read what earlier kernels wrote
   pdl_trigger();  // let the next kernel launch and run its prologue
 
@@ -325,7 +335,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // one 3-D TMA box per 64 dims (issued first by the producer) with rows
   // R..127 zeroed here; the second segment's Q is written by these four warps
   // into TMEM (lane = row), where the MMA reads it as a tensor-memory A operand.
-  if (warp < 4) {
+  // zero the Q operand's padding rows R..127 and count this warp on q_ready
+  auto zero_q_padding = [&]() {
     const int r = threadIdx.x;
     if (r >= a.R) {
 #pragma unroll
@@ -335,6 +346,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(q_ready));
+  };
+  if (warp < 4) {
+    zero_q_padding();
+    const int r = threadIdx.x;
     if (sp.n > 1) {
       const int b1 = sp.pair[1] / a.Hkv, h1 = sp.pair[1] % a.Hkv;
       const uint4* q1 = static_cast<const uint4*>(a.q) +
@@ -377,7 +392,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
     const int oob_row = a.num_pages * a.Hkv * TBLK;  // past the end: TMA zero-fills
     int issued = 0;
     bool stop = false;
-    int i = 0;  // tile index over all segments
+    int i = 0;  // ring index (a stage is i % NS, its phase parity (i / NS) & 1)
     for (int j = 0; j < sp.n && !stop; ++j) {
       const int pair = sp.pair[j], b = pair / a.Hkv, h = pair % a.Hkv;
       const int nsel = n_of(a.vl, b, a.n_sel), nbb = nb_of(a.vl, b, a.nb);
@@ -388,7 +403,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         int row = oob_row, ok = 0;
         if (base + lane < nblk && a.rows) {
           // resolved by the select step (which flagged any bad page as -1)
-          const int rr = a.rows[(size_t)pair * a.sel_stride + ub + base + lane];
+          const int rr = __ldcg(a.rows + (size_t)pair * a.sel_stride + ub + base + lane);
           if (rr >= 0 && rr < oob_row) {
             row = rr;
             ok = 1;
@@ -510,7 +525,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
       // the last arrival sees the pair complete (and acquires its partials)
-      if (arrive_acq_rel(&a.counters[sp.pair[0]]) + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
+      if ((arrive_acq_rel(&a.counters[sp.pair[0] * kPairWords]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0])
+        pair_done[0] = 1;
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -520,8 +536,11 @@ __global__ void __launch_bounds__(32 * 10, 1)
       const uint32_t rb = smem_u32(ring);
       const uint32_t qb = smem_u32(qs);
       bool q1_seen = false;
+      // tile i (its set is i & 1) lives in ring stage rs(i) with phase rp(i)
+      auto rs = [&](int t) { return t % NS; };
+      auto rp = [&](int t) { return (uint32_t)((t / NS) & 1); };
       auto issue_qk = [&](int i) {
-        const uint32_t kb = rb + (i % NS) * kStageBytes;
+        const uint32_t kb = rb + rs(i) * kStageBytes;
         const uint32_t d = tmem + col_s(i & 1);
         if (seg_of(i) == 0) {
 #pragma unroll
@@ -541,15 +560,15 @@ __global__ void __launch_bounds__(32 * 10, 1)
         tc::commit(smem_u32(&s_full[i & 1]));
       };
       bool ok = mbar_wait_abortable(smem_u32(q_ready), 0, abort_flag, a.status, 3u) &&
-                mbar_wait_abortable(smem_u32(&full[0]), 0, abort_flag, a.status, 4u);
+                mbar_wait_abortable(smem_u32(&full[rs(0)]), rp(0), abort_flag, a.status, 4u);
       tc::fence_after();
       if (ok) issue_qk(0);
       for (int i = 0; ok && i < ntot; ++i) {
         // S buffer of unit i+1's set is free: its previous reader (softmax of
         // unit i-1) arrived on p_ready before PV(i-1) was issued
         if (i + 1 < ntot) {
-          if (!mbar_wait_abortable(smem_u32(&full[(i + 1) % NS]), ((i + 1) / NS) & 1, abort_flag,
-                                   a.status, 5u)) {
+          if (!mbar_wait_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
+                                   5u)) {
             ok = false;
             break;
           }
@@ -571,7 +590,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         }
         tc::fence_after();
         const int first = seg_of(i) ? n0 : 0;  // the segment's first tile
-        const uint32_t vb = rb + (i % NS) * kStageBytes + kTileBytes;
+        const uint32_t vb = rb + rs(i) * kStageBytes + kTileBytes;
         const uint32_t pa = tmem + col_p(i & 1);
 #pragma unroll
         for (int kt = 0; kt < TBLK / 16; ++kt) {
@@ -581,7 +600,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
           const uint64_t bd = tc::smem_desc(vb + kt * 2048, kBoxBytes, 1024);
           tc::mma_ts(tmem + col_o(i & 1), pa + kt * 8, bd, idp, (i - first >= 2 || kt > 0) ? 1u : 0u);
         }
-        tc::commit(smem_u32(&empty[i % NS]));
+        tc::commit(smem_u32(&empty[rs(i)]));
         tc::commit(smem_u32(&o_done[i & 1]));
       }
       // tensor memory is released only after every issued MMA has finished
@@ -806,56 +825,135 @@ __global__ void __launch_bounds__(32 * 10, 1)
     // mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0) {
-      if (arrive_acq_rel(&a.counters[pair]) + 1u == (unsigned)sp.nseg[jf]) pair_done[jf] = 1;
+      if ((arrive_acq_rel(&a.counters[pair * kPairWords]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf])
+        pair_done[jf] = 1;
     }
   }
   __syncthreads();
 
-  // ------------------------------------------------- merge by the last arrival
-  // The CTA whose arrival completed a pair (the count reached the pair's
-  // segment count) merges every row of that pair; all other CTAs are done.
-  // No CTA ever waits for another, so nothing here depends on which CTAs
-  // are resident at the same time.
+  // ----------------------------------------------------------------- merge
   //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
   // summed in slot order whichever CTA merges, so results do not depend on
   // timing. The partials come into the idle ring by bulk copies (one per slot
-  // and row range). The merging CTA also returns the count word to zero for
-  // the next call: every arrival of this call is in by then.
+  // and row range) and are combined from shared memory. The count word of a
+  // pair holds its arrivals (low 16 bits) and the CTAs that finished their
+  // merge share (high bits).
   uint32_t mphase = 0;
-  for (int j = 0; j < sp.n; ++j) {
-    if (!pair_done[j]) continue;  // the same in every thread (set before a barrier)
-    const int pair = sp.pair[j];
-    const int ns = sp.nseg[j] + sp.mid[j];
+  // bulk-copy rows [r0, r0 + nr) of the ns partial slots of `pair` into the
+  // ring (nr even, so every (m, l) copy is a multiple of 16 bytes) and
+  // combine rows [r0, r0 + nv) into out
+  auto merge_rows = [&](int pair, int ns, int r0, int nr, int nv) {
     const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    // rows per pass: an even count (every (m, l) copy a multiple of 16
-    // bytes); with at most 64 slots two rows always fit
+    float* so = reinterpret_cast<float*>(ring);                           // [ns][nr][TD]
+    float2* sml = reinterpret_cast<float2*>(so + (size_t)ns * nr * TD);   // [ns][nr]
+    if (threadIdx.x == 0) {
+      // the partials were written by other CTAs through the generic proxy
+      // and acquired through the count word; order that before the copy
+      // engine reads them
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      fence_async_smem();
+      const uint32_t mb = smem_u32(merge_bar);
+      mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kMergeRowBytes));
+      for (int sl = 0; sl < ns; ++sl) {
+        const size_t row0 = pbase + (size_t)sl * a.rpad + r0;
+        bulk_load(smem_u32(so + (size_t)sl * nr * TD), a.part_o + row0 * TD, (uint32_t)(nr * TD * 4),
+                  mb);
+        bulk_load(smem_u32(sml + (size_t)sl * nr), a.part_ml + row0 * 2, (uint32_t)(nr * 8), mb);
+      }
+    }
+    if (!mbar_wait_drain(smem_u32(merge_bar), mphase) && threadIdx.x == 0)
+      atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+    mphase ^= 1u;
+    combine_rows(a, pair / a.Hkv, pair % a.Hkv, ns, nr, r0, nv, so, sml);
+    __syncthreads();  // the next copies overwrite the staging area
+  };
+  // Row slices of a pair, merged in parallel by the pair's CTAs: slice q
+  // (q < nsl = min(segments, 32)) covers rows [q * share, (q + 1) * share)
+  // and belongs to the CTA whose segment is the pair's q-th. A slice is
+  // merged by whoever claims its bit in the pair's claim word first. Each CTA
+  // waits (briefly, bounded) for the pair's last arrival and claims its own
+  // slice; the CTA whose arrival completed the pair merges its own slice and
+  // then claims, in one atomic, every slice still unclaimed: the slices of
+  // CTAs that are slow, gave up waiting or are not resident. So every slice
+  // is merged exactly once and no CTA depends on another to finish. The
+  // count word's high half counts CTAs done with the pair; the last of them
+  // returns the words to zero for the next call. With no wait
+  // (merge_wait_ns == 0) the last CTA merges every row alone.
+  for (int j = 0; j < sp.n; ++j) {
+    const int pair = sp.pair[j];
+    const int nseg = sp.nseg[j], ns = nseg + sp.mid[j];
+    const int nsl = nseg < 32 ? nseg : 32;
+    const int share = ((a.R + nsl - 1) / nsl + 1) & ~1;
+    // rows per pass that the ring holds for ns slots (even; two always fit)
     int rpp = (C::kRing / (ns * kMergeRowBytes)) & ~1;
     rpp = rpp < 2 ? 2 : (rpp > a.rpad ? a.rpad : rpp);
-    float* so = reinterpret_cast<float*>(ring);                           // [ns][rpp][TD]
-    float2* sml = reinterpret_cast<float2*>(so + (size_t)ns * rpp * TD);  // [ns][rpp]
-    for (int r0 = 0; r0 < a.R; r0 += rpp) {
-      const int nr = min(rpp, a.rpad - r0);  // rows copied (padding rows included)
-      if (threadIdx.x == 0) {
-        // the partials were written by other CTAs through the generic proxy
-        // and acquired by the arrival; order that before the copy engine reads
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        fence_async_smem();
-        const uint32_t mb = smem_u32(merge_bar);
-        mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kMergeRowBytes));
-        for (int sl = 0; sl < ns; ++sl) {
-          const size_t row0 = pbase + (size_t)sl * a.rpad + r0;
-          bulk_load(smem_u32(so + (size_t)sl * rpp * TD), a.part_o + row0 * TD,
-                    (uint32_t)(nr * TD * 4), mb);
-          bulk_load(smem_u32(sml + (size_t)sl * rpp), a.part_ml + row0 * 2, (uint32_t)(nr * 8), mb);
-        }
+    // rows [r0, r1) (r0 even) in passes of rpp rows
+    auto merge_range = [&](int r0, int r1) {
+      for (int q0 = r0; q0 < r1; q0 += rpp) {
+        const int nv = min(rpp, r1 - q0);
+        merge_rows(pair, ns, q0, min((nv + 1) & ~1, a.rpad - q0), nv);
       }
-      if (!mbar_wait_drain(smem_u32(merge_bar), mphase) && threadIdx.x == 0)
-        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      mphase ^= 1u;
-      combine_rows(a, pair / a.Hkv, pair % a.Hkv, ns, rpp, r0, min(rpp, a.R - r0), so, sml);
-      __syncthreads();  // the next pass's copies overwrite the staging area
+    };
+    const bool last = pair_done[j] != 0;  // the same in every thread
+    if (a.merge_wait_ns == 0) {
+      // the last CTA merges every row; the others have left the pair's
+      // words alone since their arrival, so it may zero them at once
+      if (last) {
+        merge_range(0, a.R);
+        if (threadIdx.x == 0) a.counters[pair * kPairWords] = 0u;
+      }
+      continue;
     }
-    if (threadIdx.x == 0) a.counters[pair] = 0u;
+    const int own = sp.slot[j] < nsl ? sp.slot[j] : -1;
+    if (threadIdx.x == 0) {
+      int got = 0;
+      if (own >= 0) {
+        bool complete = last;
+        if (!complete) {
+          // a short bounded wait: the pair's CTAs normally finish together
+          const uint64_t t0 = globaltimer_ns();
+          unsigned nap = 64;
+          while (!(complete = (load_acquire(&a.counters[pair * kPairWords]) & 0xFFFFu) >=
+                              (unsigned)nseg)) {
+            if (globaltimer_ns() - t0 > (uint64_t)a.merge_wait_ns) break;
+            __nanosleep(nap);
+            nap = nap < 512 ? 2 * nap : nap;
+          }
+        }
+        if (complete) got = !(atomicOr(a.claim + pair * kPairWords, 1u << own) & (1u << own));
+      }
+      *merge_got = got;
+    }
+    __syncthreads();
+    if (*merge_got) merge_range(min(a.R, own * share), min(a.R, (own + 1) * share));
+    if (last) {
+      if (threadIdx.x == 0) {
+        const unsigned all = nsl == 32 ? 0xFFFFFFFFu : ((1u << nsl) - 1u);
+        *merge_got = (int)(all & ~atomicOr(a.claim + pair * kPairWords, all));
+      }
+      __syncthreads();
+      // each run of consecutive claimed slices is one row range, copied in
+      // as few passes as the ring allows
+      const unsigned mine = (unsigned)*merge_got;
+      for (int q = 0; q < nsl;) {
+        if (!(mine & (1u << q))) {
+          ++q;
+          continue;
+        }
+        int e = q + 1;
+        while (e < nsl && (mine & (1u << e))) ++e;
+        merge_range(min(a.R, q * share), min(a.R, e * share));
+        q = e;
+      }
+    }
+    if (threadIdx.x == 0) {
+      if ((atomicAdd(&a.counters[pair * kPairWords], 1u << 16) >> 16) == (unsigned)nseg - 1u) {
+        // every CTA of the pair is done with its words
+        a.counters[pair * kPairWords] = 0u;
+        a.claim[pair * kPairWords] = 0u;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -926,8 +1024,13 @@ int attend_tc_ctas_per_sm(const AttendArgs& a) {
   return occupancy_tc_cfg<4>();
 }
 
-cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t st) {
+cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st) {
   const int nsw = (a.R + 31) / 32;
+  // When one CTA would copy little (few slots of few rows), the pair's last
+  // CTA merges it alone and the others leave at once, freeing their SMs for
+  // the next kernel; otherwise the pair's CTAs share the rows.
+  const size_t one_merger = (size_t)a.slot_stride * a.rpad * kMergeRowBytes;
+  a.merge_wait_ns = one_merger <= kSoloMergeBytes ? 0u : (unsigned)kMergeWaitNs;
   if (nsw <= 1) return launch_tc_cfg<1>(a, st);
   if (nsw <= 2) return launch_tc_cfg<2>(a, st);
   return launch_tc_cfg<4>(a, st);

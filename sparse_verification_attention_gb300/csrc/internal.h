@@ -43,11 +43,16 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Per-(b, h) words that CTAs poll or count on (arrival counts, claim words)
+// sit one per 128-byte line, so that polling one pair's word
+// does not queue behind every other pair's at the same L2 slice.
+constexpr int kPairWords = 32;  // stride of such arrays, in 32-bit words
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace carve-up (offsets in bytes from the workspace base).
 struct WsLayout {
-  size_t status, ctr_score, ctr_attend, scores, rows, part_o, part_ml, total;
+  size_t status, ctr_score, ctr_attend, claim, scores, rows, part_o, part_ml, total;
   int rpad, slots;
 };
 WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax);
@@ -145,6 +150,7 @@ struct AttendArgs {
   float* part_ml;       // [B,Hkv,S,Rpad,2]
   void* out;            // [B,T,Hq,d]
   unsigned* counters;   // [B*Hkv] segment arrivals (tcgen05 path), zero between calls
+  unsigned* claim;      // [B*Hkv] merge slices claimed (tcgen05 path), zero between calls
   unsigned* status;
   int B, T, Hq, Hkv, G, d, blk, R, rpad;
   int nb, nb_max, num_pages, n_sel, sel_stride;
@@ -166,6 +172,11 @@ struct AttendArgs {
   // Set only when this call's selection was not just written by the
   // preceding kernel; a stale guess only costs bandwidth, never results.
   int spec_prefetch;
+  // How long (ns) a CTA that finished its units waits for the rest of its
+  // pair so that the pair's CTAs share the merge in row slices; whatever is
+  // unclaimed when the wait ends is merged by the pair's last CTA to arrive.
+  // 0: the last CTA merges every row and nothing waits.
+  unsigned merge_wait_ns;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
   VarLen vl;  // per-sequence nb, tail and n_sel (on = 0: the uniform ones)
@@ -228,12 +239,12 @@ int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster);
 // splits write global partials for launch_merge.
 cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st);
 // tcgen05 path: bf16, d == 128, blk == 64, R <= 128, T <= 64.
-// Writes global split partials (stream-K runs, or the split map above); the
-// CTA whose arrival completes a (b, h) merges that pair's partials into out
-// (no separate merge launch, and no CTA waits for another).
+// Writes global split partials (stream-K runs, or the split map above) and
+// merges each (b, h)'s partials into out inside the same launch: the pair's
+// CTAs share the rows for a bounded wait, the last to arrive merges the rest.
 bool attend_tc_applies(const AttendArgs& a, int dtype);
 int attend_tc_ctas_per_sm(const AttendArgs& a);
-cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t st);
+cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st);
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
 // Log-sum-exp merge of the global split partials into out (any path; honours
 // the non-uniform split map).

@@ -69,6 +69,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // status[1]), so a CTA whose pipeline stalls gives up after one budget
 // instead of once per wait.
 constexpr uint64_t kWaitBudgetNs = 200ull * 1000 * 1000;
+// How long a CTA waits for the rest of a pair before it leaves its share of
+// the merge to the pair's last CTA (see attend_tc.cu).
+constexpr uint64_t kMergeWaitNs = 20ull * 1000;
 __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity,
                                                     volatile int* abort, unsigned* status,
                                                     unsigned site) {

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned ctas = (unsigned)((nbb + a.rows_per_cta - 1) / a.rows_per_cta);
-    const bool last = arrive_acq_rel(&a.counters[pair]) == ctas - 1;
+    const bool last = arrive_acq_rel(&a.counters[pair * kPairWords]) == ctas - 1;
     s_last = last;
   }
   __syncthreads();
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
                       a.num_pages, a.status};
     cta_topk_fit<kScoreThreads, kScoreKeys>(srow, nbb, n_of(a.vl, b, a.k), a.sel + (size_t)pair * a.kmax,
                                         a.kmax, tsm, tr);
-    if (threadIdx.x == 0) a.counters[pair] = 0;  // ready for the next call
+    if (threadIdx.x == 0) a.counters[pair * kPairWords] = 0;  // ready for the next call
   }
 }
 

@@ -250,9 +250,11 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   L.slots = units + 1 > kMaxSplits ? kMaxSplits : units + 1;
   const size_t pairs = (size_t)s.B * s.Hkv;
   L.status = 0;
+  const size_t words = align256(pairs * kPairWords * sizeof(uint32_t));  // one line per pair
   L.ctr_score = kStatusBytes;
-  L.ctr_attend = L.ctr_score + align256(pairs * sizeof(uint32_t));
-  L.scores = L.ctr_attend + align256(pairs * sizeof(uint32_t));
+  L.ctr_attend = L.ctr_score + words;
+  L.claim = L.ctr_attend + words;
+  L.scores = L.claim + words;
   L.rows = L.scores + align256(pairs * (size_t)(nb_max > 0 ? nb_max : 1) * sizeof(float));
   L.part_o = L.rows + align256(pairs * (size_t)(kmax > 0 ? kmax : 1) * sizeof(int32_t));
   L.part_ml = L.part_o + align256(pairs * L.slots * (size_t)L.rpad * s.d * sizeof(float));
@@ -477,6 +479,7 @@ static void fill_args(AttendArgs& a, const sv_shape* s, const void* q, const sv_
   a.part_ml = w ? reinterpret_cast<float*>(w + L.part_ml) : nullptr;
   a.status = w ? reinterpret_cast<unsigned*>(w + L.status) : nullptr;
   a.counters = w ? reinterpret_cast<unsigned*>(w + L.ctr_attend) : nullptr;
+  a.claim = w ? reinterpret_cast<unsigned*>(w + L.claim) : nullptr;
   a.B = s->B;
   a.T = s->T;
   a.Hq = s->Hq;
@@ -557,23 +560,48 @@ static sv_status do_score_select(const sv_shape* s, const void* q, const float* 
 // stand-in for the symbol: kernels get its device address, looked up below.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-static std::atomic<void*> g_noalloc_ptr[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up on the
-// first call made with that device current and cached.
+// Device address of the scratch on the current device, looked up with that
+// device current and cached per (device, context): a device reset or a
+// re-created primary context loads the module again, possibly elsewhere, so
+// a new context means a new lookup.
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ctx[kMaxDevices];
+static void* g_noalloc_ptr[kMaxDevices];
+
+static void* current_context() {
+  using GetCurrent = int (*)(void**);  // cuCtxGetCurrent(CUcontext*)
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrent>(p);
+  });
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
 static sv_status noalloc_scratch(void** ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return fail(SV_ERR_UNSUPPORTED, "device %d: at most %d devices", dev, kMaxDevices);
-  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
-  if (!p) {
+  void* ctx = current_context();
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!ctx || ctx != g_noalloc_ctx[dev] || !g_noalloc_ptr[dev]) {
+    void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (static scratch)");
-    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = current_context();  // the lookup may have made the context current
   }
-  *ptr = p;
+  *ptr = g_noalloc_ptr[dev];
   return SV_OK;
 }
 
@@ -589,7 +617,9 @@ static WsLayout noalloc_layout(const sv_shape& s, int rpad, int slot_stride) {
   L.status = 0;
   L.ctr_attend = kStatusBytes;
   L.ctr_score = L.ctr_attend;  // unused: this entry does not score
-  L.part_o = L.ctr_attend + align256(pairs * sizeof(uint32_t));
+  const size_t words = align256(pairs * kPairWords * sizeof(uint32_t));  // one line per pair
+  L.claim = L.ctr_attend + words;
+  L.part_o = L.claim + words;
   L.scores = L.part_o;  // unused
   L.rows = L.part_o;    // unused
   L.part_ml = L.part_o + align256(rows * s.d * sizeof(float));
@@ -662,6 +692,19 @@ size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax) {
 sv_status sv_clear_status(void* workspace, void* stream) {
   if (!workspace) return fail(SV_ERR_INVALID_ARG, "workspace is NULL");
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+sv_status sv_reset_workspace(const sv_shape* shape, int nb_max, int kmax, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if (nb_max < 0 || kmax < 0)
+    return fail(SV_ERR_INVALID_ARG, "nb_max=%d / kmax=%d is negative", nb_max, kmax);
+  WsLayout L;
+  if ((r = check_ws(shape, nb_max, kmax, workspace, ws_bytes, &L)) != SV_OK) return r;
+  // the status word and the per-(b, h) words lie in front of the scores
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.scores, (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "cudaMemsetAsync");
 }
 
@@ -935,6 +978,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   uint8_t* w = static_cast<uint8_t*>(base);
   a.status = reinterpret_cast<unsigned*>(w + L.status);
   a.counters = reinterpret_cast<unsigned*>(w + L.ctr_attend);
+  a.claim = reinterpret_cast<unsigned*>(w + L.claim);
   a.part_o = reinterpret_cast<float*>(w + L.part_o);
   a.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   a.n_splits = p.n_splits;

@@ -83,11 +83,13 @@ def test_budget_rejects_invalid(L):
 def test_workspace_sizes(L):
     s = api.make_shape(4, 32, 8, 128, 64, 8, torch.bfloat16)
     n = api.sv_workspace_bytes(s, 2048, 128)
-    # status + two per-(b,h) counter arrays + scores + the kept blocks' pool
-    # rows (kmax per pair) + split partials o and (m, l); 130 work units (128
-    # blocks, a partial block, the draft tile) capped at 64 slots
+    # status + three arrays of per-(b,h) words, one 128-byte line per pair
+    # (score and attend counts, a merge claim word) + the scores + the
+    # kept blocks' pool rows (kmax per pair) + split partials o and (m, l);
+    # 130 work units (128 blocks, a partial block, the draft tile) capped at
+    # 64 slots
     pairs = 4 * 8
-    ctrs = 2 * 256
+    ctrs = 3 * pairs * 128
     scores = pairs * 2048 * 4
     rows = pairs * 128 * 4
     part = pairs * 64 * 32 * 128 * 4

@@ -709,6 +709,30 @@ def test_draft_selection_overlap_vs_oracle():
     assert (got - want).abs().mean().item() < 0.02
 
 
+def test_reset_workspace_repairs_stale_words():
+    """A call that gave up on a wait may leave a pair's count or claim words
+    non-zero. sv_reset_workspace zeroes the status word and every
+    per-(b, h) word, after which the same workspace gives the same result
+    again (the garbage is written by the test, on the host's orders; no wait
+    is made to run out)."""
+    wl = small_wl(B=4, Hq=32, Hkv=8, ctx=64 * 60, budget=W.Budget(W.BUDGET_FIXED, 20, 0, 0, 0, 0, 0))
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    clean = st.verify().clone()
+    torch.cuda.synchronize()
+    pairs = wl.B * wl.Hkv
+    header = 256 + 3 * pairs * 128  # status, then three arrays of one 128-byte line per pair
+    st.ws[:header].fill_(0x5A)
+    nb_max = st.x.block_table.shape[1]
+    api.sv_reset_workspace(st.shape, nb_max, max(st.kmax, wl.NB, 1), st.ws)
+    assert int(st.ws[:header].count_nonzero()) == 0
+    again = st.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    assert torch.equal(again, clean)
+
+
 def test_reuse_guard_on_device():
     """A reuse layer may read a slot only after a computing layer wrote it for
     the same context and budget: the matching reuse attends over it, while a
