@@ -304,6 +304,35 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           int* k_out, void* out, void* workspace, size_t ws_bytes,
                           void* stream);
 
+/* sv_verify_layer with the step's per-token tensors in HOST memory: the
+ * call a serving loop makes once the KV pool, representatives and slot live
+ * on the device. On `stream` it enqueues, in order: the copies of q_host
+ * [B, T, Hq, d], draft_k_host and draft_v_host [B, T, Hkv, d] into the
+ * caller's device buffers q_dev, draft_k_dev, draft_v_dev (same shapes); the
+ * verification exactly as sv_verify_layer (reuse, slot, k_out, workspace
+ * alike); and the copy of the result out_dev [B, T, Hq, d] into out_host.
+ * Element type: the shape's dtype. All of it is asynchronous: the host
+ * buffers must stay valid, and unchanged, until the stream reaches the copies
+ * (page-locked host memory makes the copies truly asynchronous). When
+ * copy_in_stream / copy_out_stream are not NULL the input copies go on
+ * copy_in_stream and the output copy on copy_out_stream, ordered against
+ * `stream` by events the library records (one pool of events per device,
+ * created on first use), so that the next call's inputs and this call's
+ * output move while other work computes; the caller then must not reuse
+ * the device buffers of a call before its output copy has completed
+ * (rotating sets of buffers, as a serving loop double-buffers, is enough).
+ * Validation is the same as sv_verify_layer's, done before anything is
+ * enqueued; q_host, draft_k_host, draft_v_host and out_host must not be
+ * NULL. */
+sv_status sv_verify_layer_host(const sv_shape* shape, const void* q_host, void* q_dev,
+                               const sv_kv* kv, const float* reps, const sv_budget* budget,
+                               const void* draft_k_host, const void* draft_v_host,
+                               void* draft_k_dev, void* draft_v_dev,
+                               const int32_t* draft_parent, int reuse, sv_sel_slot* slot,
+                               int* k_out, void* out_host, void* out_dev, void* workspace,
+                               size_t ws_bytes, void* stream, void* copy_in_stream,
+                               void* copy_out_stream);
+
 /* Acceptance write-back: the step after verification. The pages have no
  * formula for it; it closes the loop that [SV-Fig1] verifies one step of:
  * the accepted drafts become context for the next step. Sequence b (ctx_b =

@@ -31,7 +31,7 @@ EXPORTED = ("sv_abi_version", "sv_last_error", "sv_budget_blocks", "sv_workspace
             "sv_clear_status", "sv_read_status", "sv_build_reps", "sv_score_blocks",
             "sv_select_blocks", "sv_score_select", "sv_sparse_attend", "sv_attend_plan",
             "sv_verify_layer", "sv_sparse_attend_noalloc", "sv_append_kv",
-            "sv_selection_overlap", "sv_reset_workspace")
+            "sv_selection_overlap", "sv_reset_workspace", "sv_verify_layer_host")
 
 
 class SvError(RuntimeError):
@@ -124,6 +124,10 @@ def lib() -> C.CDLL:
                                  vp]),
             "sv_selection_overlap": (i, [vp, i, i, i, i, C.POINTER(C.c_int32), vp, vp, vp]),
             "sv_reset_workspace": (i, [C.POINTER(Shape), i, i, vp, sz, vp]),
+            "sv_verify_layer_host": (i, [C.POINTER(Shape), vp, vp, C.POINTER(KV), vp,
+                                         C.POINTER(BudgetC), vp, vp, vp, vp,
+                                         C.POINTER(C.c_int32), i, C.POINTER(SelSlotC),
+                                         C.POINTER(C.c_int), vp, vp, vp, sz, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -186,10 +190,18 @@ def make_kv(k_pool: torch.Tensor, v_pool: Optional[torch.Tensor], block_table: t
     return kv
 
 
+_parents_cache: dict = {}
+
+
 def _parents(parents: Optional[Sequence[int]]):
     if parents is None:
         return None
-    arr = (C.c_int32 * len(parents))(*parents)
+    key = tuple(parents)
+    arr = _parents_cache.get(key)
+    if arr is None:  # the C array is only read during the call
+        arr = (C.c_int32 * len(key))(*key)
+        if len(_parents_cache) < 64:
+            _parents_cache[key] = arr
     return arr
 
 
@@ -312,6 +324,25 @@ def sv_verify_layer(shape: Shape, q, kv: KV, reps, budget: Optional[W.Budget], d
                                  _ptr(draft_k), _ptr(draft_v), _parents(parents), int(reuse),
                                  None if slot is None else C.byref(slot.c), C.byref(k), _ptr(out),
                                  _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return k.value
+
+
+def sv_verify_layer_host(shape: Shape, q_host, q, kv: KV, reps, budget: Optional[W.Budget],
+                         dk_host, dv_host, draft_k, draft_v, parents, reuse: int,
+                         slot: Optional[SelSlot], out_host, out, ws, stream=None,
+                         copy_in_stream=None, copy_out_stream=None) -> int:
+    """sv_verify_layer with q, draft K/V and the output in host memory
+    (pinned tensors for asynchronous copies); q, draft_k, draft_v and out are
+    the device buffers the call stages them through."""
+    b = None if budget is None else C.byref(make_budget(budget))
+    k = C.c_int(-1)
+    ci = None if copy_in_stream is None else _stream(copy_in_stream)
+    co = None if copy_out_stream is None else _stream(copy_out_stream)
+    _check(lib().sv_verify_layer_host(
+        C.byref(shape), _ptr(q_host), _ptr(q), C.byref(kv), _ptr(reps), b, _ptr(dk_host),
+        _ptr(dv_host), _ptr(draft_k), _ptr(draft_v), _parents(parents), int(reuse),
+        None if slot is None else C.byref(slot.c), C.byref(k), _ptr(out_host), _ptr(out), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream), ci, co))
     return k.value
 
 

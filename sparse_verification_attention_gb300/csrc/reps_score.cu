@@ -161,6 +161,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
     return;
   }
 
+  if (a.sel && a.block_table) {
+    // warm L2 with the block-table entries of these rows: the selecting CTA
+    // reads the kept blocks' pages from there
+    const int32_t* bt = a.block_table + (size_t)b * a.nb_max;
+    for (int e = r0 + 32 * threadIdx.x; e < r1; e += 32 * kScoreThreads) prefetch_l2(bt + e);
+  }
   float4 qh[CH];
   bool have_q = false;
   for (int base = r0 + warp * R; base < r1; base += kScoreWarps * R) {

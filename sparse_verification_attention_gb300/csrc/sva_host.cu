@@ -231,6 +231,47 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+// Encoded tensor maps, kept by what the encoding depends on (which map,
+// base address, sizes): a map describes only an address range and its
+// layout, so it stays valid for any later call on the same tensor, and the
+// driver call that encodes it is skipped. A small set, replaced round-robin.
+struct MapKey {
+  int kind;
+  const void* base;
+  int v[6];
+  bool operator==(const MapKey& o) const {
+    if (kind != o.kind || base != o.base) return false;
+    for (int i = 0; i < 6; ++i)
+      if (v[i] != o.v[i]) return false;
+    return true;
+  }
+};
+
+template <typename Encode>
+bool cached_map(const MapKey& key, CUtensorMap* map, Encode&& encode) {
+  constexpr int kSlots = 64;
+  static MapKey keys[kSlots];
+  static CUtensorMap maps[kSlots];
+  static bool used[kSlots];
+  static int next = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < kSlots; ++i)
+      if (used[i] && keys[i] == key) {
+        *map = maps[i];
+        return true;
+      }
+  }
+  if (!encode(map)) return false;
+  std::lock_guard<std::mutex> g(mu);
+  keys[next] = key;
+  maps[next] = *map;
+  used[next] = true;
+  next = (next + 1) % kSlots;
+  return true;
+}
+
 }  // namespace
 
 int current_device() {
@@ -262,8 +303,36 @@ WsLayout ws_layout(const sv_shape& s, int nb_max, int kmax) {
   return L;
 }
 
+static bool encode_pool_map_now(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
+                                int blk, int d, const char** why);
+static bool encode_draft_map_now(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d,
+                                 int rows, const char** why);
+static bool encode_q_map_now(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
+                             const char** why);
+
 bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv, int blk, int d,
                      const char** why) {
+  return cached_map(MapKey{0, pool, {num_pages, Hkv, blk, d, 0, 0}}, map, [&](CUtensorMap* m) {
+    return encode_pool_map_now(m, pool, num_pages, Hkv, blk, d, why);
+  });
+}
+
+bool encode_draft_map(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d, int rows,
+                      const char** why) {
+  return cached_map(MapKey{1, dkv, {B, T, Hkv, d, rows, 0}}, map, [&](CUtensorMap* m) {
+    return encode_draft_map_now(m, dkv, B, T, Hkv, d, rows, why);
+  });
+}
+
+bool encode_q_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
+                  const char** why) {
+  return cached_map(MapKey{2, q, {B, T, Hq, G, d, 0}}, map, [&](CUtensorMap* m) {
+    return encode_q_map_now(m, q, B, T, Hq, G, d, why);
+  });
+}
+
+static bool encode_pool_map_now(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
+                                int blk, int d, const char** why) {
   auto enc = get_encode();
   if (!enc) {
     *why = "cuTensorMapEncodeTiled unavailable";
@@ -283,8 +352,8 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int Hkv,
   return true;
 }
 
-bool encode_draft_map(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d, int rows,
-                      const char** why) {
+static bool encode_draft_map_now(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, int d,
+                                 int rows, const char** why) {
   auto enc = get_encode();
   if (!enc) {
     *why = "cuTensorMapEncodeTiled unavailable";
@@ -307,8 +376,8 @@ bool encode_draft_map(CUtensorMap* map, const void* dkv, int B, int T, int Hkv, 
   return true;
 }
 
-bool encode_q_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
-                  const char** why) {
+static bool encode_q_map_now(CUtensorMap* map, const void* q, int B, int T, int Hq, int G, int d,
+                             const char** why) {
   auto enc = get_encode();
   if (!enc) {
     *why = "cuTensorMapEncodeTiled unavailable";
@@ -872,10 +941,76 @@ sv_status sv_attend_plan(const sv_shape* shape, const sv_kv* kv, int n_sel, sv_p
   return SV_OK;
 }
 
-sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,
-                          const sv_budget* budget, const void* draft_k, const void* draft_v,
-                          const int32_t* draft_parent, int reuse, sv_sel_slot* slot, int* k_out,
-                          void* out, void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+// The host side of sv_verify_layer_host: per-token inputs copied in before
+// the first launch, the output copied back after the last.
+struct HostIO {
+  const void *q, *dk, *dv;
+  void* out;
+  size_t q_bytes, dkv_bytes;
+  cudaStream_t in_st, out_st;  // null: the compute stream
+};
+
+// Events that order copy streams against the compute stream: a pool per
+// device, created on first use and reused round-robin (an event may be
+// recorded again once the waits on its earlier record have been enqueued,
+// which happens within the same call).
+cudaError_t pool_event(cudaEvent_t* ev) {
+  constexpr int kEvents = 64;
+  static cudaEvent_t pool[kMaxDevices][kEvents];
+  static std::once_flag once[kMaxDevices];
+  static std::atomic<unsigned> next[kMaxDevices];
+  static cudaError_t made[kMaxDevices];
+  const int dev = current_device();
+  std::call_once(once[dev], [dev] {
+    made[dev] = cudaSuccess;
+    for (int i = 0; i < kEvents && made[dev] == cudaSuccess; ++i)
+      made[dev] = cudaEventCreateWithFlags(&pool[dev][i], cudaEventDisableTiming);
+  });
+  if (made[dev] != cudaSuccess) return made[dev];
+  *ev = pool[dev][next[dev].fetch_add(1) % kEvents];
+  return cudaSuccess;
+}
+
+// Make `waiter` wait for the work enqueued so far on `producer`.
+cudaError_t stream_after(cudaStream_t waiter, cudaStream_t producer) {
+  cudaEvent_t ev;
+  cudaError_t e = pool_event(&ev);
+  if (e == cudaSuccess) e = cudaEventRecord(ev, producer);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
+  return e;
+}
+
+sv_status stage_in(const HostIO* io, const void* q, const void* dk, const void* dv,
+                   cudaStream_t st) {
+  if (!io) return SV_OK;
+  const cudaStream_t cs = io->in_st ? io->in_st : st;
+  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(q), io->q, io->q_bytes,
+                                  cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<void*>(dk), io->dk, io->dkv_bytes, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<void*>(dv), io->dv, io->dkv_bytes, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess && io->in_st) e = stream_after(st, io->in_st);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "input copy");
+}
+
+sv_status stage_out(const HostIO* io, const void* out, cudaStream_t st) {
+  if (!io) return SV_OK;
+  cudaError_t e = cudaSuccess;
+  if (io->out_st) e = stream_after(io->out_st, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(io->out, out, io->q_bytes, cudaMemcpyDeviceToHost,
+                        io->out_st ? io->out_st : st);
+  return e == cudaSuccess ? SV_OK : cuda_fail(e, "output copy");
+}
+
+sv_status verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,
+                       const sv_budget* budget, const void* draft_k, const void* draft_v,
+                       const int32_t* draft_parent, int reuse, sv_sel_slot* slot, int* k_out,
+                       void* out, void* workspace, size_t ws_bytes, void* stream,
+                       const HostIO* io) {
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
@@ -901,8 +1036,11 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                         ? std::max(kmax, nb) : kmax;
     if ((r = check_ws(shape, kv->nb_max, kws, workspace, ws_bytes, &L)) != SV_OK) return r;
     if (k_out) *k_out = nb;
-    return run_attend(shape, q, kv, nullptr, nb, nb, draft_k, draft_v, draft_parent, out,
-                      workspace, L, (cudaStream_t)stream);
+    const cudaStream_t st = (cudaStream_t)stream;
+    if ((r = stage_in(io, q, draft_k, draft_v, st)) != SV_OK) return r;
+    r = run_attend(shape, q, kv, nullptr, nb, nb, draft_k, draft_v, draft_parent, out, workspace,
+                   L, st);
+    return r == SV_OK ? stage_out(io, out, st) : r;
   }
   int k_b[kMaxVarB];
   const int k = budgets_of(budget, kv, c, shape->B, k_b);
@@ -924,6 +1062,7 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                 slot->stamp ? "reuse of a selection computed for another shape, context or budget"
                             : "reuse of a selection slot that no computing call has written");
   cudaStream_t st = (cudaStream_t)stream;
+  if ((r = stage_in(io, q, draft_k, draft_v, st)) != SV_OK) return r;
   int32_t* rows = nullptr;
   if (!reuse && kmax > 0) {
     rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.rows);
@@ -934,7 +1073,38 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
   r = run_attend(shape, q, kv, sel_cache, k, kmax, draft_k, draft_v, draft_parent, out, workspace,
                  L, st, c.var ? k_b : nullptr, rows);
   if (r == SV_OK && reuse == 0) slot->stamp = stamp;
-  return r;
+  return r == SV_OK ? stage_out(io, out, st) : r;
+}
+
+}  // namespace
+
+sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv, const float* reps,
+                          const sv_budget* budget, const void* draft_k, const void* draft_v,
+                          const int32_t* draft_parent, int reuse, sv_sel_slot* slot, int* k_out,
+                          void* out, void* workspace, size_t ws_bytes, void* stream) {
+  return verify_layer(shape, q, kv, reps, budget, draft_k, draft_v, draft_parent, reuse, slot,
+                      k_out, out, workspace, ws_bytes, stream, nullptr);
+}
+
+sv_status sv_verify_layer_host(const sv_shape* shape, const void* q_host, void* q_dev,
+                               const sv_kv* kv, const float* reps, const sv_budget* budget,
+                               const void* draft_k_host, const void* draft_v_host,
+                               void* draft_k_dev, void* draft_v_dev,
+                               const int32_t* draft_parent, int reuse, sv_sel_slot* slot,
+                               int* k_out, void* out_host, void* out_dev, void* workspace,
+                               size_t ws_bytes, void* stream, void* copy_in_stream,
+                               void* copy_out_stream) {
+  sv_status r = check_shape(shape);
+  if (r != SV_OK) return r;
+  if (!q_host || !draft_k_host || !draft_v_host || !out_host)
+    return fail(SV_ERR_INVALID_ARG, "q_host/draft_k_host/draft_v_host/out_host is NULL");
+  const size_t es = shape->dtype == SV_BF16 ? 2 : 4;
+  const size_t rows = (size_t)shape->B * shape->T;
+  const HostIO io{q_host, draft_k_host, draft_v_host, out_host,
+                  rows * shape->Hq * shape->d * es, rows * shape->Hkv * shape->d * es,
+                  (cudaStream_t)copy_in_stream, (cudaStream_t)copy_out_stream};
+  return verify_layer(shape, q_dev, kv, reps, budget, draft_k_dev, draft_v_dev, draft_parent,
+                      reuse, slot, k_out, out_dev, workspace, ws_bytes, stream, &io);
 }
 
 sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const sv_kv* kv,

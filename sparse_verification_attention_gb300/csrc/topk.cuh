@@ -16,18 +16,25 @@
 // every per-key loop unrolls without branches and the independent loads and
 // latency chains of a thread's keys overlap.
 //
-// Bucketed path (tried first). The scores are binned linearly over
-// [min, max] into kTopkBins bins. The binning is monotone: a higher bin only
-// holds strictly larger scores. One shared histogram and a suffix scan give
-// the bin b* holding the k-th largest score. Every key above b* is kept, and
-// every key below it is dropped. Order keys by the composite
-// (key << 32 | ~index): a larger score first, then the lower index. The keys
-// of b* (at most kTopkMaxCand) are ranked against each other by that
-// composite. The one of rank k - (keys above b*) - 1 is the threshold T, and
-// a key is kept if and only if its composite is >= T. Keys above b* pass and
-// keys below it fail automatically. A boundary bin with more keys, equal
-// scores everywhere, or non-finite extremes fall back to the radix search
-// below.
+// Bucketed path (tried first). The keys are binned by their offset from
+// the smallest key, (key - min key) >> shift, with shift the smallest that
+// leaves at most kTopkBins bins. Order keys follow the float bit patterns, so
+// the bins are about logarithmic in the score: a few far-out scores (an
+// attention sink, strongly planted blocks) do not squeeze the bulk of the
+// scores into a handful of bins, as bins linear in the score would. The
+// binning is monotone: a higher bin only holds strictly larger keys. One
+// shared histogram and a suffix scan give the bin b* holding the k-th
+// largest key. Every key above b* is kept, and every key below it is
+// dropped. Order keys by the composite (key << 32 | ~index): a larger score
+// first, then the lower index. The keys of b* (at most kTopkMaxCand) are
+// ranked against each other by that composite. The one of rank
+// k - (keys above b*) - 1 is the threshold T, and a key is kept if and only
+// if its composite is >= T. Keys above b* pass and keys below it fail
+// automatically. A boundary bin with more than kTopkRankCand keys is
+// refined first: its key range becomes the next histogram's range (bins
+// 2^10 times narrower), and so on down to single keys. A boundary bin that
+// still holds more than kTopkMaxCand keys (many equal scores), or equal keys
+// everywhere, falls back to the radix search below.
 //
 // Radix search. The k-th largest key is found two bits
 // per pass from the most significant end: each warp counts its keys at or
@@ -61,14 +68,19 @@ constexpr int kTopkRadixBits = 2;
 constexpr int kTopkCands = (1 << kTopkRadixBits) - 1;  // candidates per pass
 constexpr int kTopkBins = 1024;                        // bucketed path: histogram bins
 constexpr int kTopkMaxCand = 256;                      // largest boundary bin it ranks
+constexpr int kTopkRankCand = 48;                      // larger boundary bins are refined
+constexpr int kTopkBinBits = 10;                       // kTopkBins = 2^kTopkBinBits
 
-// Bin of a key for scores in [lo, lo + kTopkBins / scale]: monotone in the
-// key (rounded subtraction and multiplication are monotone, truncation of a
-// non-negative value is a floor), and the same instructions wherever used.
-__device__ __forceinline__ int key_bin(uint32_t key, float lo, float scale) {
-  const float x = __fmul_rn(__fsub_rn(key_value(key), lo), scale);  // >= 0
-  const int i = __float2int_rz(x);  // NaN gives 0; the clamps keep any value in range
-  return i <= 0 ? 0 : (i < kTopkBins - 1 ? i : kTopkBins - 1);
+// Bin of a key k >= kmin: (k - kmin) >> shift, monotone in the key.
+__device__ __forceinline__ int key_bin(uint32_t key, uint32_t kmin, int shift) {
+  return (int)((key - kmin) >> shift);
+}
+
+// Smallest shift that maps [0, span] into kTopkBins bins.
+__device__ __forceinline__ int key_bin_shift(uint32_t span) {
+  static_assert((1 << kTopkBinBits) == kTopkBins, "bin count is a power of two");
+  const int bits = 32 - __clz(span);  // significant bits of span (0 for span 0)
+  return bits > kTopkBinBits ? bits - kTopkBinBits : 0;
 }
 
 template <int NT, int KPT>
@@ -76,11 +88,11 @@ struct TopkSmem {
   uint32_t cnt[2][kTopkCands][NT / 32];  // per-pass per-candidate per-warp counts
   uint32_t above[NT / 32], ties[NT / 32], kept[NT / 32];
   uint32_t wmin[NT / 32], wmax[NT / 32], wsum[NT / 32];
-  uint32_t hist[kTopkBins];
+  uint32_t hist[2][kTopkBins];  // two levels in flight: one filled, one zeroed
   unsigned long long cand[kTopkMaxCand];  // composites of the boundary bin's keys
   unsigned long long thr;                 // the threshold composite T
   int bstar;
-  uint32_t bstar_above, ncand;
+  uint32_t bstar_above, bstar_cnt, ncand;
 };
 
 // Optional second output of a selection: the pool row of every kept block,
@@ -148,7 +160,11 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
     const int j = wbase + 32 * e + lane;
     const bool ok = j < nb;
     rk[e] = ok ? order_key(__ldcg(sc + j)) : 0u;
-    if constexpr (kPagesInRegs) pg[e] = (ok && tr.bt) ? tr.bt[j] : -1;
+    if constexpr (kPagesInRegs) {
+      // issued here, beside the scores, and not where the pages are used
+      pg[e] = -1;
+      if (ok && tr.bt) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(pg[e]) : "l"(tr.bt + j));
+    }
     valid |= (Mask)(ok ? 1u : 0u) << e;
   }
 
@@ -172,11 +188,12 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
       sm.wmin[warp] = lmin;
       sm.wmax[warp] = lmax;
     }
-    for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0u;
+    for (int i = tid; i < kTopkBins; i += NT) sm.hist[0][i] = 0u;
     if (tid == 0) {
       sm.ncand = 0u;
-      sm.bstar = 0;  // overwritten below; a valid index whatever happens
+      sm.bstar = 0;  // overwritten below; valid values whatever happens
       sm.bstar_above = 0u;
+      sm.bstar_cnt = 0xffffffffu;
     }
     __syncthreads();
     uint32_t kmn = 0xffffffffu, kmx = 0u;
@@ -185,57 +202,87 @@ __device__ void cta_topk(const float* sc, int nb, int k_req, int32_t* out, int k
       kmn = min(kmn, sm.wmin[w]);
       kmx = max(kmx, sm.wmax[w]);
     }
-    const float lo = key_value(kmn);
-    const float range = __fsub_rn(key_value(kmx), lo);
-    const float scale = (float)kTopkBins / range;
-    // the same decision in every thread: a finite, non-zero spread
-    if (range > 0.f && scale > 0.f && scale <= 3.0e38f) {
-#pragma unroll
-      for (int e = 0; e < KPT; ++e) {
-        if ((valid >> e) & 1u) atomicAdd(&sm.hist[key_bin(rk[e], lo, scale)], 1u);
-      }
-      __syncthreads();
-      // suffix counts: thread t scans bins kTopkBins-1-BPT*t-j (j < BPT), so
-      // thread order runs from the highest bin down
-      uint32_t hb[BPT], s = 0;
-#pragma unroll
-      for (int j = 0; j < BPT; ++j) {
-        hb[j] = sm.hist[kTopkBins - 1 - BPT * tid - j];
-        s += hb[j];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (lane == 31) sm.wsum[warp] = incl;
-      __syncthreads();
-#pragma unroll
-      for (int w = 0; w < NW; ++w) incl += (w < warp) ? sm.wsum[w] : 0u;
-      uint32_t cum = incl - s;  // keys in bins above this thread's
-      if (cum < (uint32_t)k && (uint32_t)k <= incl) {  // exactly one thread
-#pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-          if (cum + hb[j] >= (uint32_t)k) {
-            sm.bstar = kTopkBins - 1 - BPT * tid - j;
-            sm.bstar_above = cum;
-            break;
-          }
-          cum += hb[j];
-        }
-      }
-      __syncthreads();
-      const int bstar = sm.bstar;
-      const uint32_t above = sm.bstar_above;
-      if (sm.hist[bstar] <= (uint32_t)kTopkMaxCand) {  // same value in every thread
-        // the keys of the boundary bin, in any order
+    // the same decision in every thread: keys that are not all equal
+    if (kmx > kmn) {
+      // window of keys [lo, lo + (kTopkBins << shift)); `above` keys lie
+      // above it; the k-th largest key is inside it
+      uint32_t lo = kmn, above = 0u, cnt = 0u;
+      int shift = key_bin_shift(kmx - kmn), bstar = 0;
+      for (int level = 0;; ++level) {
+        uint32_t* hist = sm.hist[level & 1];
 #pragma unroll
         for (int e = 0; e < KPT; ++e) {
-          if (((valid >> e) & 1u) && key_bin(rk[e], lo, scale) == bstar) {
-            const uint32_t slot = atomicAdd(&sm.ncand, 1u);
-            if (slot < (uint32_t)kTopkMaxCand)
+          if (((valid >> e) & 1u) && rk[e] >= lo) {
+            const uint32_t bin = (rk[e] - lo) >> shift;
+            if (bin < (uint32_t)kTopkBins) atomicAdd(&hist[bin], 1u);
+          }
+        }
+        // the other histogram is free (its last reader passed the barrier
+        // that published the previous level's boundary bin)
+        for (int i = tid; i < kTopkBins; i += NT) sm.hist[(level + 1) & 1][i] = 0u;
+        __syncthreads();
+        // suffix counts: thread t scans bins kTopkBins-1-BPT*t-j (j < BPT), so
+        // thread order runs from the highest bin down
+        uint32_t hb[BPT], s = 0;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+          hb[j] = hist[kTopkBins - 1 - BPT * tid - j];
+          s += hb[j];
+        }
+        uint32_t incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (lane == 31) sm.wsum[warp] = incl;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) incl += (w < warp) ? sm.wsum[w] : 0u;
+        uint32_t cum = incl - s;  // window keys in bins above this thread's
+        const uint32_t need = (uint32_t)k - above;  // >= 1, <= the window's keys
+        if (cum < need && need <= incl) {  // exactly one thread
+#pragma unroll
+          for (int j = 0; j < BPT; ++j) {
+            if (cum + hb[j] >= need) {
+              sm.bstar = kTopkBins - 1 - BPT * tid - j;
+              sm.bstar_above = above + cum;
+              sm.bstar_cnt = hb[j];
+              break;
+            }
+            cum += hb[j];
+          }
+        }
+        __syncthreads();
+        bstar = sm.bstar;
+        above = sm.bstar_above;
+        cnt = sm.bstar_cnt;
+        // refine while the boundary bin is too full to rank cheaply
+        if (cnt <= (uint32_t)kTopkRankCand || shift == 0) break;
+        lo += (uint32_t)bstar << shift;
+        shift = shift > kTopkBinBits ? shift - kTopkBinBits : 0;
+      }
+      if (cnt <= (uint32_t)kTopkMaxCand) {  // same value in every thread
+        // the keys of the boundary bin, in any order: one shared-memory
+        // atomic per warp reserves all of the warp's places
+        unsigned bal[KPT];
+        uint32_t nw = 0;
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          bal[e] = __ballot_sync(0xffffffffu, ((valid >> e) & 1u) && rk[e] >= lo &&
+                                                  ((rk[e] - lo) >> shift) == (uint32_t)bstar);
+          nw += (uint32_t)__popc(bal[e]);
+        }
+        if (nw) {
+          uint32_t base = 0;
+          if (lane == 0) base = atomicAdd(&sm.ncand, nw);
+          base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+          for (int e = 0; e < KPT; ++e) {
+            const uint32_t slot = base + __popc(bal[e] & lt);
+            if (((bal[e] >> lane) & 1u) && slot < (uint32_t)kTopkMaxCand)
               sm.cand[slot] = topk_composite(rk[e], wbase + 32 * e + lane);
+            base += (uint32_t)__popc(bal[e]);
           }
         }
         __syncthreads();

@@ -210,6 +210,30 @@ def test_reuse_of_unwritten_or_stale_slot_is_refused(L):
     assert st == api.SV_ERR_INVALID_ARG and "slot" in msg
 
 
+def test_verify_layer_host_validates_before_copying(L):
+    """The host-buffer entry refuses NULL host buffers, and any argument
+    sv_verify_layer refuses, before it enqueues a copy (no GPU is touched)."""
+    s = api.make_shape(1, 4, 2, 64, 16, 4, torch.float32)
+    fake = 1 << 20
+    kv = api.KV(fake, fake, fake, 64, 64, 1024)
+    b = api.make_budget(W.Budget(W.BUDGET_FIXED, 8, 0, 0, 0, 0, 0))
+    ws_n = api.sv_workspace_bytes(s, 64, 8)
+    slot = api.SelSlotC(fake, 8, 0)
+    f = L.sv_verify_layer_host
+    for hosts in ((None, fake, fake, fake), (fake, None, fake, fake), (fake, fake, None, fake),
+                  (fake, fake, fake, None)):
+        hq, hk, hv, ho = hosts
+        st, msg = _status(L, f, C.byref(s), hq, fake, C.byref(kv), fake, C.byref(b), hk, hv, fake,
+                          fake, None, 0, C.byref(slot), None, ho, fake, fake, ws_n, None, None,
+                          None)
+        assert st == api.SV_ERR_INVALID_ARG and "host" in msg, msg
+    # a reuse of a slot no computing call wrote: refused like sv_verify_layer
+    st, msg = _status(L, f, C.byref(s), fake, fake, C.byref(kv), None, C.byref(b), fake, fake,
+                      fake, fake, None, 1, C.byref(slot), None, fake, fake, fake, ws_n, None, None,
+                      None)
+    assert st == api.SV_ERR_INVALID_ARG and "no computing call" in msg, msg
+
+
 def test_per_sequence_context_validation(L):
     """seq_ctx is checked on the host: negative lengths, a block table too
     narrow for the longest sequence and more than 64 sequences are refused

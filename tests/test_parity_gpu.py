@@ -757,6 +757,41 @@ def test_reuse_guard_on_device():
     assert e.value.status == api.SV_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("streams", [False, True], ids=["one_stream", "copy_streams"])
+def test_verify_layer_host_buffers(streams):
+    """sv_verify_layer_host takes the step's q and draft K/V from pinned host
+    memory and returns the output there: it must give, bit for bit, what
+    sv_verify_layer gives on device buffers, for a computing layer and for a
+    reuse layer after it, on one stream and with separate copy streams."""
+    wl = small_wl(B=2, Hq=32, Hkv=8, ctx=64 * 50 + 9)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    ref0 = api.LayerState(wl, xd)
+    out0 = ref0.verify().clone()
+    ref1 = api.LayerState(wl, xd, build_reps=False)
+    out1 = ref1.verify(reuse=api.VERIFY_REUSE, sel_from=ref0).clone()
+    torch.cuda.synchronize()
+    hq, hk, hv = (t.contiguous().pin_memory() for t in (x.q, x.draft_k, x.draft_v))
+    ci, co = (torch.cuda.Stream(), torch.cuda.Stream()) if streams else (None, None)
+    st0 = api.LayerState(wl, xd)
+    st1 = api.LayerState(wl, xd, build_reps=False)
+    st1.slot = st0.slot
+    outs = []
+    for st, reuse in ((st0, api.VERIFY_COMPUTE), (st1, api.VERIFY_REUSE)):
+        q_dev, dk_dev, dv_dev = (torch.empty_like(t) for t in (xd.q, xd.draft_k, xd.draft_v))
+        out_dev = torch.empty_like(st.out)
+        out_h = torch.full(st.out.shape, float("nan"), dtype=st.out.dtype).pin_memory()
+        k = api.sv_verify_layer_host(st.shape, hq, q_dev, st.kv, st.reps, wl.budget, hk, hv,
+                                     dk_dev, dv_dev, st.parents, reuse, st.slot, out_h, out_dev,
+                                     st.ws, None, ci, co)
+        assert k == ref0.k
+        outs.append(out_h)
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st0.ws) == 0 and api.sv_read_status(st1.ws) == 0
+    assert torch.equal(st0.sel, ref0.sel)
+    assert torch.equal(outs[0], out0.cpu()) and torch.equal(outs[1], out1.cpu())
+
+
 @pytest.mark.parametrize("tree", [False, True], ids=["chain", "tree16"])
 def test_overlap_by_distance_vs_oracle(tree):
     """The overlap of draft pairs' own block sets by position distance (the
