@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(32 * 10, 1)
       tma_load_3d(smem_u32(qs) + C::kQBox, &tmQ, 64, h * a.G, b * a.T, qb);
     }
     const int oob_row = a.num_pages * a.Hkv * TBLK;  // past the end: TMA zero-fills
+    // pages are read once per call: first out of L2 (see l2_evict_first_policy)
+    const uint64_t kv_policy = l2_evict_first_policy();
     int issued = 0;
     bool stop = false;
     int i = 0;  // ring index (a stage is i % NS, its phase parity (i / NS) & 1)
@@ -438,10 +440,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
               mbar_arrive_expect_tx(fb, kStageBytes);
               const uint32_t kdst = smem_u32(ring + s * kStageBytes);
               const uint32_t vdst = kdst + kTileBytes;
-              tma_load_2d(kdst, &tmK, 0, rq, fb);
-              tma_load_2d(kdst + kBoxBytes, &tmK, 64, rq, fb);
-              tma_load_2d(vdst, &tmV, 0, rq, fb);
-              tma_load_2d(vdst + kBoxBytes, &tmV, 64, rq, fb);
+              tma_load_2d_hint(kdst, &tmK, 0, rq, fb, kv_policy);
+              tma_load_2d_hint(kdst + kBoxBytes, &tmK, 64, rq, fb, kv_policy);
+              tma_load_2d_hint(vdst, &tmV, 0, rq, fb, kv_policy);
+              tma_load_2d_hint(vdst + kBoxBytes, &tmV, 64, rq, fb, kv_policy);
               issued = i + 1;
             }
           }
@@ -476,10 +478,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
             mbar_arrive_expect_tx(fb, kStageBytes);
             const uint32_t kdst = smem_u32(ring + s * kStageBytes);
             const uint32_t vdst = kdst + kTileBytes;
-            tma_load_2d(kdst, &tmK, 0, rq, fb);
-            tma_load_2d(kdst + kBoxBytes, &tmK, 64, rq, fb);
-            tma_load_2d(vdst, &tmV, 0, rq, fb);
-            tma_load_2d(vdst + kBoxBytes, &tmV, 64, rq, fb);
+            tma_load_2d_hint(kdst, &tmK, 0, rq, fb, kv_policy);
+            tma_load_2d_hint(kdst + kBoxBytes, &tmK, 64, rq, fb, kv_policy);
+            tma_load_2d_hint(vdst, &tmV, 0, rq, fb, kv_policy);
+            tma_load_2d_hint(vdst + kBoxBytes, &tmV, 64, rq, fb, kv_policy);
             issued = i + 1;
           }
         }

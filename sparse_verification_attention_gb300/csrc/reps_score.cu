@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
     const int32_t* bt = a.block_table + (size_t)b * a.nb_max;
     for (int e = r0 + 32 * threadIdx.x; e < r1; e += 32 * kScoreThreads) prefetch_l2(bt + e);
   }
+  const uint64_t pol = l2_evict_first_policy();  // representatives are read once per call
   float4 qh[CH];
   bool have_q = false;
   for (int base = r0 + warp * R; base < r1; base += kScoreWarps * R) {
@@ -177,7 +178,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
       for (int c = 0; c < CH; ++c) {
         const int ch = lane + 32 * c;
         rv[u][c] = (base + u < r1 && ch < nchunk)
-                       ? __ldg(reinterpret_cast<const float4*>(rep0 + (size_t)(base + u) * a.d) + ch)
+                       ? ld_stream_f4(reinterpret_cast<const float4*>(rep0 + (size_t)(base + u) * a.d) + ch,
+                                      pol)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
