@@ -79,7 +79,9 @@ struct TcCfg {
   static constexpr int kQBytes = 2 * kQBox;       // the first segment's Q operand
   static constexpr int kRingOff = kQBytes;
   static constexpr int kOst = TD + 4;
-  static constexpr int kMergeBytes = (2 * kRows * kOst + 3 * kRows * 2) * 4;
+  // staging of the final segment: both sets' o [2 kRows][kOst], their
+  // (m, l) [2 kRows], the fold weights [kRows] and the folded (M, L) [kRows]
+  static constexpr int kMergeBytes = (2 * kRows * kOst + 4 * kRows * 2) * 4;
   static constexpr int kRingRaw = NS * kStageBytes;
   static constexpr int kRing = r1024(kMergeBytes > kRingRaw ? kMergeBytes : kRingRaw);
   static constexpr int kCtrlOff = kRingOff + kRing;
@@ -781,6 +783,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
   constexpr int KR = C::kRows;
   float* po = reinterpret_cast<float*>(ring);   // [2*KR][OST]
   float* pml = po + (size_t)2 * KR * OST;       // [2*KR][2], then [KR][2] weights
+  float* cml = pml + (size_t)6 * KR;            // [KR][2]: folded (M, L), cluster merge
   const int jf = sp.n - 1;  // final segment (none when the CTA has no work)
   if (jf >= 0) {
     const int pair = sp.pair[jf];
@@ -805,11 +808,26 @@ __global__ void __launch_bounds__(32 * 10, 1)
       const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
       const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
       *reinterpret_cast<float2*>(pw + 2 * rr) = make_float2(wa, wb);
-      if (rr < a.rpad) own_ml[rr] = make_float2(M, wa * ma.y + wb * mb.y);
+      if (a.cluster_merge)
+        *reinterpret_cast<float2*>(cml + 2 * rr) = make_float2(M, wa * ma.y + wb * mb.y);
+      else if (rr < a.rpad)
+        own_ml[rr] = make_float2(M, wa * ma.y + wb * mb.y);
     }
     __syncthreads();
+    if (a.cluster_merge) {
+      // folded rows in place of set A's staged rows, for the cluster merge
+      for (int idx = threadIdx.x; idx < KR * (TD / 4); idx += NT) {
+        const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
+        const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
+        float4* pa = reinterpret_cast<float4*>(po + rr * OST + c4);
+        const float4 oa = *pa;
+        const float4 ob = *reinterpret_cast<const float4*>(po + (KR + rr) * OST + c4);
+        *pa = make_float4(w.x * oa.x + w.y * ob.x, w.x * oa.y + w.y * ob.y,
+                          w.x * oa.z + w.y * ob.z, w.x * oa.w + w.y * ob.w);
+      }
+    }
     // folded rows straight to the workspace (rows past kRows are zero padding)
-    for (int idx = threadIdx.x; idx < a.rpad * (TD / 4); idx += NT) {
+    for (int idx = threadIdx.x; !a.cluster_merge && idx < a.rpad * (TD / 4); idx += NT) {
       const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (rr < KR) {
@@ -826,12 +844,61 @@ __global__ void __launch_bounds__(32 * 10, 1)
     // arrival that completes a pair also acquires the other partials. (A
     // mid-stream segment arrived from the producer warp.)
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !a.cluster_merge) {
       if ((arrive_acq_rel(&a.counters[pair * kPairWords]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf])
         pair_done[jf] = 1;
     }
   }
   __syncthreads();
+
+  if (a.cluster_merge) {
+    // ------------------------------------------------------- cluster merge
+    // The pair's CTAs are one cluster (rank = split); each has its folded
+    // partial (o rows in po, (M, L) in cml) in its own shared memory. After
+    // the cluster barrier, CTA `rank` merges rows [rank * share, ...) from
+    // every CTA's shared memory, in rank order, with the formula below; the
+    // second barrier keeps every CTA's shared memory alive until all reads
+    // are done. Every CTA reaches both barriers on every path.
+    cluster_sync_all();
+    const int ncl = a.cluster_merge;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = sp.pair[0], b = pair / a.Hkv, h = pair % a.Hkv;
+    const int share = (a.R + ncl - 1) / ncl;
+    const int r0 = min(a.R, (int)rank * share), r1 = min(a.R, r0 + share);
+    const uint32_t po_s = smem_u32(po), ml_s = smem_u32(cml);
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+    for (int idx = threadIdx.x; idx < (r1 - r0) * (TD / 4); idx += NT) {
+      const int r = r0 + idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
+      float M = -INFINITY;
+      for (int q = 0; q < ncl; ++q) M = fmaxf(M, ld_cluster_f2(cluster_map(ml_s + r * 8, q)).x);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int q = 0; q < ncl; ++q) {
+        const float2 ml = ld_cluster_f2(cluster_map(ml_s + r * 8, q));
+        const float4 o = ld_cluster_f4(cluster_map(po_s + (r * OST + c4) * 4, q));
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        if (w != 0.f) {  // a CTA without units holds no rows worth reading
+          L += w * ml.y;
+          acc.x += w * o.x;
+          acc.y += w * o.y;
+          acc.z += w * o.z;
+          acc.w += w * o.w;
+        }
+      }
+      const float inv = 1.0f / L;
+      const int t = r / a.G, gq = r % a.G;
+      __nv_bfloat16* dst = outp + (((size_t)b * a.T + t) * a.Hq + h * a.G + gq) * TD + c4;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst) = u;
+    }
+    cluster_sync_all();
+    return;
+  }
 
   // ----------------------------------------------------------------- merge
   //   M = max_s m_s, w_s = 2^(m_s - M), out = sum_s w_s o_s / sum_s w_s l_s,
@@ -979,6 +1046,9 @@ cudaError_t launch_tc_cfg(const AttendArgs& a, cudaStream_t st) {
       !encode_draft_map(&mdv, a.draft_v, a.B, a.T, a.Hkv, TD, TBLK, &why))
     return cudaErrorInvalidValue;
   const int ctas = a.streamk ? a.n_splits : a.B * a.Hkv * a.n_splits + a.split_extra;
+  if (a.cluster_merge)
+    return launch_pdl_cluster(attend_tc_kernel<NSW, K::NS>, dim3(ctas), dim3(K::C::kThreads),
+                              K::C::kSmem, a.cluster_merge, st, mk, mv, mq, mdk, mdv, a);
   return launch_pdl(attend_tc_kernel<NSW, K::NS>, dim3(ctas), dim3(K::C::kThreads), K::C::kSmem,
                     st, mk, mv, mq, mdk, mdv, a);
 }
@@ -995,7 +1065,9 @@ int occupancy_tc_cfg() {
   if (cudaFuncSetAttribute(K::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, K::C::kSmem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(K::fn(), cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaFuncSetAttribute(K::fn(), cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
     return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K::fn(), K::C::kThreads, K::C::kSmem) !=
@@ -1017,6 +1089,58 @@ bool attend_tc_applies(const AttendArgs& a, int dtype) {
     return false;
   if ((long long)(a.num_pages + 1) * a.Hkv * a.blk >= (1ll << 31)) return false;
   return true;
+}
+
+// Clusters of ncl CTAs that the device keeps resident at once.
+template <int NSW>
+int active_clusters_cfg(int ncl, int ctas) {
+  using K = TcKernel<NSW>;
+  if (occupancy_tc_cfg<NSW>() <= 0) return 0;  // sets the attributes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(K::C::kThreads);
+  cfg.dynamicSmemBytes = K::C::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, K::fn(), &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int attend_tc_cluster(const AttendArgs& a, int pairs) {
+  constexpr int kMaxPairs = 64;
+  if (pairs < 1 || pairs > kMaxPairs) return 0;
+  const int nsw = (a.R + 31) / 32;
+  const int cfgi = nsw <= 1 ? 0 : nsw <= 2 ? 1 : 2;
+  // answers depend on the device, the kernel variant and the pair count only
+  static std::atomic<int> cache[kMaxDevices][3][kMaxPairs + 1];
+  const int dev = current_device();
+  const int c = cache[dev][cfgi][pairs].load();
+  if (c != 0) return c > 0 ? c : 0;
+  // the largest cluster of 8..16 CTAs the device keeps `pairs` of resident
+  // (16 is not always the best: how many fit depends on how the SMs are
+  // grouped on the chip)
+  int best = 0;
+  for (int ncl = 16; ncl >= 8; --ncl) {
+    if (pairs * ncl > sm_count()) continue;
+    const int n = cfgi == 0   ? active_clusters_cfg<1>(ncl, pairs * ncl)
+                  : cfgi == 1 ? active_clusters_cfg<2>(ncl, pairs * ncl)
+                              : active_clusters_cfg<4>(ncl, pairs * ncl);
+    if (n >= pairs) {
+      best = ncl;
+      break;
+    }
+  }
+  cache[dev][cfgi][pairs].store(best > 0 ? best : -1);
+  return best;
 }
 
 int attend_tc_ctas_per_sm(const AttendArgs& a) {

@@ -42,6 +42,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// launch_pdl with the grid cut into thread-block clusters of `cluster` CTAs
+// (x dimension).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               int cluster, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Per-(b, h) words that CTAs poll or count on (arrival counts, claim words)
@@ -177,6 +199,11 @@ struct AttendArgs {
   // unclaimed when the wait ends is merged by the pair's last CTA to arrive.
   // 0: the last CTA merges every row and nothing waits.
   unsigned merge_wait_ns;
+  // > 0 (tcgen05 path, split map only): the n_splits = cluster_merge CTAs of
+  // a pair form one thread-block cluster and merge the pair's partials
+  // through distributed shared memory at the end; no workspace partials,
+  // counts or waits on other clusters.
+  int cluster_merge;
   float scale_log2;     // log2(e) / sqrt(d)
   unsigned long long anc[kMaxT];  // bit u of anc[t]: draft t sees draft u
   VarLen vl;  // per-sequence nb, tail and n_sel (on = 0: the uniform ones)
@@ -245,6 +272,10 @@ cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st
 bool attend_tc_applies(const AttendArgs& a, int dtype);
 int attend_tc_ctas_per_sm(const AttendArgs& a);
 cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st);
+// Largest cluster size in 8..16 (CTAs per pair, one pair per cluster) for
+// which all `pairs` clusters of the tcgen05 kernel are resident at once, 0 if
+// none.
+int attend_tc_cluster(const AttendArgs& a, int pairs);
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
 // Log-sum-exp merge of the global split partials into out (any path; honours
 // the non-uniform split map).

@@ -443,6 +443,17 @@ static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int 
     // some pairs getting one split more than others
     p.per_sm = attend_tc_ctas_per_sm(a);
     const int slots = sm_count() * (p.per_sm > 0 ? p.per_sm : 1);
+    // Few pairs: one cluster of 8 to 16 CTAs per pair, the pair's units
+    // split evenly over it and merged through distributed shared memory.
+    // Many pairs keep stream-K, which uses every SM.
+    const int ncl = pairs * 8 <= slots ? attend_tc_cluster(a, pairs) : 0;
+    if (ncl > 0 && n_units >= ncl) {
+      p.cluster = ncl;
+      p.n_splits = ncl;
+      p.slot_stride = ncl;
+      p.bps = (n_units + ncl - 1) / ncl;
+      return p;
+    }
     // stream-K cuts equal runs of equal-length pairs: uniform contexts only
     const int sk = a.vl.on ? 0 : streamk_slots(pairs, n_units, slots);
     if (sk > 0 && sk <= max_slots) {
@@ -516,12 +527,13 @@ static sv_status run_attend(const sv_shape* s, const void* q, const sv_kv* kv, c
   a.slot_stride = p.slot_stride;
   a.streamk = p.streamk;
   cudaError_t e;
-  if (p.cluster > 0) {
+  if (p.cluster > 0 && p.path != SV_PATH_TCGEN05) {
     e = launch_attend_fast(a, p.cluster, st);
     if (e != cudaSuccess) return cuda_fail(e, "attend launch");
     return SV_OK;
   }
-  if (p.path == SV_PATH_TCGEN05) {  // merges in its last CTA per (b, h)
+  if (p.path == SV_PATH_TCGEN05) {  // merges in the same launch
+    a.cluster_merge = p.cluster;
     e = launch_attend_tc(a, st);
     return e == cudaSuccess ? SV_OK : cuda_fail(e, "attend launch");
   }
@@ -1161,9 +1173,10 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
   // the arrival counters (the partials are fully written before being read)
   cudaError_t e = cudaMemsetAsync(base, 0, L.part_o, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (static scratch)");
-  if (p.cluster > 0) {
+  if (p.cluster > 0 && p.path != SV_PATH_TCGEN05) {
     e = launch_attend_fast(a, p.cluster, st);
   } else if (p.path == SV_PATH_TCGEN05) {
+    a.cluster_merge = p.cluster;
     e = launch_attend_tc(a, st);
   } else {
     e = p.path == SV_PATH_MMA_SYNC ? launch_attend_fast(a, 0, st)

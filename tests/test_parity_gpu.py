@@ -207,9 +207,17 @@ ATTEND_CASES = [
     ("tc_sk_32pairs_129units", dict(B=4, Hq=32, Hkv=8, ctx=64 * 200), 128),
     ("tc_sk_tree16_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
                                ctx=64 * 40), 29),
-    ("tc_sk_one_unit_per_cta", dict(B=4, Hq=8, Hkv=2, ctx=64 * 30), 18),
-    ("tc_sk_runs_cross_pairs", dict(B=19, Hq=4, Hkv=1, T=4, ctx=64 * 12), 8),
+    ("tc_sk_one_unit_per_cta", dict(B=19, Hq=8, Hkv=2, ctx=64 * 30), 3),
+    ("tc_sk_runs_cross_pairs", dict(B=23, Hq=4, Hkv=1, T=4, ctx=64 * 12), 8),
     ("tc_sk_two_unit_pairs", dict(B=75, Hq=4, Hkv=2, T=2, ctx=64 * 4), 1),
+    # few pairs: one cluster of 8 to 16 CTAs per pair (as many as the device
+    # keeps resident for that many pairs), merged through distributed shared
+    # memory
+    ("tc_cluster_B1_H8", dict(B=1, Hq=32, Hkv=8, ctx=64 * 100), 64),
+    ("tc_cluster_tree16_R128_tail", dict(B=1, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                                         ctx=64 * 60 + 5), 40),
+    ("tc_cluster_12pairs", dict(B=3, Hq=32, Hkv=4, ctx=64 * 40), 30),
+    ("tc_cluster_idle_ctas", dict(B=1, Hq=32, Hkv=8, ctx=64 * 20), 16),
     # contexts ending in a partial block: its tokens are always attended
     ("tc_tail_split", dict(ctx=64 * 20 + 17), 7),
     ("tc_sk_tail", dict(B=4, Hq=32, Hkv=8, ctx=64 * 100 + 40), 50),
@@ -246,8 +254,8 @@ def test_sparse_attend(name, over, n_sel):
     want_path = {"tc": api.SV_PATH_TCGEN05, "mma": api.SV_PATH_MMA_SYNC,
                  "generic": api.SV_PATH_CUDA_CORES}[name.split("_")[0]]
     assert plan.path == want_path, (plan.path, want_path)
-    if "cluster" in name and want_path == api.SV_PATH_MMA_SYNC:
-        assert plan.cluster > 0
+    if "cluster" in name:
+        assert plan.cluster >= (8 if want_path == api.SV_PATH_TCGEN05 else 1), plan.cluster
     if "_sk_" in name:
         assert plan.streamk == 1, (plan.n_splits, plan.blocks_per_split)
     out = torch.zeros_like(xd.q)
