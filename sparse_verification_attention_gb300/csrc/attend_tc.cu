@@ -100,6 +100,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
 }
 
 constexpr int kMergeRowBytes = TD * 4 + 8;  // a partial row's o and (m, l)
+constexpr int kMaxCluster = 16;  // CTAs per pair in the cluster merge
 constexpr size_t kSoloMergeBytes = 128 * 1024;  // see launch_attend_tc
 
 // Log-sum-exp combine of rows [r0, r0 + nv) of one pair from partials staged
@@ -869,21 +870,32 @@ __global__ void __launch_bounds__(32 * 10, 1)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
     for (int idx = threadIdx.x; idx < (r1 - r0) * (TD / 4); idx += NT) {
       const int r = r0 + idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
+      // every remote load of this (row, 4 columns) issued before any is used:
+      // one round trip through the cluster's shared memory
+      float2 ml[kMaxCluster];
+      float4 o[kMaxCluster];
+#pragma unroll
+      for (int q = 0; q < kMaxCluster; ++q) {
+        if (q < ncl) {
+          ml[q] = ld_cluster_f2(cluster_map(ml_s + r * 8, q));
+          o[q] = ld_cluster_f4(cluster_map(po_s + (r * OST + c4) * 4, q));
+        }
+      }
       float M = -INFINITY;
-      for (int q = 0; q < ncl; ++q) M = fmaxf(M, ld_cluster_f2(cluster_map(ml_s + r * 8, q)).x);
+#pragma unroll
+      for (int q = 0; q < kMaxCluster; ++q)
+        if (q < ncl) M = fmaxf(M, ml[q].x);
       float L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int q = 0; q < ncl; ++q) {
-        const float2 ml = ld_cluster_f2(cluster_map(ml_s + r * 8, q));
-        const float4 o = ld_cluster_f4(cluster_map(po_s + (r * OST + c4) * 4, q));
-        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-        if (w != 0.f) {  // a CTA without units holds no rows worth reading
-          L += w * ml.y;
-          acc.x += w * o.x;
-          acc.y += w * o.y;
-          acc.z += w * o.z;
-          acc.w += w * o.w;
+#pragma unroll
+      for (int q = 0; q < kMaxCluster; ++q) {
+        if (q < ncl && ml[q].x != -INFINITY) {  // a CTA without units adds nothing
+          const float w = exp2f(ml[q].x - M);
+          L += w * ml[q].y;
+          acc.x += w * o[q].x;
+          acc.y += w * o[q].y;
+          acc.z += w * o[q].z;
+          acc.w += w * o[q].w;
         }
       }
       const float inv = 1.0f / L;
@@ -1129,7 +1141,7 @@ int attend_tc_cluster(const AttendArgs& a, int pairs) {
   // (16 is not always the best: how many fit depends on how the SMs are
   // grouped on the chip)
   int best = 0;
-  for (int ncl = 16; ncl >= 8; --ncl) {
+  for (int ncl = kMaxCluster; ncl >= 8; --ncl) {
     if (pairs * ncl > sm_count()) continue;
     const int n = cfgi == 0   ? active_clusters_cfg<1>(ncl, pairs * ncl)
                   : cfgi == 1 ? active_clusters_cfg<2>(ncl, pairs * ncl)
