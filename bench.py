@@ -3,17 +3,19 @@
 One step = one verification layer per layer of the workload through the
 public per-layer call (sv_verify_layer): on a computing layer the fused
 block scoring + budgeted top-k selection kernel, then the split-KV
-tensor-core attention whose last CTA per (sequence, KV head) merges the
-partials; on a reuse layer (the 32-layer stack) only the attention, over the
-previous computing layer's selection. Representatives are built at prefill
-and rebuilt when a block fills (every blk / T steps), outside the step; that
+tensor-core attention, which merges its partials in the same launch; on a
+reuse layer (the 32-layer stack) only the attention, over the previous
+computing layer's selection. Representatives are built at prefill and
+rebuilt when a block fills (every blk / T steps), outside the step; that
 update is timed on its own (`rep_update`).
 
 Prints ONE JSON line (rank 0). Timing: W warm-up steps, then exactly K steps
-replayed from CUDA graphs, bracketed by a barrier and a device synchronize on
-both sides, CUDA events on the launching stream, max over ranks. L2: the
-steps rotate over enough independent input sets that their working set is
->= 4x the L2 size, so every step reads cold HBM.
+replayed from CUDA graphs (one graph holding one step of every input set in
+turn, so that consecutive steps chain as consecutive layers do, plus
+single-step graphs for a remainder), bracketed by a barrier and a device
+synchronize on both sides, CUDA events on the launching stream, max over
+ranks. L2: the steps rotate over enough independent input sets that their
+working set is >= 4x the L2 size, so every step reads cold HBM.
 
 Roofline: the attention launch alone is timed with CUDA events on its stream
 over a second loop of graph-replayed attention launches (rotating input sets,
@@ -437,19 +439,30 @@ def measure(args, wl, dist, steps: int, warmup: int, full: bool, clocks=None):
         with torch.cuda.graph(g):
             run_step(wl, ss)
         graphs.append(g)
+    # one step of every set in turn in one graph: consecutive steps chain as
+    # consecutive layers do (each kernel's dependents launch early and wait
+    # on it), which separate graph launches would not
+    rotation = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rotation):
+        for ss in sets:
+            run_step(wl, ss)
     torch.cuda.synchronize()
     check_status(sets, "graph capture")
 
+    def replay_steps(n):  # exactly n steps: whole rotations, then single steps
+        for _ in range(n // n_sets):
+            rotation.replay()
+        for i in range(n % n_sets):
+            graphs[i].replay()
+
     if clocks is not None:
         clocks.start()
-    for i in range(warmup):
-        graphs[i % n_sets].replay()
+    replay_steps(warmup)
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(steps):
-        graphs[i % n_sets].replay()
+    replay_steps(steps)
     e1.record()
     torch.cuda.synchronize()
     barrier(dist)

@@ -151,6 +151,17 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const __grid_co
   const int r1 = min(nbb, r0 + a.rows_per_cta);
   const float* rep0 = a.reps + (size_t)pair * a.nb_max * a.d;
   float* srow = a.scores + (size_t)pair * a.nb;
+  if (threadIdx.x < 32 && r0 < r1) {
+    // Warm L2 with this CTA's representative rows (contiguous) while the
+    // previous kernel finishes: a prefetch only, so it cannot expose data
+    // that kernel is still writing (L2 is where every write lands); the
+    // loads below still come after the wait. 16 KB per lane and copy.
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(rep0 + (size_t)r0 * a.d);
+    const size_t bytes = (size_t)(r1 - r0) * a.d * sizeof(float);  // a multiple of 16
+    constexpr size_t kChunk = 16384;
+    for (size_t off = (size_t)threadIdx.x * kChunk; off < bytes; off += 32 * kChunk)
+      prefetch_bulk_l2(base + off, (uint32_t)(bytes - off < kChunk ? bytes - off : kChunk));
+  }
   pdl_wait();
   pdl_trigger();  // the next kernel may launch; it still waits for this grid to finish
   if (r0 >= nbb) {
