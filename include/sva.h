@@ -241,8 +241,9 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
  * cores with TMEM accumulators), SV_PATH_MMA_SYNC (bf16, d in {64,128},
  * blk in {32,64}, T*G <= 128, T <= blk), else SV_PATH_CUDA_CORES; cluster > 0
  * when the splits of one (b, h) merge inside a thread-block cluster of that
- * size (on the tcgen05 path: few (b, h) pairs, 8 to 16 CTAs each, merged
- * through distributed shared memory); split_extra > 0 when that many (b, h) pairs get n_splits + 1 splits;
+ * size (on the tcgen05 path: 4 to 16 CTAs per (b, h) pair, merged through
+ * distributed shared memory, when stream-K's merge would be wide: few pairs,
+ * or 128-row tiles); split_extra > 0 when that many (b, h) pairs get n_splits + 1 splits;
  * streamk = 1 when n_splits CTAs instead share the work units of all pairs
  * in equal runs (the tcgen05 path when there are at least as many units as
  * CTAs and a run fits in one pair).

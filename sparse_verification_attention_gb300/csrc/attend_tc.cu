@@ -101,6 +101,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
 
 constexpr int kMergeRowBytes = TD * 4 + 8;  // a partial row's o and (m, l)
 constexpr int kMaxCluster = 16;  // CTAs per pair in the cluster merge
+constexpr int kMinCluster = 4;   // smallest cluster the plan uses
 constexpr size_t kSoloMergeBytes = 128 * 1024;  // see launch_attend_tc
 
 // Log-sum-exp combine of rows [r0, r0 + nv) of one pair from partials staged
@@ -1141,7 +1142,7 @@ int attend_tc_cluster(const AttendArgs& a, int pairs) {
   // (16 is not always the best: how many fit depends on how the SMs are
   // grouped on the chip)
   int best = 0;
-  for (int ncl = kMaxCluster; ncl >= 8; --ncl) {
+  for (int ncl = kMaxCluster; ncl >= kMinCluster; --ncl) {
     if (pairs * ncl > sm_count()) continue;
     const int n = cfgi == 0   ? active_clusters_cfg<1>(ncl, pairs * ncl)
                   : cfgi == 1 ? active_clusters_cfg<2>(ncl, pairs * ncl)
@@ -1153,6 +1154,10 @@ int attend_tc_cluster(const AttendArgs& a, int pairs) {
   }
   cache[dev][cfgi][pairs].store(best > 0 ? best : -1);
   return best;
+}
+
+bool attend_tc_narrow_merge(int slot_stride, int rpad) {
+  return (size_t)slot_stride * rpad * kMergeRowBytes <= kSoloMergeBytes;
 }
 
 int attend_tc_ctas_per_sm(const AttendArgs& a) {
@@ -1167,8 +1172,7 @@ cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st) {
   // When one CTA would copy little (few slots of few rows), the pair's last
   // CTA merges it alone and the others leave at once, freeing their SMs for
   // the next kernel; otherwise the pair's CTAs share the rows.
-  const size_t one_merger = (size_t)a.slot_stride * a.rpad * kMergeRowBytes;
-  a.merge_wait_ns = one_merger <= kSoloMergeBytes ? 0u : (unsigned)kMergeWaitNs;
+  a.merge_wait_ns = attend_tc_narrow_merge(a.slot_stride, a.rpad) ? 0u : (unsigned)kMergeWaitNs;
   if (nsw <= 1) return launch_tc_cfg<1>(a, st);
   if (nsw <= 2) return launch_tc_cfg<2>(a, st);
   return launch_tc_cfg<4>(a, st);

@@ -272,10 +272,13 @@ cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st
 bool attend_tc_applies(const AttendArgs& a, int dtype);
 int attend_tc_ctas_per_sm(const AttendArgs& a);
 cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st);
-// Largest cluster size in 8..16 (CTAs per pair, one pair per cluster) for
+// Largest cluster size in 4..16 (CTAs per pair, one pair per cluster) for
 // which all `pairs` clusters of the tcgen05 kernel are resident at once, 0 if
 // none.
 int attend_tc_cluster(const AttendArgs& a, int pairs);
+// True when one CTA merging a pair's slot_stride partial slots of rpad rows
+// copies little enough that the pair's last CTA should merge it alone.
+bool attend_tc_narrow_merge(int slot_stride, int rpad);
 cudaError_t launch_attend_generic(const AttendArgs& a, int dtype, cudaStream_t st);
 // Log-sum-exp merge of the global split partials into out (any path; honours
 // the non-uniform split map).

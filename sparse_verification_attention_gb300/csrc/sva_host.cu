@@ -443,10 +443,16 @@ static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int 
     // some pairs getting one split more than others
     p.per_sm = attend_tc_ctas_per_sm(a);
     const int slots = sm_count() * (p.per_sm > 0 ? p.per_sm : 1);
-    // Few pairs: one cluster of 8 to 16 CTAs per pair, the pair's units
-    // split evenly over it and merged through distributed shared memory.
-    // Many pairs keep stream-K, which uses every SM.
-    const int ncl = pairs * 8 <= slots ? attend_tc_cluster(a, pairs) : 0;
+    // stream-K cuts equal runs of equal-length pairs: uniform contexts only
+    const int sk = a.vl.on ? 0 : streamk_slots(pairs, n_units, slots);
+    const bool sk_ok = sk > 0 && sk <= max_slots;
+    // Stream-K uses every SM; it is kept when the pair's last CTA can merge
+    // the pair alone (few partial slots of few rows). Otherwise -- few pairs
+    // (many slots each), or 128-row tiles -- one cluster of 4 to 16 CTAs per
+    // pair, the pair's units split evenly over it and merged through
+    // distributed shared memory, when the device keeps all of them resident.
+    const bool narrow = sk_ok && attend_tc_narrow_merge(sk, a.rpad);
+    const int ncl = narrow ? 0 : attend_tc_cluster(a, pairs);
     if (ncl > 0 && n_units >= ncl) {
       p.cluster = ncl;
       p.n_splits = ncl;
@@ -454,9 +460,7 @@ static AttendPlan make_plan(AttendArgs& a, int dtype, int pairs, int n_sel, int 
       p.bps = (n_units + ncl - 1) / ncl;
       return p;
     }
-    // stream-K cuts equal runs of equal-length pairs: uniform contexts only
-    const int sk = a.vl.on ? 0 : streamk_slots(pairs, n_units, slots);
-    if (sk > 0 && sk <= max_slots) {
+    if (sk_ok) {
       p.streamk = 1;
       p.n_splits = slots;
       p.bps = (int)(((long long)pairs * n_units + slots - 1) / slots);
