@@ -65,7 +65,7 @@ constexpr uint32_t kColQ1 = 448;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSeg = 2;          // pair segments per CTA
 #ifndef SVA_SPEC_UNITS
-#define SVA_SPEC_UNITS 12
+#define SVA_SPEC_UNITS 4
 #endif
 constexpr int kSpecUnits = SVA_SPEC_UNITS;  // units prefetched speculatively before the wait
 
