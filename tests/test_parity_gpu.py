@@ -772,8 +772,9 @@ def test_reuse_guard_on_device():
 def test_verify_layer_host_buffers(streams):
     """sv_verify_layer_host takes the step's q and draft K/V from pinned host
     memory and returns the output there: it must give, bit for bit, what
-    sv_verify_layer gives on device buffers, for a computing layer and for a
-    reuse layer after it, on one stream and with separate copy streams."""
+    sv_verify_layer gives on device buffers, for a computing layer, a reuse
+    layer after it and a full verification, on one stream and with separate
+    copy streams."""
     wl = small_wl(B=2, Hq=32, Hkv=8, ctx=64 * 50 + 9)
     x = W.make_layer(wl)
     xd = x.to("cuda")
@@ -787,20 +788,27 @@ def test_verify_layer_host_buffers(streams):
     st0 = api.LayerState(wl, xd)
     st1 = api.LayerState(wl, xd, build_reps=False)
     st1.slot = st0.slot
-    outs = []
-    for st, reuse in ((st0, api.VERIFY_COMPUTE), (st1, api.VERIFY_REUSE)):
+    st2 = api.LayerState(wl, xd, build_reps=False)
+    ref2 = api.LayerState(wl, xd, build_reps=False)
+    out2 = ref2.verify(reuse=api.VERIFY_FULL).clone()
+    torch.cuda.synchronize()
+    outs, ks = [], []
+    for st, reuse in ((st0, api.VERIFY_COMPUTE), (st1, api.VERIFY_REUSE),
+                      (st2, api.VERIFY_FULL)):
         q_dev, dk_dev, dv_dev = (torch.empty_like(t) for t in (xd.q, xd.draft_k, xd.draft_v))
         out_dev = torch.empty_like(st.out)
         out_h = torch.full(st.out.shape, float("nan"), dtype=st.out.dtype).pin_memory()
-        k = api.sv_verify_layer_host(st.shape, hq, q_dev, st.kv, st.reps, wl.budget, hk, hv,
-                                     dk_dev, dv_dev, st.parents, reuse, st.slot, out_h, out_dev,
-                                     st.ws, None, ci, co)
-        assert k == ref0.k
+        ks.append(api.sv_verify_layer_host(st.shape, hq, q_dev, st.kv, st.reps, wl.budget, hk,
+                                           hv, dk_dev, dv_dev, st.parents, reuse, st.slot,
+                                           out_h, out_dev, st.ws, None, ci, co))
         outs.append(out_h)
     torch.cuda.synchronize()
-    assert api.sv_read_status(st0.ws) == 0 and api.sv_read_status(st1.ws) == 0
+    assert ks == [ref0.k, ref0.k, wl.NB]
+    for st in (st0, st1, st2):
+        assert api.sv_read_status(st.ws) == 0
     assert torch.equal(st0.sel, ref0.sel)
     assert torch.equal(outs[0], out0.cpu()) and torch.equal(outs[1], out1.cpu())
+    assert torch.equal(outs[2], out2.cpu())
 
 
 @pytest.mark.parametrize("tree", [False, True], ids=["chain", "tree16"])
