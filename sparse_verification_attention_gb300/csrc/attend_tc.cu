@@ -7,19 +7,24 @@
 // one KV head are stacked into one MMA tile and each selected page is read
 // from HBM once for all of them.
 //
-// Work split (one CTA per SM, since tcgen05 kernels are scheduled one per SM
-// here): the work units of a (b, h) pair are its selected blocks plus one
-// draft tile. Stream-K plans cut the flattened (pair, unit) sequence into one
-// equal run per CTA, so a CTA covers the tail of one pair and the head of the
-// next at most (two segments, each with its own Q in shared memory); plans
-// that cannot (fewer units than CTAs) give each pair whole splits.
+// Work split (one CTA per SM: the ring and all 512 TMEM columns are sized
+// for a whole SM): the work units of a (b, h) pair are its selected blocks, a
+// partial last block if any, and one draft tile. Three plans (chosen on the
+// host): stream-K cuts the flattened (pair, unit) sequence into one equal run
+// per CTA, so a CTA covers the tail of one pair and the head of the next at
+// most (two segments: the first segment's Q in shared memory, the second's
+// in TMEM); a cluster plan puts one thread-block cluster of 4..16 CTAs on
+// each pair and splits its units evenly; otherwise a split map gives each
+// pair whole splits.
 //
 // CTA roles (a 6-stage ring keeps ~192 KB of K/V in flight per SM):
-//   * producer warp: loads the first segment's Q by 3-D TMA, resolves selected
-//     block -> page through the block table (32 at a time, one lane each) and
-//     issues 2-D TMA copies (128-byte swizzle) of the page's K and V tiles
-//     into the ring; the draft tile (the pair's draft K/V rows) comes the
-//     same way, through a 3-D map over the draft tensors.
+//   * producer warp: loads the first segment's Q by 3-D TMA, takes each
+//     selected block's pool row (written beside the selection by the top-k,
+//     or looked up through the block table when the caller passes its own
+//     selection; 32 at a time, one lane each) and issues 2-D TMA copies
+//     (128-byte swizzle, L2 evict-first) of the page's K and V tiles into the
+//     ring; the draft tile (the pair's draft K/V rows) comes the same way,
+//     through a 4-D map over the draft tensors.
 //   * MMA warp (one elected lane): S_i = Q K_i^T into TMEM (M=128 rows, N=64
 //     tokens, K=128), then after softmax O += P_i V_i with P read from TMEM
 //     (M=128, N=128, K=64, V as an MN-major operand); the first P.V of each
@@ -33,12 +38,13 @@
 //     max (log2 domain; the accumulator is rescaled only when some row's max
 //     grows by more than 2^8, decided per warp so that the warp-collective
 //     TMEM loads/stores are taken by all lanes) and sum.
-//   * partials: a segment that ends mid-stream writes each set's unnormalised
-//     (o, m, l) rows from registers (the producer warp counts its arrival);
-//     the final segment folds the two sets in shared memory first and counts
-//     its arrival at the end of the CTA. Each CTA then waits until its pairs'
-//     segments have all arrived and merges its share of their rows with
-//     log-sum-exp weights, writing the output.
+//   * partials and merge: a segment that ends mid-stream writes each set's
+//     unnormalised (o, m, l) rows from registers; the final segment folds
+//     the two sets in shared memory. Cluster plans then merge the pair's
+//     folded rows through distributed shared memory; the others publish them
+//     in the workspace with an acquire-release arrival, and the pair's last
+//     CTA to arrive merges them (alone when its copy is small, else sharing
+//     row slices with the pair's CTAs that are still waiting).
 // Rows past R are padding: zero query rows whose outputs are never read.
 #include <atomic>
 
