@@ -199,7 +199,7 @@ struct AttendArgs {
   // unclaimed when the wait ends is merged by the pair's last CTA to arrive.
   // 0: the last CTA merges every row and nothing waits.
   unsigned merge_wait_ns;
-  // > 0 (tcgen05 path, split map only): the n_splits = cluster_merge CTAs of
+  // > 0 (tcgen05 path, one segment per CTA): the n_splits = cluster_merge CTAs of
   // a pair form one thread-block cluster and merge the pair's partials
   // through distributed shared memory at the end; no workspace partials,
   // counts or waits on other clusters.
@@ -266,9 +266,11 @@ int attend_fast_ctas_per_sm(const AttendArgs& a, bool cluster);
 // splits write global partials for launch_merge.
 cudaError_t launch_attend_fast(const AttendArgs& a, int cluster, cudaStream_t st);
 // tcgen05 path: bf16, d == 128, blk == 64, R <= 128, T <= 64.
-// Writes global split partials (stream-K runs, or the split map above) and
-// merges each (b, h)'s partials into out inside the same launch: the pair's
-// CTAs share the rows for a bounded wait, the last to arrive merges the rest.
+// Merges each (b, h)'s split partials into out inside the same launch: with
+// a.cluster_merge through distributed shared memory in the pair's cluster;
+// otherwise from global partials (stream-K runs, or the split map above),
+// by the pair's last CTA to arrive (alone when its copy is small, else
+// sharing row slices with the pair's CTAs still waiting, for a bounded wait).
 bool attend_tc_applies(const AttendArgs& a, int dtype);
 int attend_tc_ctas_per_sm(const AttendArgs& a);
 cudaError_t launch_attend_tc(AttendArgs a, cudaStream_t st);
