@@ -34,6 +34,9 @@
  *     SV_ERR_INVALID_ARG or SV_ERR_UNSUPPORTED has launched nothing.
  *   - Nothing throws across the ABI. sv_last_error() describes the last
  *     non-OK status of the calling thread.
+ *   - Every call that enqueues GPU work is wrapped, on the host, in an NVTX
+ *     range named after the call (visible to timeline tools; no cost
+ *     without one).
  *   - Limits: 1 <= T <= 64; Hq % Hkv == 0; d % 8 == 0 and 8 <= d <= 256;
  *     NB = ctx/blk full blocks <= 16384; a partial last block (ctx % blk
  *     tokens) is allowed; B <= 64 when the cache gives per-sequence

@@ -10,6 +10,8 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 
 namespace sva {
@@ -759,6 +761,17 @@ static int budgets_of(const sv_budget* bd, const sv_kv* kv, const Ctxs& c, int B
 
 using namespace sva;
 
+namespace {
+// An NVTX range named after the C-ABI call, around its whole host side
+// (validation, planning, launches), for timeline tools; a no-op without one.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+}  // namespace
+
 extern "C" {
 
 int sv_abi_version(void) { return SV_ABI_VERSION; }
@@ -775,6 +788,7 @@ size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax) {
 }
 
 sv_status sv_clear_status(void* workspace, void* stream) {
+  const CallRange range("sv_clear_status");
   if (!workspace) return fail(SV_ERR_INVALID_ARG, "workspace is NULL");
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), (cudaStream_t)stream);
   return e == cudaSuccess ? SV_OK : cuda_fail(e, "cudaMemsetAsync");
@@ -782,6 +796,7 @@ sv_status sv_clear_status(void* workspace, void* stream) {
 
 sv_status sv_reset_workspace(const sv_shape* shape, int nb_max, int kmax, void* workspace,
                              size_t ws_bytes, void* stream) {
+  const CallRange range("sv_reset_workspace");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if (nb_max < 0 || kmax < 0)
@@ -794,6 +809,7 @@ sv_status sv_reset_workspace(const sv_shape* shape, int nb_max, int kmax, void* 
 }
 
 sv_status sv_read_status(const void* workspace, uint32_t* flags, void* stream) {
+  const CallRange range("sv_read_status");
   if (!workspace || !flags) return fail(SV_ERR_INVALID_ARG, "workspace/flags is NULL");
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost,
@@ -807,6 +823,7 @@ sv_status sv_read_status(const void* workspace, uint32_t* flags, void* stream) {
 
 sv_status sv_build_reps(const sv_shape* shape, const sv_kv* kv, int first_block, int n_blocks,
                         float* reps, void* stream) {
+  const CallRange range("sv_build_reps");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
@@ -827,6 +844,7 @@ sv_status sv_append_kv(const sv_shape* shape, void* k_pool, void* v_pool, const 
                        int nb_max, int num_pages, const int32_t* seq_ctx, const int32_t* n_accept,
                        const int32_t* accept_idx, const void* draft_k, const void* draft_v,
                        float* reps, void* workspace, void* stream) {
+  const CallRange range("sv_append_kv");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if (!k_pool || !v_pool || !block_table || !seq_ctx || !n_accept || !accept_idx || !draft_k ||
@@ -856,6 +874,7 @@ sv_status sv_append_kv(const sv_shape* shape, void* k_pool, void* v_pool, const 
 
 sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* reps, const sv_kv* kv,
                           float* scores, void* stream) {
+  const CallRange range("sv_score_blocks");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
@@ -874,6 +893,7 @@ sv_status sv_score_blocks(const sv_shape* shape, const void* q, const float* rep
 
 sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, int k, int32_t* sel,
                            int kmax, void* stream) {
+  const CallRange range("sv_select_blocks");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if (nb < 0 || nb > kMaxNB) return fail(SV_ERR_UNSUPPORTED, "nb=%d outside [0, %d]", nb, kMaxNB);
@@ -889,6 +909,7 @@ sv_status sv_select_blocks(const sv_shape* shape, const float* scores, int nb, i
 sv_status sv_score_select(const sv_shape* shape, const void* q, const float* reps, const sv_kv* kv,
                           const sv_budget* budget, int32_t* sel, int kmax, int* k_out,
                           void* workspace, size_t ws_bytes, void* stream) {
+  const CallRange range("sv_score_select");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, false)) != SV_OK) return r;
@@ -914,6 +935,7 @@ sv_status sv_sparse_attend(const sv_shape* shape, const void* q, const sv_kv* kv
                            int n_sel, int sel_stride, const void* draft_k, const void* draft_v,
                            const int32_t* draft_parent, void* out, void* workspace,
                            size_t ws_bytes, void* stream) {
+  const CallRange range("sv_sparse_attend");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
@@ -1098,6 +1120,7 @@ sv_status sv_verify_layer(const sv_shape* shape, const void* q, const sv_kv* kv,
                           const sv_budget* budget, const void* draft_k, const void* draft_v,
                           const int32_t* draft_parent, int reuse, sv_sel_slot* slot, int* k_out,
                           void* out, void* workspace, size_t ws_bytes, void* stream) {
+  const CallRange range("sv_verify_layer");
   return verify_layer(shape, q, kv, reps, budget, draft_k, draft_v, draft_parent, reuse, slot,
                       k_out, out, workspace, ws_bytes, stream, nullptr);
 }
@@ -1110,6 +1133,7 @@ sv_status sv_verify_layer_host(const sv_shape* shape, const void* q_host, void* 
                                int* k_out, void* out_host, void* out_dev, void* workspace,
                                size_t ws_bytes, void* stream, void* copy_in_stream,
                                void* copy_out_stream) {
+  const CallRange range("sv_verify_layer_host");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if (!q_host || !draft_k_host || !draft_v_host || !out_host)
@@ -1128,6 +1152,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
                                    const void* draft_k, const void* draft_v,
                                    const int32_t* draft_parent, void* out, uint32_t* flags_out,
                                    void* stream) {
+  const CallRange range("sv_sparse_attend_noalloc");
   sv_status r = check_shape(shape);
   if (r != SV_OK) return r;
   if ((r = check_kv(shape, kv, true)) != SV_OK) return r;
@@ -1198,6 +1223,7 @@ sv_status sv_sparse_attend_noalloc(const sv_shape* shape, const void* q, const s
 sv_status sv_selection_overlap(const int32_t* sels, int T, int pairs, int kmax, int k,
                                const int32_t* draft_parent, float* overlap0, float* by_distance,
                                void* stream) {
+  const CallRange range("sv_selection_overlap");
   if (T < 1 || T > kMaxT) return fail(SV_ERR_UNSUPPORTED, "T=%d outside [1, %d]", T, kMaxT);
   if (pairs < 0 || kmax < 1 || k < 1 || k > kmax)
     return fail(SV_ERR_INVALID_ARG, "pairs=%d, k=%d, kmax=%d: need pairs >= 0, 1 <= k <= kmax",
