@@ -768,6 +768,49 @@ def test_reuse_guard_on_device():
     assert e.value.status == api.SV_ERR_INVALID_ARG
 
 
+GUARD_CASES = [
+    ("tc_streamk", dict(B=4, Hq=32, Hkv=8, ctx=64 * 200 + 21), 40),
+    ("tc_cluster", dict(B=1, Hq=32, Hkv=8, ctx=64 * 100 + 7), 30),
+    ("tc_cluster_tree_R128", dict(B=8, Hq=32, Hkv=4, T=16, parents=W.TREE16_PARENTS,
+                                  ctx=64 * 40 + 9), 20),
+    ("mma_blk32", dict(B=2, Hq=8, Hkv=2, blk=32, ctx=32 * 80 + 5), 15),
+    ("generic_d96", dict(B=2, Hq=8, Hkv=2, d=96, blk=32, ctx=32 * 60 + 3), 11),
+]
+
+
+@pytest.mark.parametrize("name,over,k", GUARD_CASES, ids=[c[0] for c in GUARD_CASES])
+def test_guard_pages_are_never_read(name, over, k):
+    """Guard pages: the same layer with every page moved to an odd slot of a
+    pool twice as large whose even slots hold NaN. Representatives, scores,
+    selection and attention read only pages the block table names, so the
+    result must equal the unguarded run bit for bit; a stray read of an
+    unreferenced page would bring a NaN into it."""
+    from dataclasses import replace
+    wl = small_wl(budget=W.Budget(W.BUDGET_FIXED, k, 0, 0, 0, 0, 0), **over)
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    ref = api.LayerState(wl, xd)
+    out_ref = ref.verify().clone()
+    sel_ref = ref.sel.clone()
+
+    def guarded(pool):
+        g = torch.full((2 * pool.shape[0],) + tuple(pool.shape[1:]), float("nan"),
+                       dtype=pool.dtype, device=pool.device)
+        g[1::2] = pool
+        return g
+
+    bt = xd.block_table
+    xg = replace(xd, k_pool=guarded(xd.k_pool), v_pool=guarded(xd.v_pool),
+                 block_table=torch.where(bt >= 0, 2 * bt + 1, bt).to(bt.dtype))
+    st = api.LayerState(wl, xg)
+    out = st.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(ref.ws) == 0 and api.sv_read_status(st.ws) == 0
+    assert torch.equal(st.sel, sel_ref)
+    assert not torch.isnan(out).any()
+    assert torch.equal(out, out_ref)
+
+
 @pytest.mark.parametrize("streams", [False, True], ids=["one_stream", "copy_streams"])
 def test_verify_layer_host_buffers(streams):
     """sv_verify_layer_host takes the step's q and draft K/V from pinned host
