@@ -41,10 +41,14 @@
 //   * partials and merge: a segment that ends mid-stream writes each set's
 //     unnormalised (o, m, l) rows from registers; the final segment folds
 //     the two sets in shared memory. Cluster plans then merge the pair's
-//     folded rows through distributed shared memory; the others publish them
-//     in the workspace with an acquire-release arrival, and the pair's last
-//     CTA to arrive merges them (alone when its copy is small, else sharing
-//     row slices with the pair's CTAs that are still waiting).
+//     folded rows through distributed shared memory. Otherwise partials are
+//     published in the workspace with an acquire-release arrival. When a
+//     pair's merge is small, every segment takes a ticket as its stream ends
+//     and the segment holding the last ticket merges alone: it keeps its own
+//     folded rows in shared memory and waits only for the publications of
+//     segments that took their tickets before it (so are past their streams
+//     and wait on nothing). Larger merges go to the pair's last CTA to
+//     arrive, which shares row slices with the pair's CTAs still waiting.
 // Rows past R are padding: zero query rows whose outputs are never read.
 #include <atomic>
 
@@ -109,6 +113,7 @@ constexpr int kMergeRowBytes = TD * 4 + 8;  // a partial row's o and (m, l)
 constexpr int kMaxCluster = 16;  // CTAs per pair in the cluster merge
 constexpr int kMinCluster = 4;   // smallest cluster the plan uses
 constexpr size_t kSoloMergeBytes = 128 * 1024;  // see launch_attend_tc
+constexpr int kTicketWord = 1;  // word of a pair's attention count line holding merge tickets
 
 // Log-sum-exp combine of rows [r0, r0 + nv) of one pair from partials staged
 // in shared memory: o at so[(s * ld + r) * TD], (m, l) at sml[s * ld + r] for
@@ -164,6 +169,22 @@ __device__ __forceinline__ void combine_rows(const AttendArgs& a, int b, int h, 
       *reinterpret_cast<uint2*>(dst + (cg + 8 * i) * 4) = u;
     }
   }
+}
+
+// Bounded wait (thread scope, acquire at device scope) until the low 16 bits
+// of *w reach `need`: false after kWaitBudgetNs, with `site` recorded in
+// status[1].
+__device__ __forceinline__ bool wait_count_at_least(const unsigned* w, unsigned need,
+                                                    unsigned* status, unsigned site) {
+  if ((load_acquire(w) & 0xFFFFu) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while ((load_acquire(w) & 0xFFFFu) < need) {
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      atomicMax(status + 1, site);
+      return false;
+    }
+  }
+  return true;
 }
 
 // The work of one CTA: up to kMaxSeg segments, each a run of consecutive work
@@ -258,13 +279,13 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // warp-uniform indices (per-lane indices into it would serialize)
   __shared__ unsigned long long s_anc[kMaxT];
 
-  const SegPlan sp = plan_segments(a);
+  // the CTA's segments, in shared memory: read again after the stream, where
+  // a per-thread copy would come back from local memory through L2
+  __shared__ SegPlan s_plan;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = sp.n > 0 ? sp.u1[0] - sp.u0[0] : 0;
-  const int ntot = n0 + (sp.n > 1 ? sp.u1[1] - sp.u0[1] : 0);
-  auto seg_of = [&](int i) { return i < n0 ? 0 : 1; };
 
   if (threadIdx.x == 0) {
+    s_plan = plan_segments(a);
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
@@ -298,6 +319,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  const SegPlan& sp = s_plan;
+  const int n0 = sp.n > 0 ? sp.u1[0] - sp.u0[0] : 0;
+  const int ntot = n0 + (sp.n > 1 ? sp.u1[1] - sp.u0[1] : 0);
+  auto seg_of = [&](int i) { return i < n0 ? 0 : 1; };
   const uint32_t tmem = *tmem_slot;
   if (warp == PRODUCER) {
     // warm L2 with this CTA's block-table rows while earlier kernels finish
@@ -388,6 +413,11 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // per-thread results of the final segment for the epilogue (softmax threads)
   float o_row[TD];
   float m_run = -INFINITY, l_run = 0.f;
+  // Narrow merges (the last CTA of a pair merges every row) go by tickets: a
+  // segment takes its pair's ticket when its stream ends, and the segment
+  // holding the last ticket merges; the others publish their partials.
+  const bool ticketed = a.merge_wait_ns == 0 && !a.cluster_merge;
+  unsigned final_ticket = 0u;  // thread 0: the final segment's ticket
 
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
@@ -536,9 +566,15 @@ __global__ void __launch_bounds__(32 * 10, 1)
     if (lane == 0 && sp.n > 1) {
       if (!mbar_wait_abortable(smem_u32(mid_done), 0, abort_flag, a.status, 12u))
         atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-      // the last arrival sees the pair complete (and acquires its partials)
-      if ((arrive_acq_rel(&a.counters[sp.pair[0] * kPairWords]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0])
+      // the last arrival sees the pair complete (and acquires its partials);
+      // with tickets, the last ticket merges (after every publication)
+      unsigned* w = a.counters + sp.pair[0] * kPairWords;
+      const unsigned pub = arrive_acq_rel(w);
+      if (ticketed) {
+        if (atomicAdd(w + kTicketWord, 1u) + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
+      } else if ((pub & 0xFFFFu) + 1u == (unsigned)sp.nseg[0]) {
         pair_done[0] = 1;
+      }
     }
   } else if (warp == MMAW) {
     // ------------------------------------------------------------ MMA issue
@@ -728,6 +764,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&p_ready[X]));
       }
+      // the final segment's ticket, taken as its stream ends: the atomic's
+      // round trip overlaps the read-out and staging below
+      if (ticketed && threadIdx.x == 0 && j == sp.n - 1)
+        final_ticket = atomicAdd(&a.counters[sp.pair[j] * kPairWords + kTicketWord], 1u);
       // read out this set's O of segment j (its last P.V must have finished)
       bool fin = ok && kseg > 0;
       if (fin)
@@ -806,7 +846,13 @@ __global__ void __launch_bounds__(32 * 10, 1)
             make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
       *reinterpret_cast<float2*>(pml + 2 * row) = make_float2(m_run, l_run);
     }
+    // holding the pair's last ticket: merge with this partial kept here
+    if (threadIdx.x == 0 && ticketed && final_ticket + 1u == (unsigned)sp.nseg[jf])
+      pair_done[jf] = 2;
     __syncthreads();
+    // the folded partial stays in shared memory for a cluster merge or for
+    // this CTA's own merge
+    const bool keep = a.cluster_merge || pair_done[jf] == 2;
     // per-row weights of the two sets (w_X = 2^(m_X - M)) and the folded (M, L)
     float* pw = pml + (size_t)4 * KR;  // [KR][2]
     for (int rr = threadIdx.x; rr < KR; rr += NT) {
@@ -816,14 +862,14 @@ __global__ void __launch_bounds__(32 * 10, 1)
       const float wa = (ma.x == -INFINITY) ? 0.f : exp2f(ma.x - M);
       const float wb = (mb.x == -INFINITY) ? 0.f : exp2f(mb.x - M);
       *reinterpret_cast<float2*>(pw + 2 * rr) = make_float2(wa, wb);
-      if (a.cluster_merge)
+      if (keep)
         *reinterpret_cast<float2*>(cml + 2 * rr) = make_float2(M, wa * ma.y + wb * mb.y);
       else if (rr < a.rpad)
         own_ml[rr] = make_float2(M, wa * ma.y + wb * mb.y);
     }
     __syncthreads();
-    if (a.cluster_merge) {
-      // folded rows in place of set A's staged rows, for the cluster merge
+    if (keep) {
+      // folded rows in place of set A's staged rows
       for (int idx = threadIdx.x; idx < KR * (TD / 4); idx += NT) {
         const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
         const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
@@ -835,7 +881,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
       }
     }
     // folded rows straight to the workspace (rows past kRows are zero padding)
-    for (int idx = threadIdx.x; !a.cluster_merge && idx < a.rpad * (TD / 4); idx += NT) {
+    for (int idx = threadIdx.x; !keep && idx < a.rpad * (TD / 4); idx += NT) {
       const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (rr < KR) {
@@ -848,13 +894,13 @@ __global__ void __launch_bounds__(32 * 10, 1)
       *reinterpret_cast<float4*>(own_o + (size_t)rr * TD + c4) = v;
     }
     // CTA barrier, then one thread's acquire-release arrival publishes
-    // every thread's partial writes (the barrier orders them before it); the
-    // arrival that completes a pair also acquires the other partials. (A
-    // mid-stream segment arrived from the producer warp.)
+    // every thread's partial writes (the barrier orders them before it);
+    // without tickets the arrival that completes a pair also acquires the
+    // other partials. (A mid-stream segment arrived from the producer warp.)
     __syncthreads();
-    if (threadIdx.x == 0 && !a.cluster_merge) {
-      if ((arrive_acq_rel(&a.counters[pair * kPairWords]) & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf])
-        pair_done[jf] = 1;
+    if (threadIdx.x == 0 && !keep) {
+      const unsigned pub = arrive_acq_rel(&a.counters[pair * kPairWords]);
+      if (!ticketed && (pub & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf]) pair_done[jf] = 1;
     }
   }
   __syncthreads();
@@ -927,28 +973,54 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // pair holds its arrivals (low 16 bits) and the CTAs that finished their
   // merge share (high bits).
   uint32_t mphase = 0;
-  // bulk-copy rows [r0, r0 + nr) of the ns partial slots of `pair` into the
-  // ring (nr even, so every (m, l) copy is a multiple of 16 bytes) and
-  // combine rows [r0, r0 + nv) into out
-  auto merge_rows = [&](int pair, int ns, int r0, int nr, int nv) {
+  // Staging of merge passes: with tickets it starts past the final
+  // segment's folded partial (po, cml), which a merge may still read.
+  const int stage_off = ticketed ? 2 * KR * OST + 8 * KR : 0;
+  // bulk-copy rows [r0, r0 + nr) of the ns partial slots of `pair` (all but
+  // slot `kept`, whose folded rows are in po and cml) into the ring (nr
+  // even, so every (m, l) copy is a multiple of 16 bytes) and combine rows
+  // [r0, r0 + nv) into out. With `pub`, the copies wait until its count
+  // reaches `need` (acquire), while the other warps place the kept slot.
+  auto merge_rows = [&](int pair, int ns, int r0, int nr, int nv, int kept, const unsigned* pub,
+                        unsigned need) {
     const size_t pbase = (size_t)pair * a.slot_stride * a.rpad;
-    float* so = reinterpret_cast<float*>(ring);                           // [ns][nr][TD]
+    float* so = reinterpret_cast<float*>(ring) + stage_off;               // [ns][nr][TD]
     float2* sml = reinterpret_cast<float2*>(so + (size_t)ns * nr * TD);   // [ns][nr]
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
+      if (pub && threadIdx.x == 0 && !wait_count_at_least(pub, need, a.status, 14u))
+        atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
+      __syncwarp();  // the acquire above orders the warp's copies
       // the partials were written by other CTAs through the generic proxy
-      // and acquired through the count word; order that before the copy
-      // engine reads them
+      // and acquired through the count word, and the staging area was last
+      // used through the generic proxy; order both before the copy engine
+      // runs. Lane 0 posts the byte count, then lane s issues slot s's copies.
       asm volatile("fence.proxy.async.global;" ::: "memory");
       fence_async_smem();
       const uint32_t mb = smem_u32(merge_bar);
-      mbar_arrive_expect_tx(mb, (uint32_t)(ns * nr * kMergeRowBytes));
-      for (int sl = 0; sl < ns; ++sl) {
+      const int ncopy = ns - (kept >= 0 ? 1 : 0);
+      if (threadIdx.x == 0) mbar_arrive_expect_tx(mb, (uint32_t)(ncopy * nr * kMergeRowBytes));
+      __syncwarp();
+      for (int sl = threadIdx.x; sl < ns; sl += 32) {
+        if (sl == kept) continue;
         const size_t row0 = pbase + (size_t)sl * a.rpad + r0;
         bulk_load(smem_u32(so + (size_t)sl * nr * TD), a.part_o + row0 * TD, (uint32_t)(nr * TD * 4),
                   mb);
         bulk_load(smem_u32(sml + (size_t)sl * nr), a.part_ml + row0 * 2, (uint32_t)(nr * 8), mb);
       }
     }
+    if (kept >= 0) {
+      // this CTA's own slot: its folded rows, copied into place by warps
+      // 1.. while warp 0 waits and the other slots land
+      float* ko = so + (size_t)kept * nr * TD;
+      for (int idx = threadIdx.x - 32; idx >= 0 && idx < nr * (TD / 4); idx += NT - 32) {
+        const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
+        *reinterpret_cast<float4*>(ko + rr * TD + c4) =
+            *reinterpret_cast<const float4*>(po + (r0 + rr) * OST + c4);
+      }
+      for (int rr = threadIdx.x - 32; rr >= 0 && rr < nr; rr += NT - 32)
+        sml[(size_t)kept * nr + rr] = reinterpret_cast<const float2*>(cml)[r0 + rr];
+    }
+    __syncthreads();  // the kept slot is in place; warp 0 has issued every copy
     if (!mbar_wait_drain(smem_u32(merge_bar), mphase) && threadIdx.x == 0)
       atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
     mphase ^= 1u;
@@ -970,28 +1042,40 @@ __global__ void __launch_bounds__(32 * 10, 1)
   for (int j = 0; j < sp.n; ++j) {
     const int pair = sp.pair[j];
     const int nseg = sp.nseg[j], ns = nseg + sp.mid[j];
-    const int nsl = nseg < 32 ? nseg : 32;
-    const int share = ((a.R + nsl - 1) / nsl + 1) & ~1;
-    // rows per pass that the ring holds for ns slots (even; two always fit)
-    int rpp = (C::kRing / (ns * kMergeRowBytes)) & ~1;
+    // rows per pass that the ring holds for ns slots (even; two always fit:
+    // wide merges stage from the ring's start, and a narrow merge's slots
+    // are few enough to fit past the folded partial)
+    int rpp = ((C::kRing - stage_off * 4) / (ns * kMergeRowBytes)) & ~1;
     rpp = rpp < 2 ? 2 : (rpp > a.rpad ? a.rpad : rpp);
     // rows [r0, r1) (r0 even) in passes of rpp rows
-    auto merge_range = [&](int r0, int r1) {
+    auto merge_range = [&](int r0, int r1, int kept, const unsigned* pub, unsigned need) {
       for (int q0 = r0; q0 < r1; q0 += rpp) {
         const int nv = min(rpp, r1 - q0);
-        merge_rows(pair, ns, q0, min((nv + 1) & ~1, a.rpad - q0), nv);
+        merge_rows(pair, ns, q0, min((nv + 1) & ~1, a.rpad - q0), nv, kept, q0 == r0 ? pub : nullptr,
+                   need);
       }
     };
-    const bool last = pair_done[j] != 0;  // the same in every thread
-    if (a.merge_wait_ns == 0) {
-      // the last CTA merges every row; the others have left the pair's
-      // words alone since their arrival, so it may zero them at once
-      if (last) {
-        merge_range(0, a.R);
-        if (threadIdx.x == 0) a.counters[pair * kPairWords] = 0u;
+    const int pd = pair_done[j];  // the same in every thread
+    if (ticketed) {
+      // The narrow merge, by the pair's last ticket. Every other segment took
+      // its ticket earlier, so it is past its stream and publishes without
+      // waiting for anything: wait for those publications (every segment's,
+      // or all but this one's when its partial stayed here), merge every
+      // row, and return the pair's words to zero (nothing else touches them
+      // any more).
+      if (pd) {
+        unsigned* w = a.counters + pair * kPairWords;
+        merge_range(0, a.R, pd == 2 ? sp.slot[j] : -1, w, (unsigned)(pd == 2 ? nseg - 1 : nseg));
+        if (threadIdx.x == 0) {
+          w[0] = 0u;
+          w[kTicketWord] = 0u;
+        }
       }
       continue;
     }
+    const bool last = pd != 0;
+    const int nsl = nseg < 32 ? nseg : 32;
+    const int share = ((a.R + nsl - 1) / nsl + 1) & ~1;
     const int own = sp.slot[j] < nsl ? sp.slot[j] : -1;
     if (threadIdx.x == 0) {
       int got = 0;
@@ -1013,7 +1097,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
       *merge_got = got;
     }
     __syncthreads();
-    if (*merge_got) merge_range(min(a.R, own * share), min(a.R, (own + 1) * share));
+    if (*merge_got) merge_range(min(a.R, own * share), min(a.R, (own + 1) * share), -1, nullptr, 0u);
     if (last) {
       if (threadIdx.x == 0) {
         const unsigned all = nsl == 32 ? 0xFFFFFFFFu : ((1u << nsl) - 1u);
@@ -1030,7 +1114,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         }
         int e = q + 1;
         while (e < nsl && (mine & (1u << e))) ++e;
-        merge_range(min(a.R, q * share), min(a.R, e * share));
+        merge_range(min(a.R, q * share), min(a.R, e * share), -1, nullptr, 0u);
         q = e;
       }
     }
@@ -1163,7 +1247,14 @@ int attend_tc_cluster(const AttendArgs& a, int pairs) {
 }
 
 bool attend_tc_narrow_merge(int slot_stride, int rpad) {
-  return (size_t)slot_stride * rpad * kMergeRowBytes <= kSoloMergeBytes;
+  // A narrow merge stages its passes past the merging CTA's folded partial:
+  // two rows of every slot must fit there (they always do under the size
+  // rule; checked rather than assumed).
+  const int kr = rpad <= 32 ? 32 : rpad <= 64 ? 64 : 128;
+  const size_t folded = ((size_t)2 * kr * TcCfg<4, 6>::kOst + 8 * kr) * 4;
+  const size_t room = TcCfg<4, 6>::kRing - folded;
+  return (size_t)slot_stride * rpad * kMergeRowBytes <= kSoloMergeBytes &&
+         (size_t)2 * slot_stride * kMergeRowBytes <= room;
 }
 
 int attend_tc_ctas_per_sm(const AttendArgs& a) {
