@@ -619,7 +619,10 @@ def run_gpu(args, wl, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": f["attend_gbs"], "peak": f["peak"],
                      "unit": "GB/s", "frac": f["attend_frac"], "traffic": traffic,
                      "kernel": {api.SV_PATH_TCGEN05: "attend_tc_kernel (tcgen05 split-KV "
-                                "attention, LSE merge by the last CTA of each pair)",
+                                "attention, LSE merge in the same launch: "
+                                + ("through distributed shared memory, one cluster per pair"
+                                   if plan.cluster else "by the CTA holding each pair's last "
+                                   "ticket") + ")",
                                 api.SV_PATH_MMA_SYNC: "attend_fast_kernel (mma.sync split-KV)",
                                 api.SV_PATH_CUDA_CORES: "attend_generic_kernel + merge_kernel"
                                 }[plan.path],

@@ -569,10 +569,10 @@ __global__ void __launch_bounds__(32 * 10, 1)
       // the last arrival sees the pair complete (and acquires its partials);
       // with tickets, the last ticket merges (after every publication)
       unsigned* w = a.counters + sp.pair[0] * kPairWords;
-      const unsigned pub = arrive_acq_rel(w);
       if (ticketed) {
+        arrive_release(w);
         if (atomicAdd(w + kTicketWord, 1u) + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
-      } else if ((pub & 0xFFFFu) + 1u == (unsigned)sp.nseg[0]) {
+      } else if ((arrive_acq_rel(w) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0]) {
         pair_done[0] = 1;
       }
     }
@@ -899,8 +899,11 @@ __global__ void __launch_bounds__(32 * 10, 1)
     // other partials. (A mid-stream segment arrived from the producer warp.)
     __syncthreads();
     if (threadIdx.x == 0 && !keep) {
-      const unsigned pub = arrive_acq_rel(&a.counters[pair * kPairWords]);
-      if (!ticketed && (pub & 0xFFFFu) + 1u == (unsigned)sp.nseg[jf]) pair_done[jf] = 1;
+      if (ticketed)
+        arrive_release(&a.counters[pair * kPairWords]);
+      else if ((arrive_acq_rel(&a.counters[pair * kPairWords]) & 0xFFFFu) + 1u ==
+               (unsigned)sp.nseg[jf])
+        pair_done[jf] = 1;
     }
   }
   __syncthreads();

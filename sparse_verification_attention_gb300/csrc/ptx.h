@@ -111,6 +111,13 @@ __device__ __forceinline__ unsigned arrive_acq_rel(unsigned* ctr) {
   return old;
 }
 
+// Count one arrival with release semantics at device scope, without waiting
+// for the old value: every store that happens before it is visible to a
+// thread whose acquire load sees the count.
+__device__ __forceinline__ void arrive_release(unsigned* ctr) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
 // Load with acquire semantics at device scope.
 __device__ __forceinline__ unsigned load_acquire(const unsigned* p) {
   unsigned v;
