@@ -29,7 +29,8 @@
 //     tokens, K=128), then after softmax O += P_i V_i with P read from TMEM
 //     (M=128, N=128, K=64, V as an MN-major operand); the first P.V of each
 //     softmax set in a segment starts a fresh accumulator; stages are
-//     released by tcgen05 commits.
+//     released by tcgen05 commits. It polls its barriers with test_wait
+//     (never suspended), so it issues as soon as a hand-off lands.
 //   * two softmax sets: set A takes the even tiles, set B the odd ones, each
 //     with its own S, P and O in TMEM, so two independent softmax chains
 //     overlap. In each set the warp owning TMEM lane quarter q holds stacked
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         // S buffer of unit i+1's set is free: its previous reader (softmax of
         // unit i-1) arrived on p_ready before PV(i-1) was issued
         if (i + 1 < ntot) {
-          if (!mbar_wait_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
+          if (!mbar_spin_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
                                    5u)) {
             ok = false;
             break;
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
         }
         // p_ready also says the set has read out its previous segment's O, so
         // the first P.V of a segment may overwrite it
-        if (!mbar_wait_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
+        if (!mbar_spin_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
           ok = false;
           break;
         }

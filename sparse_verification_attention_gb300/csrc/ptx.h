@@ -50,6 +50,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase of an mbarrier (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on a phase of an mbarrier: false after `limit` polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i)
@@ -87,6 +100,30 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parit
         atomicMax(status + 1, site);
       }
       return false;
+    }
+  }
+}
+
+// mbar_wait_abortable polling with test_wait: the thread is never suspended,
+// so it sees the phase complete as soon as the barrier does (the abort flag
+// and the clock are checked every 64 polls).
+__device__ __forceinline__ bool mbar_spin_abortable(uint32_t bar, uint32_t parity,
+                                                    volatile int* abort, unsigned* status,
+                                                    unsigned site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 63u) == 0u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+        *abort = 1;
+        if (status) {
+          atomicOr(status, SV_FLAG_WAIT_TIMEOUT);
+          atomicMax(status + 1, site);
+        }
+        return false;
+      }
     }
   }
 }
