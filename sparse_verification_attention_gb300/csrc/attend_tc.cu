@@ -25,12 +25,13 @@
 //     (128-byte swizzle, L2 evict-first) of the page's K and V tiles into the
 //     ring; the draft tile (the pair's draft K/V rows) comes the same way,
 //     through a 4-D map over the draft tensors.
-//   * MMA warp (one elected lane): S_i = Q K_i^T into TMEM (M=128 rows, N=64
-//     tokens, K=128), then after softmax O += P_i V_i with P read from TMEM
-//     (M=128, N=128, K=64, V as an MN-major operand); the first P.V of each
-//     softmax set in a segment starts a fresh accumulator; stages are
-//     released by tcgen05 commits. It polls its barriers with test_wait
-//     (never suspended), so it issues as soon as a hand-off lands.
+//   * MMA issue (one elected lane; for 128-row tiles one per softmax set, in
+//     two warps): S_i = Q K_i^T into TMEM (M=128 rows, N=64 tokens, K=128),
+//     then after softmax O += P_i V_i with P read from TMEM (M=128, N=128,
+//     K=64, V as an MN-major operand); the first P.V of each softmax set in
+//     a segment starts a fresh accumulator; stages are released by tcgen05
+//     commits. The issuers poll their barriers with test_wait (never
+//     suspended), so each issues as soon as a hand-off lands.
 //   * two softmax sets: set A takes the even tiles, set B the odd ones, each
 //     with its own S, P and O in TMEM, so two independent softmax chains
 //     overlap. In each set the warp owning TMEM lane quarter q holds stacked
@@ -66,6 +67,10 @@ constexpr int kBoxBytes = TBLK * 128;         // one 64-column box of a tile
 constexpr int kTileBytes = 2 * kBoxBytes;     // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V, 32 KB
 constexpr uint32_t kTmemCols = 512;
+// threads per CTA: 8 softmax warps (two sets of four), the producer warp and
+// an MMA-issuing warp, plus a second MMA-issuing warp for 128-row tiles
+// (NSW = 4: one issuer per softmax set)
+__host__ __device__ constexpr int cta_threads(int nsw) { return nsw == 4 ? 32 * 11 : 32 * 10; }
 // TMEM columns of set X in {0, 1}: S (64 fp32), O (128 fp32), P (32 x bf16x2)
 __host__ __device__ constexpr uint32_t col_s(int x) { return x ? 64u : 0u; }
 __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 256u : 128u; }
@@ -84,7 +89,7 @@ constexpr int r1024(int x) { return (x + 1023) / 1024 * 1024; }
 
 template <int NSW, int NS>
 struct TcCfg {
-  static constexpr int kThreads = 32 * 10;        // 8 softmax + producer + MMA
+  static constexpr int kThreads = cta_threads(NSW);
   static constexpr int kRows = 32 * NSW;          // stacked rows held in TMEM lanes (>= R)
   static constexpr int kQBox = 128 * 128;         // one 64-column Q box, 128 rows
   static constexpr int kQBytes = 2 * kQBox;       // the first segment's Q operand
@@ -122,9 +127,9 @@ constexpr int kTicketWord = 1;  // word of a pair's attention count line holding
 // float4 columns, so every load of a slot is independent of the others;
 // the weights are formed in place (slot order, so the sums do not depend on
 // which CTA merges). All threads of the CTA call it.
+template <int NT>
 __device__ __forceinline__ void combine_rows(const AttendArgs& a, int b, int h, int ns, int ld,
                                              int r0, int nv, const float* so, const float2* sml) {
-  constexpr int NT = 32 * 10;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
   const int cg = threadIdx.x & 7;
   for (int r = threadIdx.x >> 3; r < nv; r += NT / 8) {
@@ -250,12 +255,12 @@ __device__ SegPlan plan_segments(const AttendArgs& a) {
 }
 
 template <int NSW, int NS>
-__global__ void __launch_bounds__(32 * 10, 1)
+__global__ void __launch_bounds__(cta_threads(NSW), 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDK,
                      const __grid_constant__ CUtensorMap tmDV, const __grid_constant__ AttendArgs a) {
   using C = TcCfg<NSW, NS>;
-  constexpr int PRODUCER = 8, MMAW = 9;
+  constexpr int PRODUCER = 8, MMAW = 9, MMAW2 = 10;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
       mbar_init(smem_u32(&p_ready[i]), NSW);
       mbar_init(smem_u32(&o_done[i]), 1);
     }
-    mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(mma_done), NSW == 4 ? 2 : 1);  // one arrival per MMA issuer
     mbar_init(smem_u32(q_ready), 5);  // producer's expect_tx + 4 zeroing warps
     mbar_init(smem_u32(q1_ready), 4);
     mbar_init(smem_u32(mid_done), 2 * NSW);
@@ -577,9 +582,21 @@ __global__ void __launch_bounds__(32 * 10, 1)
         pair_done[0] = 1;
       }
     }
-  } else if (warp == MMAW) {
+  } else if (warp == MMAW || warp == MMAW2) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0 && ntot > 0) {
+    // A tcgen05.mma takes its issuing thread tens of cycles (about 40 ns for
+    // the N=64 S steps), which makes MMA issue the per-tile limit.
+    // - 128-row tiles (NSW = 4): one issuing thread per softmax set (warp
+    //   MMAW + X issues set X's tiles X, X+2, ...), so neither set's chain
+    //   (S -> softmax -> P.V -> next S) waits behind the other's P
+    //   (measured: 37.6 -> 36.7 us at 128 rows).
+    // - Fewer rows: one thread issues both sets in tile order, S(i+1) ahead
+    //   of P.V(i); with two issuers these shapes were 3-7% slower, the two
+    //   chains contending for the tensor pipe.
+    // tcgen05.commit tracks the issuing thread's own MMAs.
+    constexpr bool kSplitIssue = NSW == 4;
+    const int X = warp - MMAW;  // split issue: the set this thread issues
+    if (lane == 0 && ntot > 0 && (kSplitIssue || warp == MMAW)) {
       constexpr uint32_t idq = tc::idesc_bf16(128, 64, false, false);
       constexpr uint32_t idp = tc::idesc_bf16(128, TD, false, true);
       const uint32_t rb = smem_u32(ring);
@@ -588,71 +605,111 @@ __global__ void __launch_bounds__(32 * 10, 1)
       // tile i (its set is i & 1) lives in ring stage rs(i) with phase rp(i)
       auto rs = [&](int t) { return t % NS; };
       auto rp = [&](int t) { return (uint32_t)((t / NS) & 1); };
+      // Descriptors built once: a descriptor's address field is the byte
+      // address >> 4, so a stage or k-step offset (a multiple of 16 bytes,
+      // inside shared memory) is added to it directly.
+      const uint64_t dq0 = tc::smem_desc(qb, 16, 1024);                      // Q (segment 0)
+      const uint64_t dk0 = tc::smem_desc(rb, 16, 1024);                      // K of stage 0
+      const uint64_t dv0 = tc::smem_desc(rb + kTileBytes, kBoxBytes, 1024);  // V of stage 0
+      auto stage_off = [&](int t) { return (uint64_t)(rs(t) * (kStageBytes >> 4)); };
       auto issue_qk = [&](int i) {
-        const uint32_t kb = rb + rs(i) * kStageBytes;
+        const uint64_t dk = dk0 + stage_off(i);
         const uint32_t d = tmem + col_s(i & 1);
         if (seg_of(i) == 0) {
 #pragma unroll
           for (int kk = 0; kk < TD / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc(qb + (kk >> 2) * C::kQBox + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t ad = dq0 + (uint64_t)(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4);
+            const uint64_t bd = dk + (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
             tc::mma_ss(d, ad, bd, idq, kk > 0 ? 1u : 0u);
           }
         } else {
           // second segment: A = Q from TMEM (16 dims = 8 columns per k-step)
 #pragma unroll
           for (int kk = 0; kk < TD / 16; ++kk) {
-            const uint64_t bd = tc::smem_desc(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = dk + (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
             tc::mma_ts(d, tmem + kColQ1 + kk * 8, bd, idq, kk > 0 ? 1u : 0u);
           }
         }
         tc::commit(smem_u32(&s_full[i & 1]));
       };
-      bool ok = mbar_wait_abortable(smem_u32(q_ready), 0, abort_flag, a.status, 3u) &&
-                mbar_wait_abortable(smem_u32(&full[rs(0)]), rp(0), abort_flag, a.status, 4u);
-      tc::fence_after();
-      if (ok) issue_qk(0);
-      for (int i = 0; ok && i < ntot; ++i) {
-        // S buffer of unit i+1's set is free: its previous reader (softmax of
-        // unit i-1) arrived on p_ready before PV(i-1) was issued
-        if (i + 1 < ntot) {
-          if (!mbar_spin_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
-                                   5u)) {
-            ok = false;
-            break;
-          }
-          if (seg_of(i + 1) == 1 && !q1_seen) {
-            if (!mbar_wait_abortable(smem_u32(q1_ready), 0, abort_flag, a.status, 7u)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after();
-            q1_seen = true;
-          }
-          issue_qk(i + 1);
-        }
-        // p_ready also says the set has read out its previous segment's O, so
-        // the first P.V of a segment may overwrite it
-        if (!mbar_spin_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
+      auto issue_pv = [&](int i) {
         const int first = seg_of(i) ? n0 : 0;  // the segment's first tile
-        const uint32_t vb = rb + rs(i) * kStageBytes + kTileBytes;
+        const uint64_t dv = dv0 + stage_off(i);
         const uint32_t pa = tmem + col_p(i & 1);
 #pragma unroll
         for (int kt = 0; kt < TBLK / 16; ++kt) {
           // V tile as an MN-major operand: 64 head dims per 128-byte row (the
           // next 64 dims one box further, LBO), 8 tokens per 1024-byte group
           // (SBO); each k-step covers 16 tokens = two groups.
-          const uint64_t bd = tc::smem_desc(vb + kt * 2048, kBoxBytes, 1024);
+          const uint64_t bd = dv + (uint64_t)((kt * 2048) >> 4);
           tc::mma_ts(tmem + col_o(i & 1), pa + kt * 8, bd, idp, (i - first >= 2 || kt > 0) ? 1u : 0u);
         }
         tc::commit(smem_u32(&empty[rs(i)]));
         tc::commit(smem_u32(&o_done[i & 1]));
+      };
+      bool ok = mbar_wait_abortable(smem_u32(q_ready), 0, abort_flag, a.status, 3u);
+      if constexpr (kSplitIssue) {
+        for (int i = X; ok && i < ntot; i += 2) {
+          // S(i): the tile has landed, and the set's S buffer is free (its
+          // previous reader arrived on p_ready before this thread's last P.V)
+          if (!mbar_spin_abortable(smem_u32(&full[rs(i)]), rp(i), abort_flag, a.status, 5u)) {
+            ok = false;
+            break;
+          }
+          if (seg_of(i) == 1 && !q1_seen) {
+            if (!mbar_wait_abortable(smem_u32(q1_ready), 0, abort_flag, a.status, 7u)) {
+              ok = false;
+              break;
+            }
+            q1_seen = true;
+          }
+          tc::fence_after();
+          issue_qk(i);
+          // p_ready also says the set has read out its previous segment's O,
+          // so the first P.V of a segment may overwrite it
+          if (!mbar_spin_abortable(smem_u32(&p_ready[X]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          issue_pv(i);
+        }
+      } else {
+        ok = ok && mbar_spin_abortable(smem_u32(&full[rs(0)]), rp(0), abort_flag, a.status, 4u);
+        tc::fence_after();
+        if (ok) issue_qk(0);
+        for (int i = 0; ok && i < ntot; ++i) {
+          // S buffer of unit i+1's set is free: its previous reader (softmax of
+          // unit i-1) arrived on p_ready before PV(i-1) was issued
+          if (i + 1 < ntot) {
+            if (!mbar_spin_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
+                                     5u)) {
+              ok = false;
+              break;
+            }
+            if (seg_of(i + 1) == 1 && !q1_seen) {
+              if (!mbar_wait_abortable(smem_u32(q1_ready), 0, abort_flag, a.status, 7u)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after();
+              q1_seen = true;
+            }
+            issue_qk(i + 1);
+          }
+          // p_ready also says the set has read out its previous segment's O, so
+          // the first P.V of a segment may overwrite it
+          if (!mbar_spin_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status,
+                                   6u)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          issue_pv(i);
+        }
       }
       // tensor memory is released only after every issued MMA has finished
+      // (every issuer arrives; one with no tiles arrives at once)
       tc::commit(smem_u32(mma_done));
       mbar_wait_drain(smem_u32(mma_done), 0);
     }
@@ -827,7 +884,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
   // The final segment: stage both sets' (o, m, l) for the kRows real lanes and
   // fold set B into set A with log-sum-exp weights (row r of set X staged at
   // X*kRows + r).
-  constexpr int NT = 32 * 10;
+  constexpr int NT = C::kThreads;
   constexpr int OST = C::kOst;
   constexpr int KR = C::kRows;
   float* po = reinterpret_cast<float*>(ring);   // [2*KR][OST]
@@ -1028,7 +1085,7 @@ __global__ void __launch_bounds__(32 * 10, 1)
     if (!mbar_wait_drain(smem_u32(merge_bar), mphase) && threadIdx.x == 0)
       atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
     mphase ^= 1u;
-    combine_rows(a, pair / a.Hkv, pair % a.Hkv, ns, nr, r0, nv, so, sml);
+    combine_rows<NT>(a, pair / a.Hkv, pair % a.Hkv, ns, nr, r0, nv, so, sml);
     __syncthreads();  // the next copies overwrite the staging area
   };
   // Row slices of a pair, merged in parallel by the pair's CTAs: slice q
