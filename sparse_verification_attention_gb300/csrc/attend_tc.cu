@@ -25,13 +25,14 @@
 //     (128-byte swizzle, L2 evict-first) of the page's K and V tiles into the
 //     ring; the draft tile (the pair's draft K/V rows) comes the same way,
 //     through a 4-D map over the draft tensors.
-//   * MMA issue (one elected lane; for 128-row tiles one per softmax set, in
-//     two warps): S_i = Q K_i^T into TMEM (M=128 rows, N=64 tokens, K=128),
-//     then after softmax O += P_i V_i with P read from TMEM (M=128, N=128,
-//     K=64, V as an MN-major operand); the first P.V of each softmax set in
-//     a segment starts a fresh accumulator; stages are released by tcgen05
-//     commits. The issuers poll their barriers with test_wait (never
-//     suspended), so each issues as soon as a hand-off lands.
+//   * MMA issue, split by role over two warps (one elected lane each): one
+//     issues every S_i = Q K_i^T into TMEM (M=128 rows, N=64 tokens, K=128),
+//     the other, after softmax, every O += P_i V_i with P read from TMEM
+//     (M=128, N=128, K=64, V as an MN-major operand); the first P.V of each
+//     softmax set in a segment starts a fresh accumulator; stages are
+//     released by tcgen05 commits. The issuers poll their barriers with
+//     test_wait (never suspended), so each issues as soon as a hand-off
+//     lands.
 //   * two softmax sets: set A takes the even tiles, set B the odd ones, each
 //     with its own S, P and O in TMEM, so two independent softmax chains
 //     overlap. In each set the warp owning TMEM lane quarter q holds stacked
@@ -68,9 +69,8 @@ constexpr int kTileBytes = 2 * kBoxBytes;     // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V, 32 KB
 constexpr uint32_t kTmemCols = 512;
 // threads per CTA: 8 softmax warps (two sets of four), the producer warp and
-// an MMA-issuing warp, plus a second MMA-issuing warp for 128-row tiles
-// (NSW = 4: one issuer per softmax set)
-__host__ __device__ constexpr int cta_threads(int nsw) { return nsw == 4 ? 32 * 11 : 32 * 10; }
+// two MMA-issuing warps (one issues every S, the other every P.V)
+constexpr int kCtaThreads = 32 * 11;
 // TMEM columns of set X in {0, 1}: S (64 fp32), O (128 fp32), P (32 x bf16x2)
 __host__ __device__ constexpr uint32_t col_s(int x) { return x ? 64u : 0u; }
 __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 256u : 128u; }
@@ -89,7 +89,7 @@ constexpr int r1024(int x) { return (x + 1023) / 1024 * 1024; }
 
 template <int NSW, int NS>
 struct TcCfg {
-  static constexpr int kThreads = cta_threads(NSW);
+  static constexpr int kThreads = kCtaThreads;
   static constexpr int kRows = 32 * NSW;          // stacked rows held in TMEM lanes (>= R)
   static constexpr int kQBox = 128 * 128;         // one 64-column Q box, 128 rows
   static constexpr int kQBytes = 2 * kQBox;       // the first segment's Q operand
@@ -255,7 +255,7 @@ __device__ SegPlan plan_segments(const AttendArgs& a) {
 }
 
 template <int NSW, int NS>
-__global__ void __launch_bounds__(cta_threads(NSW), 1)
+__global__ void __launch_bounds__(kCtaThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDK,
                      const __grid_constant__ CUtensorMap tmDV, const __grid_constant__ AttendArgs a) {
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(cta_threads(NSW), 1)
       mbar_init(smem_u32(&p_ready[i]), NSW);
       mbar_init(smem_u32(&o_done[i]), 1);
     }
-    mbar_init(smem_u32(mma_done), NSW == 4 ? 2 : 1);  // one arrival per MMA issuer
+    mbar_init(smem_u32(mma_done), 2);  // one arrival per MMA issuer
     mbar_init(smem_u32(q_ready), 5);  // producer's expect_tx + 4 zeroing warps
     mbar_init(smem_u32(q1_ready), 4);
     mbar_init(smem_u32(mid_done), 2 * NSW);
@@ -584,19 +584,16 @@ __global__ void __launch_bounds__(cta_threads(NSW), 1)
     }
   } else if (warp == MMAW || warp == MMAW2) {
     // ------------------------------------------------------------ MMA issue
-    // A tcgen05.mma takes its issuing thread tens of cycles (about 40 ns for
-    // the N=64 S steps), which makes MMA issue the per-tile limit.
-    // - 128-row tiles (NSW = 4): one issuing thread per softmax set (warp
-    //   MMAW + X issues set X's tiles X, X+2, ...), so neither set's chain
-    //   (S -> softmax -> P.V -> next S) waits behind the other's P
-    //   (measured: 37.6 -> 36.7 us at 128 rows).
-    // - Fewer rows: one thread issues both sets in tile order, S(i+1) ahead
-    //   of P.V(i); with two issuers these shapes were 3-7% slower, the two
-    //   chains contending for the tensor pipe.
-    // tcgen05.commit tracks the issuing thread's own MMAs.
-    constexpr bool kSplitIssue = NSW == 4;
-    const int X = warp - MMAW;  // split issue: the set this thread issues
-    if (lane == 0 && ntot > 0 && (kSplitIssue || warp == MMAW)) {
+    // Two issuing threads, split by role: warp MMAW issues every S, warp
+    // MMAW2 every P.V, each in tile order. A tcgen05.mma takes its issuing
+    // thread tens of cycles (about 40 ns at these shapes), and a
+    // tcgen05.commit tracks every earlier MMA of its thread: with one thread
+    // issuing both, a set's next S waited for its P.V to be issued and then
+    // to complete. Split by role, S(i) goes out as soon as tile i has landed
+    // and the softmax of tile i-2 (same set) has read its S buffer, and its
+    // commit waits for S MMAs only. (One issuer per softmax set instead was
+    // measured 3-7% slower than one thread for both at 32 rows.)
+    if (lane == 0 && ntot > 0) {
       constexpr uint32_t idq = tc::idesc_bf16(128, 64, false, false);
       constexpr uint32_t idp = tc::idesc_bf16(128, TD, false, true);
       const uint32_t rb = smem_u32(ring);
@@ -648,10 +645,17 @@ __global__ void __launch_bounds__(cta_threads(NSW), 1)
         tc::commit(smem_u32(&o_done[i & 1]));
       };
       bool ok = mbar_wait_abortable(smem_u32(q_ready), 0, abort_flag, a.status, 3u);
-      if constexpr (kSplitIssue) {
-        for (int i = X; ok && i < ntot; i += 2) {
-          // S(i): the tile has landed, and the set's S buffer is free (its
-          // previous reader arrived on p_ready before this thread's last P.V)
+      if (warp == MMAW) {
+        // every S, in tile order: tile i landed, and its set's S buffer free
+        // (the softmax of tile i-2 arrived on p_ready after reading it). The
+        // softmax of tile i+2 cannot arrive before S(i+2) is issued, so the
+        // phase waited for is never overtaken.
+        for (int i = 0; ok && i < ntot; ++i) {
+          if (i >= 2 && !mbar_spin_abortable(smem_u32(&p_ready[i & 1]), ((i - 2) >> 1) & 1,
+                                             abort_flag, a.status, 6u)) {
+            ok = false;
+            break;
+          }
           if (!mbar_spin_abortable(smem_u32(&full[rs(i)]), rp(i), abort_flag, a.status, 5u)) {
             ok = false;
             break;
@@ -665,40 +669,14 @@ __global__ void __launch_bounds__(cta_threads(NSW), 1)
           }
           tc::fence_after();
           issue_qk(i);
-          // p_ready also says the set has read out its previous segment's O,
-          // so the first P.V of a segment may overwrite it
-          if (!mbar_spin_abortable(smem_u32(&p_ready[X]), (i >> 1) & 1, abort_flag, a.status, 6u)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after();
-          issue_pv(i);
         }
       } else {
-        ok = ok && mbar_spin_abortable(smem_u32(&full[rs(0)]), rp(0), abort_flag, a.status, 4u);
-        tc::fence_after();
-        if (ok) issue_qk(0);
+        // every P.V, in tile order, once the softmax of the tile has written
+        // P; p_ready also says the set has read out its previous segment's O,
+        // so the first P.V of a segment may overwrite it. The stage is
+        // released after its P.V: its S had completed before the softmax
+        // could write P.
         for (int i = 0; ok && i < ntot; ++i) {
-          // S buffer of unit i+1's set is free: its previous reader (softmax of
-          // unit i-1) arrived on p_ready before PV(i-1) was issued
-          if (i + 1 < ntot) {
-            if (!mbar_spin_abortable(smem_u32(&full[rs(i + 1)]), rp(i + 1), abort_flag, a.status,
-                                     5u)) {
-              ok = false;
-              break;
-            }
-            if (seg_of(i + 1) == 1 && !q1_seen) {
-              if (!mbar_wait_abortable(smem_u32(q1_ready), 0, abort_flag, a.status, 7u)) {
-                ok = false;
-                break;
-              }
-              tc::fence_after();
-              q1_seen = true;
-            }
-            issue_qk(i + 1);
-          }
-          // p_ready also says the set has read out its previous segment's O, so
-          // the first P.V of a segment may overwrite it
           if (!mbar_spin_abortable(smem_u32(&p_ready[i & 1]), (i >> 1) & 1, abort_flag, a.status,
                                    6u)) {
             ok = false;
