@@ -145,8 +145,9 @@ int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
 /* Bytes of workspace that score/select/attend/verify calls with this shape
  * need, for selections of up to kmax blocks over up to nb_max blocks. The
  * first 256 bytes hold the device status word; after it come three arrays
- * of per-(b, h) words, one 128-byte line each (scoring and attention
- * counts, a merge claim word), then scores, pool rows and split partials. The whole workspace
+ * of per-(b, h) words, one 128-byte line each (the scoring count; the
+ * attention's count of published partials and its merge tickets; a merge
+ * claim word), then scores, pool rows and split partials. The whole workspace
  * must be zero before its first use (allocate it zeroed). Every call that
  * completes returns the per-(b, h) words to zero; the status word keeps its
  * flags until sv_clear_status. A call that raised SV_FLAG_WAIT_TIMEOUT may
