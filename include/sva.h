@@ -69,6 +69,8 @@ typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
 #define SV_FLAG_BAD_BLOCK_INDEX 0x1u  /* selected block index outside [0, NB)  */
 #define SV_FLAG_BAD_PAGE 0x2u         /* block_table entry outside [0, pages)  */
 #define SV_FLAG_WAIT_TIMEOUT 0x4u     /* a pipeline wait gave up (never hangs) */
+#define SV_FLAG_STALE_WORKSPACE 0x8u  /* a per-(b, h) merge word held a count left by an
+                                         earlier call (sv_reset_workspace repairs it) */
 
 /* Problem shape. Stacked query rows per KV head: R = T * (Hq / Hkv). */
 typedef struct {
@@ -152,7 +154,10 @@ int sv_budget_blocks(const sv_budget* budget, int ctx, int nb);
  * completes returns the per-(b, h) words to zero; the status word keeps its
  * flags until sv_clear_status. A call that raised SV_FLAG_WAIT_TIMEOUT may
  * leave those words non-zero: call sv_reset_workspace before the workspace
- * is used again. Returns 0 on an invalid shape. Host only. */
+ * is used again. A call that finds a merge ticket beyond its pair's count
+ * (a word left non-zero) raises SV_FLAG_STALE_WORKSPACE and leaves that
+ * pair's output unwritten; the same reset repairs it. Returns 0 on an
+ * invalid shape. Host only. */
 size_t sv_workspace_bytes(const sv_shape* shape, int nb_max, int kmax);
 
 /* Zero the workspace status word (async on stream). */

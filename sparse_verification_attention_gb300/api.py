@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libsva.so")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE, SV_ERR_CUDA, \
     SV_ERR_DEVICE_FAULT = range(6)
 SV_BF16, SV_F32 = 0, 1
-SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT = 1, 2, 4
+SV_FLAG_BAD_BLOCK_INDEX, SV_FLAG_BAD_PAGE, SV_FLAG_WAIT_TIMEOUT, SV_FLAG_STALE_WORKSPACE = 1, 2, 4, 8
 
 SV_PATH_CUDA_CORES, SV_PATH_MMA_SYNC, SV_PATH_TCGEN05 = 0, 1, 2
 ABI_VERSION = 4  # SV_ABI_VERSION the structures below match

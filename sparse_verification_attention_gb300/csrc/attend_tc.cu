@@ -577,7 +577,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       unsigned* w = a.counters + sp.pair[0] * kPairWords;
       if (ticketed) {
         arrive_release(w);
-        if (atomicAdd(w + kTicketWord, 1u) + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
+        const unsigned t = atomicAdd(w + kTicketWord, 1u);
+        if (t + 1u == (unsigned)sp.nseg[0]) pair_done[0] = 1;
+        else if (t >= (unsigned)sp.nseg[0]) atomicOr(a.status, SV_FLAG_STALE_WORKSPACE);
       } else if ((arrive_acq_rel(w) & 0xFFFFu) + 1u == (unsigned)sp.nseg[0]) {
         pair_done[0] = 1;
       }
@@ -882,9 +884,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
             make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
       *reinterpret_cast<float2*>(pml + 2 * row) = make_float2(m_run, l_run);
     }
-    // holding the pair's last ticket: merge with this partial kept here
-    if (threadIdx.x == 0 && ticketed && final_ticket + 1u == (unsigned)sp.nseg[jf])
-      pair_done[jf] = 2;
+    // holding the pair's last ticket: merge with this partial kept here; a
+    // ticket past the pair's count means a word left by an earlier call
+    if (threadIdx.x == 0 && ticketed) {
+      if (final_ticket + 1u == (unsigned)sp.nseg[jf]) pair_done[jf] = 2;
+      else if (final_ticket >= (unsigned)sp.nseg[jf]) atomicOr(a.status, SV_FLAG_STALE_WORKSPACE);
+    }
     __syncthreads();
     // the folded partial stays in shared memory for a cluster merge or for
     // this CTA's own merge

@@ -744,6 +744,36 @@ def test_reset_workspace_repairs_stale_words():
     assert torch.equal(again, clean)
 
 
+def test_stale_merge_ticket_is_flagged():
+    """A merge ticket word left non-zero by an earlier call (planted here by
+    the host; nothing is made to fail on the device) gives no segment the
+    pair's last ticket. The kernel flags it instead of leaving the pair's
+    output silently unwritten, and sv_reset_workspace repairs the
+    workspace."""
+    wl = small_wl(B=4, Hq=32, Hkv=8, ctx=64 * 60, budget=W.Budget(W.BUDGET_FIXED, 20, 0, 0, 0, 0, 0))
+    x = W.make_layer(wl)
+    xd = x.to("cuda")
+    st = api.LayerState(wl, xd)
+    plan = api.sv_attend_plan(st.shape, st.kv, st.k)
+    assert plan.path == api.SV_PATH_TCGEN05 and plan.streamk == 1 and plan.cluster == 0
+    clean = st.verify().clone()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    pairs = wl.B * wl.Hkv
+    ticket = 256 + pairs * 128 + 3 * 128 + 4  # pair 3's attention line, merge-ticket word
+    st.ws[ticket:ticket + 4] = torch.tensor([0x5A, 0x5A, 0, 0], dtype=torch.uint8, device="cuda")
+    st.verify()
+    torch.cuda.synchronize()
+    flags = int(st.ws[:4].view(torch.int32).item())
+    assert flags & api.SV_FLAG_STALE_WORKSPACE, hex(flags)
+    nb_max = st.x.block_table.shape[1]
+    api.sv_reset_workspace(st.shape, nb_max, max(st.kmax, wl.NB, 1), st.ws)
+    again = st.verify()
+    torch.cuda.synchronize()
+    assert api.sv_read_status(st.ws) == 0
+    assert torch.equal(again, clean)
+
+
 def test_reuse_guard_on_device():
     """A reuse layer may read a slot only after a computing layer wrote it for
     the same context and budget: the matching reuse attends over it, while a
