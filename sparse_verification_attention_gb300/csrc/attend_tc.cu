@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     }
   }
 
-  // per-thread results of the final segment for the epilogue (softmax threads)
+  // per-thread softmax state (m, l of the final segment for the epilogue),
+  // and a mid-stream segment's O row on its way to the workspace
   float o_row[TD];
   float m_run = -INFINITY, l_run = 0.f;
   // Narrow merges (the last CTA of a pair merges every row) go by tickets: a
@@ -806,28 +807,32 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
       // round trip overlaps the read-out and staging below
       if (ticketed && threadIdx.x == 0 && j == sp.n - 1)
         final_ticket = atomicAdd(&a.counters[sp.pair[j] * kPairWords + kTicketWord], 1u);
-      // read out this set's O of segment j (its last P.V must have finished)
+      // this set's O of segment j is complete once its last P.V is (the final
+      // segment's O stays in TMEM: the epilogue folds it from there)
       bool fin = ok && kseg > 0;
       if (fin)
         fin = mbar_wait_abortable(smem_u32(&o_done[X]), (k - 1) & 1, abort_flag, a.status, 11u);
-      if (__all_sync(0xffffffffu, fin)) {
-        tc::fence_after();
-#pragma unroll
-        for (int cc = 0; cc < TD / 32; ++cc) {
-          uint32_t ov[32];
-          tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
-          tc::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o_row[32 * cc + e] = __uint_as_float(ov[e]);
-        }
-      } else {
+      const bool ofin = __all_sync(0xffffffffu, fin);
+      if (!ofin) {
         if (kseg > 0 || !ok) atomicOr(a.status, SV_FLAG_WAIT_TIMEOUT);
-#pragma unroll
-        for (int e = 0; e < TD; ++e) o_row[e] = 0.f;
-        m_run = -INFINITY;
+        m_run = -INFINITY;  // weight 0 in every fold: its O is never read
         l_run = 0.f;
       }
       if (j + 1 < sp.n) {
+        if (ofin) {
+          tc::fence_after();
+#pragma unroll
+          for (int cc = 0; cc < TD / 32; ++cc) {
+            uint32_t ov[32];
+            tc::ld32(tmem + lane_base + colO + 32 * cc, ov);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o_row[32 * cc + e] = __uint_as_float(ov[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < TD; ++e) o_row[e] = 0.f;
+        }
         // Mid-stream segment: this set's partial goes straight to the
         // workspace (set A in the segment's slot, set B in the pair's extra
         // slot nseg); the producer warp counts its arrival once every warp
@@ -847,23 +852,17 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(mid_done));
       }
     }
-    if (!active) {
-#pragma unroll
-      for (int e = 0; e < TD; ++e) o_row[e] = 0.f;
-    }
   }
 
   tc::fence_before();
-  __syncthreads();  // all TMEM reads and MMAs done; the ring is idle
-  if (warp == MMAW) {
-    tc::fence_after();
-    tc::dealloc(tmem, kTmemCols);
-  }
+  __syncthreads();  // every MMA done (each set waited for its last P.V); the ring is idle
 
   // ---------------------------------------------------------------- epilogue
-  // The final segment: stage both sets' (o, m, l) for the kRows real lanes and
-  // fold set B into set A with log-sum-exp weights (row r of set X staged at
-  // X*kRows + r).
+  // The final segment: both sets' (m, l) meet in shared memory (row r of set
+  // X at X*kRows + r), and their O rows are folded with log-sum-exp weights
+  // straight out of TMEM: the warp of lane quarter q in set X folds columns
+  // [64X, 64X+64) of rows 32q..32q+31 (a warp reaches every column of its
+  // lane quarter, so it reads both sets' O).
   constexpr int NT = C::kThreads;
   constexpr int OST = C::kOst;
   constexpr int KR = C::kRows;
@@ -878,10 +877,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
     float2* own_ml = reinterpret_cast<float2*>(a.part_ml) + slot;
     if (warp < 8 && (warp & 3) < NSW) {
       const int row = (warp >> 2) * KR + 32 * (warp & 3) + lane;
-#pragma unroll
-      for (int c = 0; c < TD; c += 4)
-        *reinterpret_cast<float4*>(po + row * OST + c) =
-            make_float4(o_row[c], o_row[c + 1], o_row[c + 2], o_row[c + 3]);
       *reinterpret_cast<float2*>(pml + 2 * row) = make_float2(m_run, l_run);
     }
     // holding the pair's last ticket: merge with this partial kept here; a
@@ -909,30 +904,32 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         own_ml[rr] = make_float2(M, wa * ma.y + wb * mb.y);
     }
     __syncthreads();
-    if (keep) {
-      // folded rows in place of set A's staged rows
-      for (int idx = threadIdx.x; idx < KR * (TD / 4); idx += NT) {
-        const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
-        const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
-        float4* pa = reinterpret_cast<float4*>(po + rr * OST + c4);
-        const float4 oa = *pa;
-        const float4 ob = *reinterpret_cast<const float4*>(po + (KR + rr) * OST + c4);
-        *pa = make_float4(w.x * oa.x + w.y * ob.x, w.x * oa.y + w.y * ob.y,
-                          w.x * oa.z + w.y * ob.z, w.x * oa.w + w.y * ob.w);
+    if (warp < 8 && (warp & 3) < NSW) {
+      // a set whose weight is 0 (no tile in this segment, or a wait gave up)
+      // has an O that is never read: select, not multiply
+      tc::fence_after();
+      const int xs = warp >> 2, q4 = warp & 3, rr = 32 * q4 + lane;
+      const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
+      const uint32_t lb = (uint32_t)(32 * q4) << 16;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 64 * xs + 32 * hh;
+        uint32_t oa[32], ob[32];
+        tc::ld32(tmem + lb + col_o(0) + c0, oa);
+        tc::ld32(tmem + lb + col_o(1) + c0, ob);
+        tc::wait_ld();
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          f[e] = (w.x != 0.f ? w.x * __uint_as_float(oa[e]) : 0.f) +
+                 (w.y != 0.f ? w.y * __uint_as_float(ob[e]) : 0.f);
+        float* dst = keep ? po + (size_t)rr * OST + c0 : own_o + (size_t)rr * TD + c0;
+        if (keep || rr < a.rpad) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        }
       }
-    }
-    // folded rows straight to the workspace (rows past kRows are zero padding)
-    for (int idx = threadIdx.x; !keep && idx < a.rpad * (TD / 4); idx += NT) {
-      const int rr = idx / (TD / 4), c4 = (idx % (TD / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rr < KR) {
-        const float2 w = *reinterpret_cast<const float2*>(pw + 2 * rr);
-        const float4 oa = *reinterpret_cast<const float4*>(po + rr * OST + c4);
-        const float4 ob = *reinterpret_cast<const float4*>(po + (KR + rr) * OST + c4);
-        v = make_float4(w.x * oa.x + w.y * ob.x, w.x * oa.y + w.y * ob.y, w.x * oa.z + w.y * ob.z,
-                        w.x * oa.w + w.y * ob.w);
-      }
-      *reinterpret_cast<float4*>(own_o + (size_t)rr * TD + c4) = v;
     }
     // CTA barrier, then one thread's acquire-release arrival publishes
     // every thread's partial writes (the barrier orders them before it);
@@ -947,7 +944,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
         pair_done[jf] = 1;
     }
   }
-  __syncthreads();
+  tc::fence_before();
+  __syncthreads();  // every TMEM read done
+  if (warp == MMAW) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
+  }
 
   if (a.cluster_merge) {
     // ------------------------------------------------------- cluster merge
