@@ -43,7 +43,9 @@
 //     TMEM loads/stores are taken by all lanes) and sum.
 //   * partials and merge: a segment that ends mid-stream writes each set's
 //     unnormalised (o, m, l) rows from registers; the final segment folds
-//     the two sets in shared memory. Cluster plans then merge the pair's
+//     the two sets straight out of TMEM (only (m, l) goes through shared
+//     memory; each warp folds half the columns of its lane quarter's rows,
+//     reading both sets' O). Cluster plans then merge the pair's
 //     folded rows through distributed shared memory. Otherwise partials are
 //     published in the workspace with an acquire-release arrival. When a
 //     pair's merge is small, every segment takes a ticket as its stream ends
