@@ -596,6 +596,8 @@ def run_gpu(args, wl, rank, world, dist):
                 "ms_per_step": of["ms_per_step"], "budget_blocks": ok_,
                 "step_bytes": of["step_bytes"], "step_frac": of["step_frac"],
                 "attend_us": of["attend_ms"] * 1e3, "attend_frac": of["attend_frac"],
+                "attend_bytes": of["attend_bytes"],
+                "attend_traffic": traffic_from_profile(owl.name),  # ncu DRAM bytes, or None
                 "e2e": {"value": of["e2e"]["value"], "ms_per_step": of["e2e"]["ms_per_step"]},
                 "config": config_of(owl, ok_)}
         per_config["tiny_f32"] = {"parity_only": True,
