@@ -97,8 +97,9 @@ struct TcCfg {
   static constexpr int kQBytes = 2 * kQBox;       // the first segment's Q operand
   static constexpr int kRingOff = kQBytes;
   static constexpr int kOst = TD + 4;
-  // staging of the final segment: both sets' o [2 kRows][kOst], their
-  // (m, l) [2 kRows], the fold weights [kRows] and the folded (M, L) [kRows]
+  // epilogue area of the final segment: its folded o [kRows][kOst] (room is
+  // kept for 2 kRows rows), both sets' (m, l) [2 kRows], the fold weights
+  // [kRows] and the folded (M, L) [kRows]
   static constexpr int kMergeBytes = (2 * kRows * kOst + 4 * kRows * 2) * 4;
   static constexpr int kRingRaw = NS * kStageBytes;
   static constexpr int kRing = r1024(kMergeBytes > kRingRaw ? kMergeBytes : kRingRaw);
@@ -868,7 +869,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
   constexpr int NT = C::kThreads;
   constexpr int OST = C::kOst;
   constexpr int KR = C::kRows;
-  float* po = reinterpret_cast<float*>(ring);   // [2*KR][OST]
+  float* po = reinterpret_cast<float*>(ring);   // folded rows [KR][OST] (room for 2*KR)
   float* pml = po + (size_t)2 * KR * OST;       // [2*KR][2], then [KR][2] weights
   float* cml = pml + (size_t)6 * KR;            // [KR][2]: folded (M, L), cluster merge
   const int jf = sp.n - 1;  // final segment (none when the CTA has no work)
